@@ -1,0 +1,258 @@
+"""Float64 CPU oracle of the dense prefill forward pass (test infrastructure only).
+
+Each function names the passage it restates.  "forward.rs" is the page
+docs.rs memra-engine 0.130.0 src/forward.rs (`impl Model`, `Model::forward`);
+"v3/model.rs" is the page docs.rs needle-core v3/model.rs.
+
+Readings taken where the pages leave a step open (they show the kernels' call
+sites, not their bodies):
+  * RMSNorm: y = x / sqrt(mean(x^2) + eps) * w (eps inside the root, plain
+    multiply by w) -- the reading of the llama.cpp qwen3 graph that forward.rs
+    says it matches.
+  * NeoX RoPE: pairs (i, i + n_dims/2) for i < n_dims/2, theta_i =
+    base^(-2i/n_dims), angle = pos * theta_i, dims >= n_dims unchanged.  With
+    n_dims == head_dim this is exactly the v3/model.rs table.
+  * GQA: query head i reads kv head i // (n_head / n_head_kv).
+  * Causal: key s is visible to query t iff s <= t.
+  * SwiGLU (`ffn_act`): act = silu(gate) * up, silu(x) = x / (1 + e^-x).
+  * bf16-operand mode: matrices are rounded to bf16 once; every GEMM input
+    activation (normed h, attention output, SwiGLU act, final normed x) and the
+    q/k/v handed to attention are rounded to bf16 (nearest, ties to even); all
+    sums and the residual stream stay in float64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F64 = np.float64
+
+
+# --------------------------------------------------------------------------------------
+# bf16 rounding (bf16-operand mode)
+# --------------------------------------------------------------------------------------
+def round_bf16(x) -> np.ndarray:
+    """Round to the nearest bfloat16 value (8 significant bits), ties to even.
+
+    Written out on the float64 value: x = m * 2^e with m in [0.5, 1); keep
+    round-half-even(m * 2^8) / 2^8.  Finite normal-range inputs only (the
+    forward pass never leaves that range)."""
+    x = np.asarray(x, dtype=F64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+# --------------------------------------------------------------------------------------
+# Ops
+# --------------------------------------------------------------------------------------
+def rms_norm(x, w, eps: float) -> np.ndarray:
+    """forward.rs, Model::forward, `e.rms_norm(x, w, out, ncols, nrows, eps)`:
+    each row (last axis, length ncols) is divided by sqrt(mean(row^2) + eps)
+    and multiplied elementwise by w."""
+    x = np.asarray(x, dtype=F64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(w, dtype=F64)
+
+
+def qk_norm(x, w, head_dim: int, eps: float) -> np.ndarray:
+    """forward.rs, Model::forward, the QK-norm comment: the token-major buffer
+    [T, n_heads*head_dim] is n_heads*T contiguous rows of head_dim, and
+    `rms_norm(ncols=head_dim, nrows=n_heads*T)` normalises each row with the
+    shared scale vector w[head_dim]."""
+    x = np.asarray(x, dtype=F64)
+    return rms_norm(x.reshape(-1, head_dim), w, eps).reshape(x.shape)
+
+
+def rope_angles(pos, n_dims: int, freq_base: float) -> np.ndarray:
+    """Angle table [len(pos), n_dims/2]: angle[t, i] = pos[t] * base^(-2i/n_dims)
+    (v3/model.rs `V3Model::rope`: freq = 1/theta^(2i/dims), angle = t*freq; the
+    forward.rs call passes rope_dim_count as n_dims and freq_scale 1.0)."""
+    i = np.arange(n_dims // 2, dtype=F64)
+    theta = np.power(F64(freq_base), -2.0 * i / n_dims)
+    return np.asarray(pos, dtype=F64)[:, None] * theta[None, :]
+
+
+def rope_neox(x, pos, n_heads: int, head_dim: int, n_dims: int, freq_base: float) -> np.ndarray:
+    """forward.rs, Model::forward, `e.rope_neox(&mut q, &pos_d, head_dim,
+    rope_dim_count, n_head, t, freq_base, 1.0)`: rotate, for every (token,
+    head) row of head_dim, the pairs (i, i + n_dims/2), i < n_dims/2, by
+    angle[token, i]; dims n_dims..head_dim pass through."""
+    x = np.asarray(x, dtype=F64)
+    T = x.shape[0]
+    y = x.reshape(T, n_heads, head_dim).copy()
+    half = n_dims // 2
+    ang = rope_angles(pos, n_dims, freq_base)
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    a = y[:, :, :half].copy()
+    b = y[:, :, half:n_dims].copy()
+    y[:, :, :half] = a * c - b * s
+    y[:, :, half:n_dims] = a * s + b * c
+    return y.reshape(x.shape)
+
+
+def sdpa_causal_gqa(q, k, v, n_head: int, n_head_kv: int, head_dim: int, scale: float,
+                    rows=None) -> np.ndarray:
+    """forward.rs, Model::forward, `e.sdpa_naive(q, k, v, attn, head_dim,
+    n_head, n_head_kv, t, t, scale, true)` with scale = 1/sqrt(head_dim):
+    out[t, head i] = sum_{s <= t} softmax_s(q[t,i] . k[s,j] * scale) v[s,j],
+    j = i // (n_head / n_head_kv).  q [T, n_head*hd], k/v [T, n_head_kv*hd].
+
+    `rows` (optional) restricts the output to those query positions; each row
+    is computed from the keys 0..row only, exactly as in the full result."""
+    q = np.asarray(q, dtype=F64)
+    k = np.asarray(k, dtype=F64)
+    v = np.asarray(v, dtype=F64)
+    T = q.shape[0]
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    group = n_head // n_head_kv
+    out = np.zeros((len(rows), n_head * head_dim), dtype=F64)
+    n_keys = int(rows.max()) + 1 if len(rows) else 0
+    key_idx = np.arange(n_keys)
+    hidden = key_idx[None, :] > rows[:, None]           # key s not visible to query t
+    for i in range(n_head):
+        j = i // group
+        qi = q[rows, i * head_dim:(i + 1) * head_dim]
+        kj = k[:n_keys, j * head_dim:(j + 1) * head_dim]
+        vj = v[:n_keys, j * head_dim:(j + 1) * head_dim]
+        s = (qi @ kj.T) * scale
+        s[hidden] = -np.inf
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p /= p.sum(axis=1, keepdims=True)
+        out[:, i * head_dim:(i + 1) * head_dim] = p @ vj
+    return out
+
+
+def silu(x) -> np.ndarray:
+    x = np.asarray(x, dtype=F64)
+    return x / (1.0 + np.exp(-x))
+
+
+def swiglu(gate, up) -> np.ndarray:
+    """forward.rs, Model::forward, `ffn_act(e, cfg, &gate, &up, &mut act, t*n_ff)`
+    (the dense arm; the T-parallel page calls the same step `silu_mul(g, u)`):
+    act = silu(gate) * up elementwise."""
+    return silu(gate) * np.asarray(up, dtype=F64)
+
+
+def linear(x, W) -> np.ndarray:
+    """forward.rs, Model::forward, `e.matmul(&w, &x, t)`: W is [out_features,
+    in_features] and x is token-major [T, in_features]; y = x W^T [T, out]."""
+    return np.asarray(x, dtype=F64) @ np.asarray(W, dtype=F64).T
+
+
+# --------------------------------------------------------------------------------------
+# Whole forward
+# --------------------------------------------------------------------------------------
+def _mats(w: dict, bf16: bool) -> dict:
+    out = {}
+    for name, a in w.items():
+        a = np.asarray(a, dtype=F64)
+        out[name] = round_bf16(a) if (bf16 and a.ndim == 2) else a
+    return out
+
+
+def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False) -> np.ndarray:
+    """One decoder layer, forward.rs `Model::forward` loop body, on the residual
+    stream x [T, n_embd]; returns the new x."""
+    op = round_bf16 if bf16_operands else (lambda a: a)
+    L = _mats(lw, bf16_operands)
+    d, h, g, hd = cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim
+    eps = cfg.rms_eps
+    scale = 1.0 / np.sqrt(F64(hd))
+    # attention block
+    hN = op(rms_norm(x, L["attn_norm"], eps))
+    q = linear(hN, L["wq"])
+    k = linear(hN, L["wk"])
+    v = linear(hN, L["wv"])
+    q = qk_norm(q, L["q_norm"], hd, eps)
+    k = qk_norm(k, L["k_norm"], hd, eps)
+    q = op(rope_neox(q, pos, h, hd, cfg.rope_dim_count, cfg.rope_freq_base))
+    k = op(rope_neox(k, pos, g, hd, cfg.rope_dim_count, cfg.rope_freq_base))
+    v = op(v)
+    attn = op(sdpa_causal_gqa(q, k, v, h, g, hd, scale))
+    x1 = x + linear(attn, L["wo"])
+    # ffn block (dense SwiGLU)
+    z = op(rms_norm(x1, L["ffn_norm"], eps))
+    act = op(swiglu(linear(z, L["w_gate"]), linear(z, L["w_up"])))
+    return x1 + linear(act, L["w_down"])
+
+
+def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidden: bool = False,
+            layer_source=None):
+    """forward.rs `Model::forward`: logits [T, n_vocab] for `tokens`, positions 0..T-1.
+
+    weights: {"tok_embd" [V,d], "layers": [dict per layer], "output_norm" [d],
+    "output" [V,d]}.  `layer_source(l)` may replace weights["layers"][l] (lets a
+    caller stream layers of a large model).  With return_hidden, also returns
+    hidden [n_layer+1, T, d]: the residual stream entering each layer, then the
+    stream entering output_norm."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    T = tokens.shape[0]
+    op = round_bf16 if bf16_operands else (lambda a: a)
+    emb = np.asarray(weights["tok_embd"], dtype=F64)
+    if bf16_operands:
+        emb = round_bf16(emb[tokens])
+        x = emb
+    else:
+        x = emb[tokens]
+    pos = np.arange(T)
+    hidden = [x.copy()] if return_hidden else None
+    for l in range(cfg.n_layer):
+        lw = layer_source(l) if layer_source is not None else weights["layers"][l]
+        x = forward_layer(cfg, lw, x, pos, bf16_operands)
+        if return_hidden:
+            hidden.append(x.copy())
+    hn = op(rms_norm(x, np.asarray(weights["output_norm"], dtype=F64), cfg.rms_eps))
+    W_out = np.asarray(weights["output"], dtype=F64)
+    if bf16_operands:
+        W_out = round_bf16(W_out)
+    logits = linear(hn, W_out)
+    if return_hidden:
+        return logits, np.stack(hidden)
+    return logits
+
+
+# --------------------------------------------------------------------------------------
+# Logit helpers (forward.rs `argmax`, `top2`, `prime_gate_verdict`)
+# --------------------------------------------------------------------------------------
+def argmax(logits) -> int:
+    """First index holding the maximum (a strict `>` scan keeps the lowest index on ties)."""
+    best, bv = 0, -np.inf
+    for i, v in enumerate(np.asarray(logits).tolist()):
+        if v > bv:
+            bv, best = v, i
+    return best
+
+
+def top2(logits):
+    """(i1, v1, i2, v2): the largest and second-largest entries, first index on ties."""
+    i1, v1, i2, v2 = 0, -np.inf, 0, -np.inf
+    for i, v in enumerate(np.asarray(logits).tolist()):
+        if v > v1:
+            i2, v2 = i1, v1
+            i1, v1 = i, v
+        elif v > v2:
+            i2, v2 = i, v
+    return i1, v1, i2, v2
+
+
+def prime_gate_verdict(reference, candidate, maxdiff_bound: float = 8.0, margin_bound: float = 1.0):
+    """Classify two logit vectors: "structured" if the max |diff| is non-finite or
+    above maxdiff_bound; else "match" if the argmaxes agree; else "near_tie_flip"
+    if the reference's top1-top2 margin is within margin_bound; else
+    "structured".  Returns (class, ref_argmax, cand_argmax, ref_margin, maxdiff)."""
+    t1, tv1, _, tv2 = top2(reference)
+    b1, _, _, _ = top2(candidate)
+    diff = np.abs(np.asarray(reference, dtype=F64) - np.asarray(candidate, dtype=F64))
+    maxdiff = float(diff.max()) if diff.size else 0.0
+    margin = tv1 - tv2
+    if not np.isfinite(maxdiff) or maxdiff > maxdiff_bound:
+        cls = "structured"
+    elif t1 == b1:
+        cls = "match"
+    elif margin <= margin_bound:
+        cls = "near_tie_flip"
+    else:
+        cls = "structured"
+    return cls, t1, b1, margin, maxdiff
