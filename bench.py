@@ -1,0 +1,342 @@
+"""Prefill throughput benchmark.
+
+One step = one whole prefill forward pass (embed -> every decoder layer ->
+output norm -> lm_head logits [T, n_vocab] f32) of the 8B-shape dense decoder
+over T = 4096 synthetic tokens, through the C ABI.  Weights are random-init
+(seeded N(0, 0.02), norm scales 1 + N(0, 0.1)) with that architecture; tokens
+are seeded uniform ids.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dtp|reference]
+
+N > 1 runs under torchrun as independent replicas (one sequence per rank, no
+collective on the data path); value = tokens of all ranks / max rank time.
+`--impl reference` times the CPU oracle (float64 numpy) on a bounded sample
+of the same workload, on the host cores, rank 0 only.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "prefill tokens/s and TFLOP/s vs GB300 peak (1 GPU), logits vs CPU oracle"
+UNIT = "tokens/s"
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+class OracleSample:
+    """A bounded sample of the workload for the float64 oracle, scaled to the whole
+    pass: one decoder layer over the first S_l tokens (t_layer) and the lm_head
+    over S_h rows x a V_s-row slice of the vocabulary (t_head);
+    tokens/s = T / (n_layer * t_layer * T/S_l + t_head * (T/S_h) * (V/V_s))."""
+
+    def __init__(self, cfg, s_layer: int = 1024, s_head: int = 512, v_slice: int = 8192):
+        self.cfg = cfg
+        self.bf16 = cfg.precision == "bf16"
+        self.sl = min(cfg.T, s_layer)
+        self.sh = min(cfg.T, s_head)
+        self.vs = min(cfg.n_vocab, v_slice)
+        self.lw = synth.layer_weights(cfg, 0)
+        toks = synth.tokens(cfg)[:self.sl]
+        self.x = synth.tok_embd(cfg)[toks].astype(np.float64)
+        self.W = synth.normal(0, synth.TID_OUTPUT, (self.vs, cfg.n_embd), std=0.02)
+        self.hn = synth.normal(0, 99, (self.sh, cfg.n_embd))
+
+    def run(self) -> dict:
+        import oracle
+
+        cfg, T = self.cfg, self.cfg.T
+        t0 = time.perf_counter()
+        oracle.forward_layer(cfg, self.lw, self.x, np.arange(self.sl), bf16_operands=self.bf16)
+        t_layer = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        if self.bf16:
+            oracle.linear(oracle.round_bf16(self.hn), oracle.round_bf16(self.W))
+        else:
+            oracle.linear(self.hn, self.W)
+        t_head = time.perf_counter() - t0
+        total = (cfg.n_layer * t_layer * T / self.sl
+                 + t_head * (T / self.sh) * (cfg.n_vocab / self.vs))
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        return {"value": T / total, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": (f"float64 numpy oracle ({'bf16-operand mode' if self.bf16 else 'exact'},"
+                           f" BLAS on all {cores} host cores) on {cfg.name}: 1 decoder layer over "
+                           f"the first {self.sl} tokens ({t_layer:.2f} s) + lm_head over "
+                           f"{self.sh} rows x {self.vs} vocab rows ({t_head:.2f} s), scaled to "
+                           f"{cfg.n_layer} layers x {T} tokens and the full {cfg.n_vocab} vocab")}
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="dtp", choices=["dtp", "reference"])
+    ap.add_argument("--workload", default="qwen3-8b-shape", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = synth.CONFIGS[args.workload]
+    config = {"workload": cfg.name, "T": cfg.T, "n_layer": cfg.n_layer, "n_embd": cfg.n_embd,
+              "n_head": cfg.n_head, "n_head_kv": cfg.n_head_kv, "head_dim": cfg.head_dim,
+              "n_ff": cfg.n_ff, "n_vocab": cfg.n_vocab, "sequences_per_gpu": 1,
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+              "l2": "inputs larger than L2 (packed weights exceed 129 MB)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        sampler = OracleSample(cfg)
+        sampler.run()       # one untimed warm-up (BLAS thread pool); more would only repeat it
+        samples = [sampler.run() for _ in range(args.steps)]
+        v = statistics.median(s["value"] for s in samples)
+        cb = dict(samples[0])
+        cb["value"] = v
+        print(json.dumps({"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1000.0 * cfg.T / v, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "impl": "reference", "config": config,
+                          "cpu_baseline": cb,
+                          "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    import torch
+    import dense_transformer_prefill_gb300 as dtp
+
+    dtp.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ------------------------------------------------------------------ setup (untimed)
+    t_setup = time.perf_counter()
+    m = dtp.Model(cfg, device=dev)
+    for l in range(cfg.n_layer):
+        m.load_layer(l, synth.layer_weights(cfg, l))
+    m.load_globals(synth.tok_embd(cfg), synth.output_norm(cfg), synth.output_weight(cfg))
+    toks_np = synth.tokens(cfg, seed=1000 + rank).astype(np.int32)
+    toks = torch.as_tensor(toks_np, device=dev)
+    logits = torch.empty((cfg.T, cfg.n_vocab), dtype=torch.float32, device=dev)
+    m.workspace(cfg.T)
+    setup_s = time.perf_counter() - t_setup
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        m.forward(toks, logits)
+    torch.cuda.synchronize(dev)
+    dtp.check()
+
+    # ------------------------------------------------------------------ timed region
+    kinds = ["gemm_qkv", "attn", "gemm_o", "gemm_gateup", "gemm_down", "gemm_lmhead", "rmsnorm",
+             "embed", "other"]
+    dtp.timer_enable(kinds, capacity=args.steps * (cfg.n_layer + 1) * 2)
+    gpu_index = local_rank
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local_rank])
+        except (ValueError, IndexError):
+            pass
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        n0 = dtp.launch_count()
+        start.record(stream)
+        for _ in range(args.steps):
+            m.forward(toks, logits)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        launches = dtp.launch_count() - n0
+        barrier()
+    dtp.check()
+    ms = start.elapsed_time(end)
+    kstats = {k: dtp.timer_read(k) for k in kinds}
+    dtp.timer_disable()
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * cfg.T * args.steps / (ms / 1000.0)
+
+    # ------------------------------------------------------------------ end to end (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        tok_h = torch.as_tensor(toks_np).pin_memory()
+        log_h = torch.empty((cfg.T, cfg.n_vocab), dtype=torch.float32).pin_memory()
+        ws_h = m.workspace(cfg.T, host=True)
+        for _ in range(2):
+            dtp.fwd_prefill_host(m.c, m.packed, tok_h, log_h, ws_h)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_start.record(stream)
+        for _ in range(args.steps):
+            dtp.fwd_prefill_host(m.c, m.packed, tok_h, log_h, ws_h)
+        e_end.record(stream)
+        torch.cuda.synchronize(dev)
+        dtp.check()
+        ems = e_start.elapsed_time(e_end)
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * cfg.T * args.steps / (ems / 1000.0), "unit": UNIT,
+               "h2d_bytes_per_step": int(tok_h.numel() * 4),
+               "d2h_bytes_per_step": int(log_h.numel() * 4),
+               "path": "dtp_fwd_prefill_host (pinned host tokens in, pinned host logits out)"}
+        del log_h
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    # ------------------------------------------------------------------ roofline
+    peaks = load_peaks()
+    T, d, F = cfg.T, cfg.n_embd, cfg.n_ff
+    gu_n, gu_ms = kstats["gemm_gateup"]
+    gu_flops = 2.0 * T * (2 * F) * d
+    achieved = gu_flops / (gu_ms / gu_n / 1000.0) / 1e12 if gu_n else None
+    peak = peaks["bf16_tflops_sustained"] if cfg.precision == "bf16" else None
+    roofline = {"kernel": "gemm_tc_kernel<256, EPI_SWIGLU> (gate/up projection + SwiGLU)",
+                "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if (achieved and peak) else None,
+                "traffic": None,
+                "flops_per_launch": gu_flops,
+                "peak_source": f"bf16_tflops_sustained of {peaks['source']} peaks",
+                "avg_launch_ms": gu_ms / gu_n if gu_n else None}
+    per_kernel = {}
+    step_flops = 0.0
+    for k, (n, kms) in kstats.items():
+        if n:
+            per_kernel[k] = {"launches_per_step": n / args.steps, "ms_per_step": kms / args.steps}
+    gemm_flops = cfg.gemm_flops()
+    attn_flops = cfg.attn_flops()
+    step_flops = gemm_flops + attn_flops
+    gemm_ms = sum(kstats[k][1] for k in ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down",
+                                         "gemm_lmhead")) / args.steps
+    attn_ms = kstats["attn"][1] / args.steps
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if cfg.precision == "bf16" else "f32",
+        "data": "synthetic (seeded random-init weights of the architecture, uniform token ids)",
+        "config": config, "roofline": roofline,
+        "tflops": {"step": step_flops / (ms_per_step / 1000.0) / 1e12,
+                   "gemm": gemm_flops / (gemm_ms / 1000.0) / 1e12 if gemm_ms else None,
+                   "attn": attn_flops / (attn_ms / 1000.0) / 1e12 if attn_ms else None,
+                   "gemm_frac_of_peak": (gemm_flops / (gemm_ms / 1000.0) / 1e12 / peak)
+                   if (gemm_ms and peak) else None,
+                   "attn_frac_of_peak": (attn_flops / (attn_ms / 1000.0) / 1e12 / peak)
+                   if (attn_ms and peak) else None},
+        "kernels": per_kernel,
+        "clocks": clk.summary(),
+        "gpu_launches": int(launches),
+        "e2e": e2e,
+        "setup_s": setup_s,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = OracleSample(cfg).run()
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

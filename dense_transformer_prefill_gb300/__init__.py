@@ -1,0 +1,38 @@
+"""GB300 (sm_103a) dense-transformer prefill: Python binding of the C-ABI library.
+
+Every step of the forward pass runs in the CUDA kernels of `libdtp.so`; this
+package only marshals arguments (torch tensors are used for device memory and
+streams) and raises `DtpError` on a non-zero status.  There is no CPU fallback:
+importing the binding without the built library raises.
+"""
+from .build import build  # noqa: F401
+from ._binding import (  # noqa: F401
+    DTP_BF16,
+    DTP_F32,
+    DTP_PREC_BF16,
+    DTP_PREC_F32,
+    KERNEL_KINDS,
+    DtpError,
+    Model,
+    check,
+    config_from,
+    fwd_prefill,
+    fwd_prefill_host,
+    last_error,
+    launch_count,
+    linear,
+    lib,
+    pack_globals,
+    pack_layer,
+    packed_size,
+    qk_norm_rope_neox,
+    rms_norm,
+    sdpa_causal_gqa,
+    sdpa_workspace_size,
+    swiglu,
+    timer_disable,
+    timer_enable,
+    timer_read,
+    workspace_size,
+    workspace_size_host,
+)

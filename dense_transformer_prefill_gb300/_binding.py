@@ -1,0 +1,285 @@
+"""ctypes binding of include/dtp.h.  Argument marshalling only: torch tensors
+supply device memory and the current CUDA stream; every computation happens in
+libdtp.so's kernels."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB, build  # noqa: F401
+
+DTP_F32, DTP_BF16 = 0, 1
+DTP_PREC_F32, DTP_PREC_BF16 = 0, 2
+KERNEL_KINDS = {"embed": 0, "rmsnorm": 1, "gemm_qkv": 2, "attn": 3, "gemm_o": 4,
+                "gemm_gateup": 5, "gemm_down": 6, "gemm_lmhead": 7, "other": 8}
+
+c_int, c_float, c_size_t, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+
+class DtpError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"dtp error {code}: {msg}")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_layer", c_int), ("n_embd", c_int), ("n_head", c_int), ("n_head_kv", c_int),
+                ("head_dim", c_int), ("rope_dim_count", c_int), ("n_ff", c_int),
+                ("n_vocab", c_int), ("rope_freq_base", c_float), ("rms_eps", c_float),
+                ("precision", c_int)]
+
+
+class LayerSrc(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo",
+                                       "ffn_norm", "w_gate", "w_up", "w_down")]
+
+
+_lib = None
+_lock = threading.Lock()
+
+_SIGS = {
+    "dtp_last_error": ([], ctypes.c_char_p),
+    "dtp_launch_count": ([c_int], ctypes.c_longlong),
+    "dtp_packed_size": ([ctypes.POINTER(Config)], c_size_t),
+    "dtp_pack_layer": ([ctypes.POINTER(Config), c_int, ctypes.POINTER(LayerSrc), c_void_p, c_size_t,
+                        c_void_p], c_int),
+    "dtp_pack_globals": ([ctypes.POINTER(Config), c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                          c_void_p], c_int),
+    "dtp_workspace_size": ([ctypes.POINTER(Config), c_int], c_size_t),
+    "dtp_workspace_size_host": ([ctypes.POINTER(Config), c_int], c_size_t),
+    "dtp_fwd_prefill": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int, c_void_p,
+                         c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "dtp_fwd_prefill_host": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int,
+                              c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "dtp_check": ([c_void_p], c_int),
+    "dtp_rms_norm": ([c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_float, c_void_p], c_int),
+    "dtp_qk_norm_rope_neox": ([c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                               c_float, c_float, c_void_p], c_int),
+    "dtp_sdpa_workspace_size": ([c_int, c_int, c_int, c_int], c_size_t),
+    "dtp_sdpa_causal_gqa": ([c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                             c_int, c_float, c_void_p, c_size_t, c_void_p], c_int),
+    "dtp_swiglu": ([c_void_p, c_void_p, c_void_p, c_int, c_size_t, c_void_p], c_int),
+    "dtp_linear": ([c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p,
+                    c_void_p], c_int),
+    "dtp_timer_enable": ([ctypes.c_uint, c_int], c_int),
+    "dtp_timer_disable": ([], c_int),
+    "dtp_timer_read": ([c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_float)], c_int),
+}
+
+
+def lib():
+    """The loaded libdtp.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError(f"{LIB} is not built; call dense_transformer_prefill_gb300.build()")
+            L = ctypes.CDLL(LIB)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().dtp_last_error().decode()
+
+
+def _ok(rc: int) -> None:
+    if rc != 0:
+        raise DtpError(rc, last_error())
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return DTP_F32
+    if t.dtype == torch.bfloat16:
+        return DTP_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def config_from(cfg) -> Config:
+    """Config from an object/dict with the dtp_config field names; precision may be
+    "f32"/"bf16" or the DTP_PREC_* code."""
+    get = (lambda k: cfg[k]) if isinstance(cfg, dict) else (lambda k: getattr(cfg, k))
+    prec = get("precision")
+    if isinstance(prec, str):
+        prec = {"f32": DTP_PREC_F32, "bf16": DTP_PREC_BF16}[prec]
+    return Config(get("n_layer"), get("n_embd"), get("n_head"), get("n_head_kv"), get("head_dim"),
+                  get("rope_dim_count"), get("n_ff"), get("n_vocab"), float(get("rope_freq_base")),
+                  float(get("rms_eps")), prec)
+
+
+# ----------------------------------------------------------------------------- entry points
+def packed_size(c: Config) -> int:
+    return lib().dtp_packed_size(ctypes.byref(c))
+
+
+def workspace_size(c: Config, T: int) -> int:
+    return lib().dtp_workspace_size(ctypes.byref(c), T)
+
+
+def workspace_size_host(c: Config, T: int) -> int:
+    return lib().dtp_workspace_size_host(ctypes.byref(c), T)
+
+
+def pack_layer(c: Config, layer: int, src: dict, packed: torch.Tensor, stream=None) -> None:
+    s = LayerSrc(*[_ptr(src[n]) for n, _ in LayerSrc._fields_])
+    _ok(lib().dtp_pack_layer(ctypes.byref(c), layer, ctypes.byref(s), packed.data_ptr(),
+                             packed.numel() * packed.element_size(), _stream(stream)))
+
+
+def pack_globals(c: Config, tok_embd, output_norm, output, packed: torch.Tensor, stream=None) -> None:
+    _ok(lib().dtp_pack_globals(ctypes.byref(c), _ptr(tok_embd), _ptr(output_norm), _ptr(output),
+                               packed.data_ptr(), packed.numel() * packed.element_size(),
+                               _stream(stream)))
+
+
+def fwd_prefill(c: Config, packed: torch.Tensor, tokens: torch.Tensor, logits: torch.Tensor,
+                workspace: torch.Tensor, hidden: torch.Tensor | None = None, stream=None) -> None:
+    assert tokens.dtype in (torch.int32, torch.uint32) and tokens.is_contiguous()
+    assert logits.dtype == torch.float32 and logits.is_contiguous()
+    _ok(lib().dtp_fwd_prefill(ctypes.byref(c), packed.data_ptr(),
+                              packed.numel() * packed.element_size(), tokens.data_ptr(),
+                              tokens.numel(), logits.data_ptr(), _ptr(hidden),
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream(stream)))
+
+
+def fwd_prefill_host(c: Config, packed: torch.Tensor, tokens_host: torch.Tensor,
+                     logits_host: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    assert tokens_host.device.type == "cpu" and logits_host.device.type == "cpu"
+    _ok(lib().dtp_fwd_prefill_host(ctypes.byref(c), packed.data_ptr(),
+                                   packed.numel() * packed.element_size(), tokens_host.data_ptr(),
+                                   tokens_host.numel(), logits_host.data_ptr(),
+                                   workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def check(stream=None) -> None:
+    _ok(lib().dtp_check(_stream(stream)))
+
+
+def rms_norm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, eps: float, stream=None) -> None:
+    rows, cols = x.shape
+    _ok(lib().dtp_rms_norm(x.data_ptr(), w.data_ptr(), y.data_ptr(), _dtype_code(y), rows, cols,
+                           eps, _stream(stream)))
+
+
+def qk_norm_rope_neox(x: torch.Tensor, w_norm, pos, n_heads: int, head_dim: int,
+                      rope_dim_count: int, freq_base: float, eps: float, stream=None) -> None:
+    _ok(lib().dtp_qk_norm_rope_neox(x.data_ptr(), _dtype_code(x), _ptr(w_norm), _ptr(pos),
+                                    x.shape[0], n_heads, head_dim, rope_dim_count, freq_base, eps,
+                                    _stream(stream)))
+
+
+def sdpa_workspace_size(T: int, n_head_kv: int, head_dim: int, dtype: int) -> int:
+    return lib().dtp_sdpa_workspace_size(T, n_head_kv, head_dim, dtype)
+
+
+def sdpa_causal_gqa(q, k, v, out, n_head: int, n_head_kv: int, head_dim: int, scale: float,
+                    workspace=None, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(lib().dtp_sdpa_causal_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  _dtype_code(q), q.shape[0], n_head, n_head_kv, head_dim, scale,
+                                  _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def swiglu(gate, up, out, stream=None) -> None:
+    _ok(lib().dtp_swiglu(gate.data_ptr(), up.data_ptr(), out.data_ptr(), _dtype_code(gate),
+                         gate.numel(), _stream(stream)))
+
+
+def linear(x, W, y, residual=None, stream=None) -> None:
+    M, K = x.shape
+    N = W.shape[0]
+    _ok(lib().dtp_linear(x.data_ptr(), W.data_ptr(), y.data_ptr(), _dtype_code(x), _dtype_code(y),
+                         M, N, K, _ptr(residual), _stream(stream)))
+
+
+def timer_enable(kinds, capacity: int) -> None:
+    mask = 0
+    for k in kinds:
+        mask |= 1 << (KERNEL_KINDS[k] if isinstance(k, str) else k)
+    _ok(lib().dtp_timer_enable(mask, capacity))
+
+
+def timer_disable() -> None:
+    _ok(lib().dtp_timer_disable())
+
+
+def timer_read(kind) -> tuple[int, float]:
+    n, ms = c_int(0), c_float(0.0)
+    _ok(lib().dtp_timer_read(KERNEL_KINDS[kind] if isinstance(kind, str) else kind,
+                             ctypes.byref(n), ctypes.byref(ms)))
+    return n.value, ms.value
+
+
+def launch_count(reset: bool = False) -> int:
+    return lib().dtp_launch_count(1 if reset else 0)
+
+
+# ----------------------------------------------------------------------------- model holder
+class Model:
+    """Owns the packed weight buffer (and cached workspaces) of one model on one device."""
+
+    def __init__(self, cfg, device="cuda"):
+        self.cfg = cfg
+        self.c = config_from(cfg)
+        self.device = torch.device(device)
+        n = packed_size(self.c)
+        if n == 0:
+            raise DtpError(-1, last_error())
+        self.packed = torch.empty(n, dtype=torch.uint8, device=self.device)
+        self._ws = {}
+
+    def load_layer(self, layer: int, arrays: dict, stream=None) -> None:
+        """Pack one layer from float32 arrays (numpy or torch) with the dtp_layer_src names."""
+        dev = {k: torch.as_tensor(v).to(self.device, torch.float32).contiguous()
+               for k, v in arrays.items()}
+        pack_layer(self.c, layer, dev, self.packed, stream)
+        torch.cuda.current_stream(self.device).synchronize()
+
+    def load_globals(self, tok_embd, output_norm, output, stream=None) -> None:
+        t = [torch.as_tensor(a).to(self.device, torch.float32).contiguous()
+             for a in (tok_embd, output_norm, output)]
+        pack_globals(self.c, *t, self.packed, stream)
+        torch.cuda.current_stream(self.device).synchronize()
+
+    def workspace(self, T: int, host: bool = False) -> torch.Tensor:
+        key = (T, host)
+        if key not in self._ws:
+            n = (workspace_size_host if host else workspace_size)(self.c, T)
+            if n == 0:
+                raise DtpError(-1, last_error())
+            self._ws[key] = torch.empty(n, dtype=torch.uint8, device=self.device)
+        return self._ws[key]
+
+    def forward(self, tokens: torch.Tensor, logits: torch.Tensor | None = None,
+                hidden: bool | torch.Tensor = False, stream=None):
+        T = tokens.numel()
+        if logits is None:
+            logits = torch.empty((T, self.c.n_vocab), dtype=torch.float32, device=self.device)
+        hid = None
+        if hidden is True:
+            hid = torch.empty((self.c.n_layer + 1, T, self.c.n_embd), dtype=torch.float32,
+                              device=self.device)
+        elif isinstance(hidden, torch.Tensor):
+            hid = hidden
+        fwd_prefill(self.c, self.packed, tokens, logits, self.workspace(T), hid, stream)
+        return (logits, hid) if hid is not None else logits

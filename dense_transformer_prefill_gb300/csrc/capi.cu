@@ -1,0 +1,656 @@
+// C ABI of the prefill library: argument validation, the packed-weight and
+// workspace layouts, the forward-pass orchestration ("docs.rs memra-engine
+// 0.130.0, src/forward.rs", Model::forward), per-op entry points, tensor-map
+// encoding, kernel timers and the device error words.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace dtp {
+
+// ----------------------------------------------------------------------------- errors
+static thread_local char t_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+void clear_error() { t_err[0] = 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 148;
+    }
+    return cached[dev];
+}
+
+// ----------------------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elt_bytes,
+                  uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
+                  uint32_t box_cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * (uint64_t)elt_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ----------------------------------------------------------------------------- timers
+struct TimerState {
+    std::mutex mu;
+    unsigned mask = 0;
+    int capacity = 0;
+    std::vector<cudaEvent_t> ev[DTP_K_COUNT][2];
+    int used[DTP_K_COUNT] = {0};
+};
+static TimerState g_timer;
+static std::atomic<long long> g_launches{0};
+
+LaunchScope::LaunchScope(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (!g_timer.mask) return;
+    std::lock_guard<std::mutex> lk(g_timer.mu);
+    if (!(g_timer.mask & (1u << kind)) || g_timer.used[kind] >= g_timer.capacity) return;
+    slot = g_timer.used[kind]++;
+    cudaEventRecord(g_timer.ev[kind][0][slot], stream);
+}
+LaunchScope::~LaunchScope() {
+    if (slot >= 0) cudaEventRecord(g_timer.ev[kind][1][slot], stream);
+}
+
+static void timer_destroy() {
+    for (int k = 0; k < DTP_K_COUNT; ++k) {
+        for (int j = 0; j < 2; ++j) {
+            for (cudaEvent_t e : g_timer.ev[k][j]) cudaEventDestroy(e);
+            g_timer.ev[k][j].clear();
+        }
+        g_timer.used[k] = 0;
+    }
+    g_timer.mask = 0;
+    g_timer.capacity = 0;
+}
+
+// ----------------------------------------------------------------------------- layouts
+static int validate_config(const dtp_config* c) {
+    if (!c) return fail(DTP_ERR_INVALID_ARG, "config is NULL");
+    if (c->n_layer < 0 || c->n_embd <= 0 || c->n_head <= 0 || c->n_head_kv <= 0 ||
+        c->head_dim <= 0 || c->n_ff <= 0 || c->n_vocab <= 0)
+        return fail(DTP_ERR_INVALID_ARG, "config sizes must be positive");
+    if (c->n_head % c->n_head_kv)
+        return fail(DTP_ERR_INVALID_ARG, "n_head (%d) is not a multiple of n_head_kv (%d)",
+                    c->n_head, c->n_head_kv);
+    if (c->head_dim % 2 || c->rope_dim_count <= 0 || c->rope_dim_count % 2 ||
+        c->rope_dim_count > c->head_dim)
+        return fail(DTP_ERR_INVALID_ARG, "rope_dim_count must be even and in [2, head_dim]");
+    if (!(c->rms_eps >= 0.f) || !(c->rope_freq_base > 0.f))
+        return fail(DTP_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_freq_base > 0");
+    if (c->precision != DTP_PREC_F32 && c->precision != DTP_PREC_BF16)
+        return fail(DTP_ERR_INVALID_ARG, "unknown precision %d", c->precision);
+    if (c->n_embd % 8 || c->n_ff % 64)
+        return fail(DTP_ERR_UNSUPPORTED, "n_embd must be a multiple of 8 and n_ff of 64");
+    if (c->precision == DTP_PREC_BF16) {
+        if (c->head_dim != 64 && c->head_dim != 128)
+            return fail(DTP_ERR_UNSUPPORTED, "bf16 path: head_dim must be 64 or 128");
+        if ((c->rope_dim_count / 2) % 32 || (c->head_dim - c->rope_dim_count) % 32)
+            return fail(DTP_ERR_UNSUPPORTED,
+                        "bf16 path: rope_dim_count/2 and head_dim-rope_dim_count must be "
+                        "multiples of 32");
+    }
+    return DTP_OK;
+}
+
+struct PackedLayout {
+    size_t elt = 4;
+    size_t attn_norm, w_qkv, q_norm, k_norm, wo, ffn_norm, w_gu, w_down;   // within a layer
+    size_t layer_bytes;
+    size_t tok_embd, output_norm, output;                                 // absolute
+    size_t total;
+};
+
+static PackedLayout packed_layout(const dtp_config* c) {
+    PackedLayout L;
+    L.elt = c->precision == DTP_PREC_BF16 ? 2 : 4;
+    const size_t d = c->n_embd, hd = c->head_dim, nq = (size_t)c->n_head * hd,
+                 nqkv = (size_t)(c->n_head + 2 * c->n_head_kv) * hd, F = c->n_ff;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.w_qkv = take(nqkv * d * L.elt);
+    L.wo = take(d * nq * L.elt);
+    L.w_gu = take(2 * F * d * L.elt);
+    L.w_down = take(d * F * L.elt);
+    L.attn_norm = take(d * 4);
+    L.q_norm = take(hd * 4);
+    L.k_norm = take(hd * 4);
+    L.ffn_norm = take(d * 4);
+    L.layer_bytes = o;
+    o = L.layer_bytes * c->n_layer;
+    L.tok_embd = take((size_t)c->n_vocab * d * L.elt);
+    L.output = take((size_t)c->n_vocab * d * L.elt);
+    L.output_norm = take(d * 4);
+    L.total = o;
+    return L;
+}
+
+struct Workspace {
+    size_t x, h, qkv, attn, gu, act;            // f32 path
+    size_t q, k, vt, rope;                       // bf16 path
+    long long ldvt;
+    size_t tokens, logits;                       // _host staging
+    size_t total;
+};
+
+static Workspace workspace_layout(const dtp_config* c, int T, bool host) {
+    Workspace W = {};
+    const size_t d = c->n_embd, hd = c->head_dim, nq = (size_t)c->n_head * hd,
+                 nk = (size_t)c->n_head_kv * hd, F = c->n_ff;
+    const bool bf = c->precision == DTP_PREC_BF16;
+    const size_t e = bf ? 2 : 4;
+    size_t o = 256;     // first 256 bytes reserved
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    W.x = take((size_t)T * d * 4);
+    W.h = take((size_t)T * d * e);
+    W.attn = take((size_t)T * nq * e);
+    W.act = take((size_t)T * F * e);
+    if (bf) {
+        W.ldvt = (long long)align_up(T, 8);
+        W.q = take((size_t)T * nq * 2);
+        W.k = take((size_t)T * nk * 2);
+        W.vt = take(nk * (size_t)W.ldvt * 2);
+        W.rope = take((size_t)T * (c->rope_dim_count / 2) * sizeof(float2));
+    } else {
+        W.qkv = take((size_t)T * (nq + 2 * nk) * 4);
+        W.gu = take((size_t)T * 2 * F * 4);
+    }
+    if (host) {
+        W.tokens = take((size_t)T * 4);
+        W.logits = take((size_t)T * c->n_vocab * 4);
+    }
+    W.total = o;
+    return W;
+}
+
+static bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// ----------------------------------------------------------------------------- forward
+static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
+                   const uint32_t* tokens, int T, float* logits, float* hidden, uint8_t* ws,
+                   const Workspace& W, cudaStream_t s) {
+    const int d = c->n_embd, hd = c->head_dim, h = c->n_head, g = c->n_head_kv, F = c->n_ff;
+    const int nq = h * hd, nk = g * hd, nqkv = nq + 2 * nk;
+    float* x = (float*)(ws + W.x);
+    float* hb = (float*)(ws + W.h);
+    float* qkv = (float*)(ws + W.qkv);
+    float* attn = (float*)(ws + W.attn);
+    float* gu = (float*)(ws + W.gu);
+    float* act = (float*)(ws + W.act);
+    const float scale = 1.0f / sqrtf((float)hd);
+    DTP_CUDA_CHECK(launch_embed(tokens, T, c->n_vocab, d, P + L.tok_embd, DTP_F32, x, s));
+    for (int l = 0; l < c->n_layer; ++l) {
+        const uint8_t* lp = P + (size_t)l * L.layer_bytes;
+        if (hidden)
+            DTP_CUDA_CHECK(launch_copy_f32(x, hidden + (size_t)l * T * d, (size_t)T * d, s));
+        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.attn_norm), hb, DTP_F32, T, d,
+                                      c->rms_eps, s));
+        DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(lp + L.w_qkv), qkv, DTP_F32, nqkv,
+                                        T, nqkv, d, nullptr, s, DTP_K_GEMM_QKV));
+        DTP_CUDA_CHECK(launch_qk_norm_rope(qkv, DTP_F32, nqkv, (const float*)(lp + L.q_norm),
+                                           nullptr, T, h, hd, c->rope_dim_count,
+                                           c->rope_freq_base, c->rms_eps, s));
+        DTP_CUDA_CHECK(launch_qk_norm_rope(qkv + nq, DTP_F32, nqkv, (const float*)(lp + L.k_norm),
+                                           nullptr, T, g, hd, c->rope_dim_count,
+                                           c->rope_freq_base, c->rms_eps, s));
+        DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, qkv + nq, nqkv, qkv + nq + nk, nqkv, 0, attn,
+                                        nq, DTP_F32, T, h, g, hd, scale, s));
+        DTP_CUDA_CHECK(launch_gemm_simt(attn, nq, (const float*)(lp + L.wo), x, DTP_F32, d, T, d,
+                                        nq, x, s, DTP_K_GEMM_O));
+        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.ffn_norm), hb, DTP_F32, T, d,
+                                      c->rms_eps, s));
+        DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(lp + L.w_gu), gu, DTP_F32, 2 * F, T,
+                                        2 * F, d, nullptr, s, DTP_K_GEMM_GATEUP));
+        DTP_CUDA_CHECK(launch_swiglu_interleaved64(gu, act, T, F, s));
+        DTP_CUDA_CHECK(launch_gemm_simt(act, F, (const float*)(lp + L.w_down), x, DTP_F32, d, T, d,
+                                        F, x, s, DTP_K_GEMM_DOWN));
+    }
+    if (hidden)
+        DTP_CUDA_CHECK(
+            launch_copy_f32(x, hidden + (size_t)c->n_layer * T * d, (size_t)T * d, s));
+    DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(P + L.output_norm), hb, DTP_F32, T, d,
+                                  c->rms_eps, s));
+    DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(P + L.output), logits, DTP_F32,
+                                    c->n_vocab, T, c->n_vocab, d, nullptr, s, DTP_K_GEMM_LMHEAD));
+    return DTP_OK;
+}
+
+static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
+                    const uint32_t* tokens, int T, float* logits, float* hidden, uint8_t* ws,
+                    const Workspace& W, cudaStream_t s) {
+    typedef __nv_bfloat16 bf;
+    const int d = c->n_embd, hd = c->head_dim, h = c->n_head, g = c->n_head_kv, F = c->n_ff;
+    const int nq = h * hd, nk = g * hd, nqkv = nq + 2 * nk;
+    float* x = (float*)(ws + W.x);
+    bf* hb = (bf*)(ws + W.h);
+    bf* q = (bf*)(ws + W.q);
+    bf* k = (bf*)(ws + W.k);
+    bf* vt = (bf*)(ws + W.vt);
+    bf* attn = (bf*)(ws + W.attn);
+    bf* act = (bf*)(ws + W.act);
+    float2* rope = (float2*)(ws + W.rope);
+    const float scale = 1.0f / sqrtf((float)hd);
+    const bool fa = attn_tc_supported(h, g, hd);
+    DTP_CUDA_CHECK(launch_rope_table(rope, T, c->rope_dim_count, c->rope_freq_base, s));
+    DTP_CUDA_CHECK(launch_embed(tokens, T, c->n_vocab, d, P + L.tok_embd, DTP_BF16, x, s));
+    for (int l = 0; l < c->n_layer; ++l) {
+        const uint8_t* lp = P + (size_t)l * L.layer_bytes;
+        if (hidden)
+            DTP_CUDA_CHECK(launch_copy_f32(x, hidden + (size_t)l * T * d, (size_t)T * d, s));
+        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.attn_norm), hb, DTP_BF16, T, d,
+                                      c->rms_eps, s));
+        GemmEpiArgs e;
+        e.q = q;
+        e.k = k;
+        e.vt = vt;
+        e.ldvt = W.ldvt;
+        e.q_norm = (const float*)(lp + L.q_norm);
+        e.k_norm = (const float*)(lp + L.k_norm);
+        e.rope = rope;
+        e.n_head = h;
+        e.n_head_kv = g;
+        e.head_dim = hd;
+        e.rope_dims = c->rope_dim_count;
+        e.eps = c->rms_eps;
+        DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(lp + L.w_qkv), T, nqkv, d, EPI_QKV, e, s,
+                                      DTP_K_GEMM_QKV));
+        if (fa)
+            DTP_CUDA_CHECK(launch_attn_tc(q, k, vt, W.ldvt, attn, T, h, g, hd, scale, s));
+        else
+            DTP_CUDA_CHECK(launch_attn_simt(q, nq, k, nk, vt, (int)W.ldvt, 1, attn, nq, DTP_BF16,
+                                            T, h, g, hd, scale, s));
+        GemmEpiArgs eo;
+        eo.y = x;
+        eo.y_dtype = DTP_F32;
+        eo.ldy = d;
+        eo.residual = x;
+        DTP_CUDA_CHECK(launch_gemm_tc(attn, (const bf*)(lp + L.wo), T, d, nq, EPI_STORE, eo, s,
+                                      DTP_K_GEMM_O));
+        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.ffn_norm), hb, DTP_BF16, T, d,
+                                      c->rms_eps, s));
+        GemmEpiArgs eg;
+        eg.act = act;
+        DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(lp + L.w_gu), T, 2 * F, d, EPI_SWIGLU, eg, s,
+                                      DTP_K_GEMM_GATEUP));
+        DTP_CUDA_CHECK(launch_gemm_tc(act, (const bf*)(lp + L.w_down), T, d, F, EPI_STORE, eo, s,
+                                      DTP_K_GEMM_DOWN));
+    }
+    if (hidden)
+        DTP_CUDA_CHECK(
+            launch_copy_f32(x, hidden + (size_t)c->n_layer * T * d, (size_t)T * d, s));
+    DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(P + L.output_norm), hb, DTP_BF16, T, d,
+                                  c->rms_eps, s));
+    GemmEpiArgs el;
+    el.y = logits;
+    el.y_dtype = DTP_F32;
+    el.ldy = c->n_vocab;
+    DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(P + L.output), T, c->n_vocab, d, EPI_STORE, el,
+                                  s, DTP_K_GEMM_LMHEAD));
+    return DTP_OK;
+}
+
+}  // namespace dtp
+
+using namespace dtp;
+
+// ================================================================================ C ABI
+extern "C" {
+
+const char* dtp_last_error(void) { return t_err; }
+
+long long dtp_launch_count(int reset) {
+    return reset ? g_launches.exchange(0) : g_launches.load();
+}
+
+size_t dtp_packed_size(const dtp_config* cfg) {
+    if (validate_config(cfg) != DTP_OK) return 0;
+    return packed_layout(cfg).total;
+}
+
+int dtp_pack_layer(const dtp_config* cfg, int layer, const dtp_layer_src* src, void* packed,
+                   size_t packed_bytes, dtp_stream_t stream) {
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (!src || !packed) return fail(DTP_ERR_INVALID_ARG, "NULL src or packed");
+    if (layer < 0 || layer >= cfg->n_layer)
+        return fail(DTP_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, cfg->n_layer);
+    const float* ptrs[] = {src->attn_norm, src->wq, src->wk, src->wv, src->q_norm, src->k_norm,
+                           src->wo, src->ffn_norm, src->w_gate, src->w_up, src->w_down};
+    for (const float* p : ptrs)
+        if (!p) return fail(DTP_ERR_INVALID_ARG, "a layer source pointer is NULL");
+    PackedLayout L = packed_layout(cfg);
+    if (packed_bytes < L.total)
+        return fail(DTP_ERR_WORKSPACE, "packed buffer %zu < %zu bytes", packed_bytes, L.total);
+    if (!aligned(packed, 256)) return fail(DTP_ERR_INVALID_ARG, "packed must be 256-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* lp = (uint8_t*)packed + (size_t)layer * L.layer_bytes;
+    const int bf = cfg->precision == DTP_PREC_BF16;
+    const int d = cfg->n_embd, hd = cfg->head_dim, nq = cfg->n_head * hd,
+              nk = cfg->n_head_kv * hd, F = cfg->n_ff;
+    DTP_CUDA_CHECK(launch_pack_matrix(src->wq, nq, d, lp + L.w_qkv, bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->wk, nk, d, lp + L.w_qkv + (size_t)nq * d * L.elt, bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->wv, nk, d, lp + L.w_qkv + (size_t)(nq + nk) * d * L.elt,
+                                      bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->wo, d, nq, lp + L.wo, bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->w_gate, F, d, lp + L.w_gu, bf, 1, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->w_up, F, d, lp + L.w_gu, bf, 2, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->w_down, d, F, lp + L.w_down, bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->attn_norm, 1, d, lp + L.attn_norm, 0, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->q_norm, 1, hd, lp + L.q_norm, 0, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->k_norm, 1, hd, lp + L.k_norm, 0, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->ffn_norm, 1, d, lp + L.ffn_norm, 0, 0, s));
+    return DTP_OK;
+}
+
+int dtp_pack_globals(const dtp_config* cfg, const float* tok_embd, const float* output_norm,
+                     const float* output, void* packed, size_t packed_bytes,
+                     dtp_stream_t stream) {
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (!tok_embd || !output_norm || !output || !packed)
+        return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    PackedLayout L = packed_layout(cfg);
+    if (packed_bytes < L.total)
+        return fail(DTP_ERR_WORKSPACE, "packed buffer %zu < %zu bytes", packed_bytes, L.total);
+    if (!aligned(packed, 256)) return fail(DTP_ERR_INVALID_ARG, "packed must be 256-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* P = (uint8_t*)packed;
+    const int bf = cfg->precision == DTP_PREC_BF16;
+    DTP_CUDA_CHECK(launch_pack_matrix(tok_embd, cfg->n_vocab, cfg->n_embd, P + L.tok_embd, bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(output, cfg->n_vocab, cfg->n_embd, P + L.output, bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(output_norm, 1, cfg->n_embd, P + L.output_norm, 0, 0, s));
+    return DTP_OK;
+}
+
+size_t dtp_workspace_size(const dtp_config* cfg, int T) {
+    if (validate_config(cfg) != DTP_OK || T <= 0) return 0;
+    return workspace_layout(cfg, T, false).total;
+}
+
+size_t dtp_workspace_size_host(const dtp_config* cfg, int T) {
+    if (validate_config(cfg) != DTP_OK || T <= 0) return 0;
+    return workspace_layout(cfg, T, true).total;
+}
+
+static int fwd_checked(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                       const uint32_t* tokens, int T, float* logits, float* hidden,
+                       void* workspace, size_t ws_bytes, bool host_layout, dtp_stream_t stream) {
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (T <= 0) return fail(DTP_ERR_INVALID_ARG, "T must be >= 1 (got %d)", T);
+    if (!packed || !tokens || !logits || !workspace)
+        return fail(DTP_ERR_INVALID_ARG, "NULL packed, tokens, logits or workspace");
+    PackedLayout L = packed_layout(cfg);
+    if (packed_bytes < L.total)
+        return fail(DTP_ERR_WORKSPACE, "packed buffer %zu < %zu bytes", packed_bytes, L.total);
+    Workspace W = workspace_layout(cfg, T, host_layout);
+    if (ws_bytes < W.total)
+        return fail(DTP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, W.total);
+    if (!aligned(workspace, 256) || !aligned(packed, 256) || !aligned(logits, 16) ||
+        (hidden && !aligned(hidden, 16)))
+        return fail(DTP_ERR_INVALID_ARG,
+                    "workspace/packed must be 256-byte aligned, logits/hidden 16-byte aligned");
+    if (cfg->precision == DTP_PREC_BF16 && (cfg->n_vocab % 4))
+        return fail(DTP_ERR_UNSUPPORTED, "bf16 path: n_vocab must be a multiple of 4");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cfg->precision == DTP_PREC_BF16)
+        return fwd_bf16(cfg, (const uint8_t*)packed, L, tokens, T, logits, hidden,
+                        (uint8_t*)workspace, W, s);
+    return fwd_f32(cfg, (const uint8_t*)packed, L, tokens, T, logits, hidden, (uint8_t*)workspace,
+                   W, s);
+}
+
+int dtp_fwd_prefill(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                    const uint32_t* tokens, int T, float* logits, float* hidden, void* workspace,
+                    size_t ws_bytes, dtp_stream_t stream) {
+    return fwd_checked(cfg, packed, packed_bytes, tokens, T, logits, hidden, workspace, ws_bytes,
+                       false, stream);
+}
+
+int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                         const uint32_t* tokens_host, int T, float* logits_host, void* workspace,
+                         size_t ws_bytes, dtp_stream_t stream) {
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (T <= 0) return fail(DTP_ERR_INVALID_ARG, "T must be >= 1 (got %d)", T);
+    if (!tokens_host || !logits_host || !workspace)
+        return fail(DTP_ERR_INVALID_ARG, "NULL tokens_host, logits_host or workspace");
+    for (int t = 0; t < T; ++t)
+        if (tokens_host[t] >= (uint32_t)cfg->n_vocab)
+            return fail(DTP_ERR_TOKEN_RANGE, "token %u at position %d >= n_vocab %d",
+                        tokens_host[t], t, cfg->n_vocab);
+    Workspace W = workspace_layout(cfg, T, true);
+    if (ws_bytes < W.total)
+        return fail(DTP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, W.total);
+    if (!aligned(workspace, 256)) return fail(DTP_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* ws = (uint8_t*)workspace;
+    uint32_t* tok_d = (uint32_t*)(ws + W.tokens);
+    float* logit_d = (float*)(ws + W.logits);
+    DTP_CUDA_CHECK(cudaMemcpyAsync(tok_d, tokens_host, (size_t)T * 4, cudaMemcpyHostToDevice, s));
+    rc = fwd_checked(cfg, packed, packed_bytes, tok_d, T, logit_d, nullptr, workspace, ws_bytes,
+                     true, stream);
+    if (rc) return rc;
+    DTP_CUDA_CHECK(cudaMemcpyAsync(logits_host, logit_d, (size_t)T * cfg->n_vocab * 4,
+                                   cudaMemcpyDeviceToHost, s));
+    return DTP_OK;
+}
+
+int dtp_check(dtp_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(DTP_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+    unsigned bits = read_clear_simt_errors() | read_clear_gemm_errors() | read_clear_attn_errors();
+    if (bits & ERRBIT_TIMEOUT)
+        return fail(DTP_ERR_DEVICE_TIMEOUT, "a kernel's bounded pipeline wait gave up");
+    if (bits & ERRBIT_TOKEN_RANGE)
+        return fail(DTP_ERR_TOKEN_RANGE, "a token id was >= n_vocab (its row was zeroed)");
+    return DTP_OK;
+}
+
+// ------------------------------------------------------------------------- per-op entry points
+int dtp_rms_norm(const float* x, const float* w, void* y, int y_dtype, int rows, int cols,
+                 float eps, dtp_stream_t stream) {
+    if (!x || !w || !y) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    if (rows <= 0 || cols <= 0) return fail(DTP_ERR_INVALID_ARG, "rows and cols must be >= 1");
+    if (y_dtype != DTP_F32 && y_dtype != DTP_BF16) return fail(DTP_ERR_INVALID_ARG, "bad y_dtype");
+    if (!(eps >= 0.f)) return fail(DTP_ERR_INVALID_ARG, "eps must be >= 0");
+    if ((cols % 4 == 0) && (!aligned(x, 16) || !aligned(w, 16)))
+        return fail(DTP_ERR_INVALID_ARG, "x and w must be 16-byte aligned");
+    DTP_CUDA_CHECK(launch_rmsnorm(x, w, y, y_dtype, rows, cols, eps, (cudaStream_t)stream));
+    return DTP_OK;
+}
+
+int dtp_qk_norm_rope_neox(void* x, int dtype, const float* w_norm, const int32_t* pos, int T,
+                          int n_heads, int head_dim, int rope_dim_count, float freq_base,
+                          float eps, dtp_stream_t stream) {
+    if (!x) return fail(DTP_ERR_INVALID_ARG, "NULL x");
+    if (dtype != DTP_F32 && dtype != DTP_BF16) return fail(DTP_ERR_INVALID_ARG, "bad dtype");
+    if (T <= 0 || n_heads <= 0 || head_dim <= 0 || head_dim % 2)
+        return fail(DTP_ERR_INVALID_ARG, "T, n_heads must be >= 1 and head_dim even");
+    if (rope_dim_count <= 0 || rope_dim_count % 2 || rope_dim_count > head_dim)
+        return fail(DTP_ERR_INVALID_ARG, "rope_dim_count must be even and in [2, head_dim]");
+    if (head_dim > 1024) return fail(DTP_ERR_UNSUPPORTED, "head_dim > 1024");
+    if (!(freq_base > 0.f) || !(eps >= 0.f))
+        return fail(DTP_ERR_INVALID_ARG, "freq_base must be > 0 and eps >= 0");
+    DTP_CUDA_CHECK(launch_qk_norm_rope(x, dtype, n_heads * head_dim, w_norm, pos, T, n_heads,
+                                       head_dim, rope_dim_count, freq_base, eps,
+                                       (cudaStream_t)stream));
+    return DTP_OK;
+}
+
+size_t dtp_sdpa_workspace_size(int T, int n_head_kv, int head_dim, int dtype) {
+    if (T <= 0 || n_head_kv <= 0 || head_dim <= 0 || dtype != DTP_BF16) return 0;
+    return align_up((size_t)n_head_kv * head_dim * align_up(T, 8) * 2, 256);
+}
+
+int dtp_sdpa_causal_gqa(const void* q, const void* k, const void* v, void* out, int dtype, int T,
+                        int n_head, int n_head_kv, int head_dim, float scale, void* workspace,
+                        size_t ws_bytes, dtp_stream_t stream) {
+    if (!q || !k || !v || !out) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    if (dtype != DTP_F32 && dtype != DTP_BF16) return fail(DTP_ERR_INVALID_ARG, "bad dtype");
+    if (T <= 0 || n_head <= 0 || n_head_kv <= 0 || head_dim <= 0)
+        return fail(DTP_ERR_INVALID_ARG, "sizes must be >= 1");
+    if (n_head % n_head_kv) return fail(DTP_ERR_INVALID_ARG, "n_head %% n_head_kv != 0");
+    if (head_dim > 256) return fail(DTP_ERR_UNSUPPORTED, "head_dim > 256");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == DTP_F32) {
+        DTP_CUDA_CHECK(launch_attn_simt(q, n_head * head_dim, k, n_head_kv * head_dim, v,
+                                        n_head_kv * head_dim, 0, out, n_head * head_dim, DTP_F32,
+                                        T, n_head, n_head_kv, head_dim, scale, s));
+        return DTP_OK;
+    }
+    if (!attn_tc_supported(n_head, n_head_kv, head_dim))
+        return fail(DTP_ERR_UNSUPPORTED,
+                    "bf16 attention: head_dim must be 64 or 128 and n_head/n_head_kv even");
+    const size_t need = dtp_sdpa_workspace_size(T, n_head_kv, head_dim, dtype);
+    if (!workspace || ws_bytes < need)
+        return fail(DTP_ERR_WORKSPACE, "sdpa workspace %zu < %zu bytes", ws_bytes, need);
+    if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(k, 16) || !aligned(out, 16))
+        return fail(DTP_ERR_INVALID_ARG, "q, k, out must be 16-byte and workspace 256-byte aligned");
+    const long long ldvt = (long long)align_up(T, 8);
+    __nv_bfloat16* vt = (__nv_bfloat16*)workspace;
+    DTP_CUDA_CHECK(launch_transpose_v((const __nv_bfloat16*)v, vt, T, n_head_kv * head_dim,
+                                      (int)ldvt, s));
+    DTP_CUDA_CHECK(launch_attn_tc((const __nv_bfloat16*)q, (const __nv_bfloat16*)k, vt, ldvt,
+                                  (__nv_bfloat16*)out, T, n_head, n_head_kv, head_dim, scale, s));
+    return DTP_OK;
+}
+
+int dtp_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
+               dtp_stream_t stream) {
+    if (!gate || !up || !out) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    if (dtype != DTP_F32 && dtype != DTP_BF16) return fail(DTP_ERR_INVALID_ARG, "bad dtype");
+    if (n == 0) return DTP_OK;
+    DTP_CUDA_CHECK(launch_swiglu(gate, up, out, dtype, n, (cudaStream_t)stream));
+    return DTP_OK;
+}
+
+int dtp_linear(const void* x, const void* W, void* y, int dtype, int y_dtype, int M, int N, int K,
+               const float* residual, dtp_stream_t stream) {
+    if (!x || !W || !y) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    if (M <= 0 || N <= 0 || K <= 0) return fail(DTP_ERR_INVALID_ARG, "M, N, K must be >= 1");
+    if ((dtype != DTP_F32 && dtype != DTP_BF16) || (y_dtype != DTP_F32 && y_dtype != DTP_BF16))
+        return fail(DTP_ERR_INVALID_ARG, "bad dtype");
+    if (residual && y_dtype != DTP_F32)
+        return fail(DTP_ERR_INVALID_ARG, "a residual needs a float32 output");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == DTP_F32) {
+        DTP_CUDA_CHECK(launch_gemm_simt((const float*)x, K, (const float*)W, y, y_dtype, N, M, N, K,
+                                        residual, s, DTP_K_OTHER));
+        return DTP_OK;
+    }
+    if (K % 8) return fail(DTP_ERR_UNSUPPORTED, "bf16 linear: K must be a multiple of 8");
+    if (!aligned(x, 16) || !aligned(W, 16))
+        return fail(DTP_ERR_INVALID_ARG, "bf16 linear: x and W must be 16-byte aligned");
+    GemmEpiArgs e;
+    e.y = y;
+    e.y_dtype = y_dtype;
+    e.ldy = N;
+    e.residual = residual;
+    DTP_CUDA_CHECK(launch_gemm_tc((const __nv_bfloat16*)x, (const __nv_bfloat16*)W, M, N, K,
+                                  EPI_STORE, e, s, DTP_K_OTHER));
+    return DTP_OK;
+}
+
+// ------------------------------------------------------------------------- timers
+int dtp_timer_enable(unsigned kind_mask, int capacity) {
+    if (capacity <= 0 || capacity > 1 << 20) return fail(DTP_ERR_INVALID_ARG, "bad capacity");
+    std::lock_guard<std::mutex> lk(g_timer.mu);
+    timer_destroy();
+    for (int k = 0; k < DTP_K_COUNT; ++k) {
+        if (!(kind_mask & (1u << k))) continue;
+        for (int j = 0; j < 2; ++j) {
+            g_timer.ev[k][j].resize(capacity);
+            for (int i = 0; i < capacity; ++i) {
+                cudaError_t e = cudaEventCreate(&g_timer.ev[k][j][i]);
+                if (e != cudaSuccess) {
+                    g_timer.ev[k][j].resize(i);
+                    timer_destroy();
+                    return fail(DTP_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
+                }
+            }
+        }
+    }
+    g_timer.capacity = capacity;
+    g_timer.mask = kind_mask;
+    return DTP_OK;
+}
+
+int dtp_timer_disable(void) {
+    std::lock_guard<std::mutex> lk(g_timer.mu);
+    timer_destroy();
+    return DTP_OK;
+}
+
+int dtp_timer_read(int kind, int* count, float* total_ms) {
+    if (kind < 0 || kind >= DTP_K_COUNT || !count || !total_ms)
+        return fail(DTP_ERR_INVALID_ARG, "bad kind or NULL output");
+    std::lock_guard<std::mutex> lk(g_timer.mu);
+    float tot = 0.f;
+    const int n = g_timer.used[kind];
+    for (int i = 0; i < n; ++i) {
+        float ms = 0.f;
+        cudaError_t e = cudaEventElapsedTime(&ms, g_timer.ev[kind][0][i], g_timer.ev[kind][1][i]);
+        if (e != cudaSuccess) return fail(DTP_ERR_CUDA, "cudaEventElapsedTime: %s", cudaGetErrorString(e));
+        tot += ms;
+    }
+    *count = n;
+    *total_ms = tot;
+    return DTP_OK;
+}
+
+}  // extern "C"

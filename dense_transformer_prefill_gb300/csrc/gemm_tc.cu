@@ -1,0 +1,443 @@
+// tcgen05 tensor-core GEMM for the projections, the FFN and the lm_head
+// (forward.rs, Model::forward: every `e.matmul(&w, &x, t)`), with the
+// neighbouring elementwise steps fused into the epilogue:
+//   EPI_STORE   y = x W^T (+ residual)      -- O / down projections (residual adds,
+//                                              forward.rs `e.add`) and the lm_head
+//   EPI_QKV     per-head QK-RMSNorm + NeoX RoPE on q and k, v stored transposed
+//   EPI_SWIGLU  silu(gate) * up on the interleaved gate/up product (`ffn_act`)
+//
+// D[M, N] = A[M, K] B[N, K]^T with A = activations, B = weights, both bf16 and
+// K-contiguous.  One persistent CTA per SM walks 128 x BN output tiles:
+//   warp 0      TMA producer: 128x64 A and BNx64 B boxes (128-byte swizzle) into
+//               a STAGES-deep shared-memory ring (mbarrier full/empty pairs)
+//   warp 1      one thread issues tcgen05.mma (M=128, N=BN, K=16) into a TMEM
+//               accumulator; two accumulators (2*BN columns) so the epilogue of
+//               tile i overlaps the main loop of tile i+1
+//   warps 2..5  epilogue: tcgen05.ld (TMEM lane = output row), fused math,
+//               global stores
+#include <math.h>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dtp {
+
+static __device__ unsigned g_gemm_err = 0;
+
+unsigned read_clear_gemm_errors() {
+    unsigned v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_err, sizeof(v)) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_gemm_err, &z, sizeof(z));
+    return v;
+}
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+};
+
+struct Params {
+    int M, N, K;
+    int tiles_m, tiles_n, num_kb;
+    int vec_ok;     // y row stride / base allow 16-byte vector stores
+    GemmEpiArgs ea;
+};
+
+__device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
+
+// Store 32 consecutive floats (as float or bf16) to dst (16-byte aligned when vec).
+__device__ __forceinline__ void store_row32(float* dst, const float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+}
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        uint4 u;
+        u.x = ptx::pack_bf16x2(v[j + 0], v[j + 1]);
+        u.y = ptx::pack_bf16x2(v[j + 2], v[j + 3]);
+        u.z = ptx::pack_bf16x2(v[j + 4], v[j + 5]);
+        u.w = ptx::pack_bf16x2(v[j + 6], v[j + 7]);
+        *reinterpret_cast<uint4*>(dst + j) = u;
+    }
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// ----------------------------------------------------------------------------- epilogues
+template <int BN>
+__device__ __forceinline__ void epi_store(const Params& p, uint32_t tbase, int grow, int n0) {
+    const GemmEpiArgs& ea = p.ea;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        ptx::tmem_ld32(tbase + c, r);
+        const int col0 = n0 + c;
+        if (col0 >= p.N) break;                     // warp-uniform
+        if (grow >= p.M) continue;                  // the next tcgen05.ld reconverges below
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = f32(r[j]);
+        const size_t off = (size_t)grow * ea.ldy + col0;
+        if (p.vec_ok && col0 + 32 <= p.N) {
+            if (ea.residual) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float4 a = *reinterpret_cast<const float4*>(ea.residual + off + j);
+                    v[j] += a.x; v[j + 1] += a.y; v[j + 2] += a.z; v[j + 3] += a.w;
+                }
+            }
+            if (ea.y_dtype == DTP_F32)
+                store_row32(reinterpret_cast<float*>(ea.y) + off, v);
+            else
+                store_row32(reinterpret_cast<__nv_bfloat16*>(ea.y) + off, v);
+        } else {
+            for (int j = 0; j < 32 && col0 + j < p.N; ++j) {
+                float x = v[j];
+                if (ea.residual) x += ea.residual[off + j];
+                if (ea.y_dtype == DTP_F32)
+                    reinterpret_cast<float*>(ea.y)[off + j] = x;
+                else
+                    reinterpret_cast<__nv_bfloat16*>(ea.y)[off + j] = __float2bfloat16_rn(x);
+            }
+        }
+    }
+}
+
+// q/k heads: RMSNorm over head_dim with q_norm/k_norm, then NeoX RoPE from the
+// cos/sin table; v heads: stored transposed (key index contiguous).
+template <int BN>
+__device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int grow, int n0) {
+    const GemmEpiArgs& ea = p.ea;
+    const int hd = ea.head_dim, half = ea.rope_dims / 2;
+    const int nq = ea.n_head * hd, nk = ea.n_head_kv * hd;
+    const bool live = grow < p.M;
+#pragma unroll 1
+    for (int h0 = 0; h0 < BN; h0 += hd) {
+        const int col = n0 + h0;
+        if (col >= p.N) break;
+        const uint32_t th = tbase + h0;
+        if (col < nq + nk) {
+            const bool isq = col < nq;
+            const float* w = isq ? ea.q_norm : ea.k_norm;
+            float ss = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < hd; c += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + c, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ss = fmaf(f32(r[j]), f32(r[j]), ss);
+            }
+            const float rstd = 1.0f / sqrtf(ss / (float)hd + ea.eps);
+            __nv_bfloat16* dst = isq ? ea.q + (size_t)grow * nq + col
+                                     : ea.k + (size_t)grow * nk + (col - nq);
+#pragma unroll 1
+            for (int i0 = 0; i0 < half; i0 += 32) {
+                uint32_t ra[32], rb[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + i0, ra);
+                ptx::tmem_ld32(th + half + i0, rb);
+                if (live) {
+                    const float2* cs = ea.rope + (size_t)grow * half + i0;
+                    float ya[32], yb[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float a = f32(ra[j]) * rstd * w[i0 + j];
+                        const float b = f32(rb[j]) * rstd * w[half + i0 + j];
+                        const float2 c = cs[j];
+                        ya[j] = a * c.x - b * c.y;
+                        yb[j] = a * c.y + b * c.x;
+                    }
+                    store_row32(dst + i0, ya);
+                    store_row32(dst + half + i0, yb);
+                }
+            }
+#pragma unroll 1
+            for (int c = ea.rope_dims; c < hd; c += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + c, r);
+                if (live) {
+                    float y[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[j] = f32(r[j]) * rstd * w[c + j];
+                    store_row32(dst + c, y);
+                }
+            }
+        } else {
+            const int vcol = col - nq - nk;
+#pragma unroll 1
+            for (int c = 0; c < hd; c += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + c, r);
+                if (live) {
+                    __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + grow;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        dst[(size_t)j * ea.ldvt] = __float2bfloat16_rn(f32(r[j]));
+                }
+            }
+        }
+    }
+}
+
+// gate/up interleaved in 64-column blocks: block b of the product holds gate
+// columns 64b..64b+63 then up columns 64b..64b+63; act[:, 64b + j] = silu(g) * u.
+template <int BN>
+__device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, int grow, int n0) {
+    const GemmEpiArgs& ea = p.ea;
+    const int F = p.N / 2;
+#pragma unroll 1
+    for (int b = 0; b < BN; b += 128) {
+        const int colblk = n0 + b;
+        if (colblk >= p.N) break;
+        const int f0 = colblk / 2;
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 32) {
+            uint32_t rg[32], ru[32];
+            __syncwarp();
+            ptx::tmem_ld32(tbase + b + c, rg);
+            ptx::tmem_ld32(tbase + b + 64 + c, ru);
+            if (grow < p.M) {
+                float a[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a[j] = silu_f(f32(rg[j])) * f32(ru[j]);
+                store_row32(ea.act + (size_t)grow * F + f0 + c, a);
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------- kernel
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Params p) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* tfull = bars + 2 * C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&tfull[b], 1);
+            ptx::mbar_init(&tempty[b], 128);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == 1 && lane == 0) {
+        ptx::tma_prefetch_desc(&tmA);
+        ptx::tma_prefetch_desc(&tmB);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const int num_tiles = p.tiles_m * p.tiles_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                const int mb = tile % p.tiles_m, nb = tile / p.tiles_m;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::wait_bounded(&empty[stage], phase ^ 1, abort_flag, &g_gemm_err,
+                                           ERRBIT_TIMEOUT))
+                        goto producer_done;
+                    ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    ptx::tma_load_2d(&tmA, &full[stage], sA + stage * C::A_BYTES, kb * BK, mb * BM);
+                    ptx::tma_load_2d(&tmB, &full[stage], sB + stage * C::B_BYTES, kb * BK, nb * BN);
+                    ++issued;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        producer_done:
+            if (*abort_flag) {
+                // let every load still in flight land before the CTA can exit
+                int s = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < C::STAGES && i < issued; ++i) {
+                    if (--s < 0) {
+                        s = C::STAGES - 1;
+                        ph ^= 1;
+                    }
+                    volatile int never = 0;
+                    ptx::wait_bounded(&full[s], ph, &never, &g_gemm_err, ERRBIT_TIMEOUT);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                if (!ptx::wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, &g_gemm_err,
+                                       ERRBIT_TIMEOUT))
+                    break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                bool ok = true;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::wait_bounded(&full[stage], phase, abort_flag, &g_gemm_err,
+                                           ERRBIT_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t adesc = ptx::sdesc_sw128(ptx::smem_u32(sA + stage * C::A_BYTES));
+                    const uint64_t bdesc = ptx::sdesc_sw128(ptx::smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        ptx::umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                          (kb > 0 || kk > 0) ? 1u : 0u);
+                    ptx::umma_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                ptx::umma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            // every MMA issued above completes before TMEM can be released
+            ptx::umma_commit(drain);
+            volatile int never = 0;
+            ptx::wait_bounded(drain, 0, &never, &g_gemm_err, ERRBIT_TIMEOUT);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue warps 2..5
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int mb = tile % p.tiles_m, nb = tile / p.tiles_m;
+            const bool ok = ptx::wait_bounded(&tfull[acc], acc_phase, abort_flag, &g_gemm_err,
+                                              ERRBIT_TIMEOUT);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            ptx::tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+            const int grow = mb * BM + row, n0 = nb * BN;
+            if (EPI == EPI_STORE) epi_store<BN>(p, tbase, grow, n0);
+            if (EPI == EPI_QKV) epi_qkv<BN>(p, tbase, grow, n0);
+            if (EPI == EPI_SWIGLU) epi_swiglu<BN>(p, tbase, grow, n0);
+            __syncwarp();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int BN, int EPI>
+cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+                        cudaStream_t s) {
+    using C = Cfg<BN>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::SMEM_BYTES, s>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,
+                           GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind) {
+    const int BN = (N >= 256 || epi != EPI_STORE) ? 256 : 128;
+    CUtensorMap ta, tb;
+    if (!make_tmap_2d(&ta, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, K, BM, BK))
+        return cudaErrorInvalidValue;
+    if (!make_tmap_2d(&tb, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, K, BN, BK))
+        return cudaErrorInvalidValue;
+    Params p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.tiles_m = (M + BM - 1) / BM;
+    p.tiles_n = (N + BN - 1) / BN;
+    p.num_kb = (K + BK - 1) / BK;
+    p.ea = ea;
+    p.vec_ok = 1;
+    if (epi == EPI_STORE) {
+        const int eb = ea.y_dtype == DTP_F32 ? 4 : 2;
+        if ((ea.ldy * eb) % 16 != 0 || reinterpret_cast<uintptr_t>(ea.y) % 16 != 0 ||
+            (ea.residual && reinterpret_cast<uintptr_t>(ea.residual) % 16 != 0))
+            p.vec_ok = 0;
+    }
+    LaunchScope ls(kind, s);
+    if (BN == 256) {
+        if (epi == EPI_QKV) return launch_impl<256, EPI_QKV>(ta, tb, p, s);
+        if (epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU>(ta, tb, p, s);
+        return launch_impl<256, EPI_STORE>(ta, tb, p, s);
+    }
+    return launch_impl<128, EPI_STORE>(ta, tb, p, s);
+}
+
+}  // namespace dtp

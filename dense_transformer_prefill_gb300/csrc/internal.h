@@ -1,0 +1,121 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dtp.h"
+
+namespace dtp {
+
+// ----------------------------------------------------------------------------- errors
+int fail(int code, const char* fmt, ...);      // records the message, returns code
+void clear_error();
+
+#define DTP_CUDA_CHECK(expr)                                                                   \
+    do {                                                                                       \
+        cudaError_t e_ = (expr);                                                               \
+        if (e_ != cudaSuccess)                                                                 \
+            return ::dtp::fail(DTP_ERR_CUDA, "%s: %s (%s:%d)", #expr, cudaGetErrorString(e_),  \
+                               __FILE__, __LINE__);                                            \
+    } while (0)
+
+// Device error word bits (each kernel family keeps its own word).
+enum : unsigned { ERRBIT_TOKEN_RANGE = 1u, ERRBIT_TIMEOUT = 2u };
+
+// Read and clear the error words of every kernel family on the current device.
+unsigned read_clear_simt_errors();
+unsigned read_clear_gemm_errors();
+unsigned read_clear_attn_errors();
+
+// ----------------------------------------------------------------------------- timing
+// Brackets one kernel launch with the timer events of `kind` (if enabled) and
+// counts the launch.
+struct LaunchScope {
+    LaunchScope(int kind, cudaStream_t s);
+    ~LaunchScope();
+    int kind;
+    cudaStream_t stream;
+    int slot;
+};
+
+int num_sms();
+size_t align_up(size_t x, size_t a);
+
+// ----------------------------------------------------------------------------- tensor maps
+// 2-D row-major tensor [rows, cols] (cols contiguous, row stride ld elements),
+// box [box_rows, box_cols], 128-byte swizzle.  Returns false on failure.
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elt_bytes,
+                  uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows, uint32_t box_cols);
+
+// ----------------------------------------------------------------------------- SIMT kernels
+cudaError_t launch_embed(const uint32_t* tokens, int T, int V, int d, const void* table,
+                         int table_dtype, float* x, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype, int rows,
+                           int cols, float eps, cudaStream_t s);
+cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
+                                const int32_t* pos, int T, int n_heads, int head_dim,
+                                int rope_dims, float freq_base, float eps, cudaStream_t s);
+cudaError_t launch_rope_table(float2* tab, int T, int rope_dims, float freq_base,
+                              cudaStream_t s);
+cudaError_t launch_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
+                          cudaStream_t s);
+cudaError_t launch_swiglu_interleaved64(const float* gu, float* act, int T, int F,
+                                        cudaStream_t s);
+cudaError_t launch_gemm_simt(const float* x, int ldx, const float* W, void* y, int y_dtype,
+                             int ldy, int M, int N, int K, const float* residual,
+                             cudaStream_t s, int kind);
+// Causal GQA attention on SIMT cores.  dtype of q/k/v/out: DTP_F32 or DTP_BF16.
+// v_t != 0: v is stored transposed [n_head_kv*head_dim, ldv_t] (key index contiguous).
+cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, const void* v,
+                             int ldv, int v_t, void* out, int ldo, int dtype, int T,
+                             int n_head, int n_head_kv, int head_dim, float scale,
+                             cudaStream_t s);
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, __nv_bfloat16* vt, int T, int width,
+                               int ldt, cudaStream_t s);
+cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_bf16,
+                               int mode, cudaStream_t s);
+cudaError_t launch_copy_f32(const float* src, float* dst, size_t n, cudaStream_t s);
+
+// ----------------------------------------------------------------------------- tcgen05 GEMM
+enum GemmEpi {
+    EPI_STORE = 0,    // y = acc (+ residual), y f32 or bf16
+    EPI_QKV = 1,      // q/k: per-head RMSNorm + NeoX RoPE -> bf16; v -> bf16 transposed
+    EPI_SWIGLU = 2,   // gate/up interleaved in 64-column blocks -> silu(g)*u bf16
+};
+
+struct GemmEpiArgs {
+    // EPI_STORE
+    void* y = nullptr;
+    int y_dtype = DTP_F32;
+    long long ldy = 0;
+    const float* residual = nullptr;    // f32 [M, ldy] (may alias y)
+    // EPI_QKV
+    __nv_bfloat16* q = nullptr;         // [M, n_head*hd]
+    __nv_bfloat16* k = nullptr;         // [M, n_head_kv*hd]
+    __nv_bfloat16* vt = nullptr;        // [n_head_kv*hd, ldvt]
+    long long ldvt = 0;
+    const float* q_norm = nullptr;
+    const float* k_norm = nullptr;
+    const float2* rope = nullptr;       // [M, rope_dims/2] (cos, sin)
+    int n_head = 0, n_head_kv = 0, head_dim = 0, rope_dims = 0;
+    float eps = 0.f;
+    // EPI_SWIGLU
+    __nv_bfloat16* act = nullptr;       // [M, N/2]
+};
+
+// y-side work of one GEMM: x [M, K] bf16 (row stride K), W [N, K] bf16.
+cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,
+                           GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind);
+
+// ----------------------------------------------------------------------------- tcgen05 attention
+// q [T, n_head*hd] bf16, k [T, n_head_kv*hd] bf16, vt [n_head_kv*hd, ldvt] bf16,
+// out [T, n_head*hd] bf16.
+cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                           const __nv_bfloat16* vt, long long ldvt, __nv_bfloat16* out, int T,
+                           int n_head, int n_head_kv, int head_dim, float scale, cudaStream_t s);
+bool attn_tc_supported(int n_head, int n_head_kv, int head_dim);
+
+}  // namespace dtp

@@ -1,0 +1,496 @@
+// SIMT kernels of the prefill pass: embedding gather, RMSNorm, per-head
+// QK-norm + NeoX RoPE, the RoPE angle table, SwiGLU, the float32 GEMM and the
+// float32/bf16 causal GQA attention used by the exact (float32) path, and the
+// weight-packing conversions.
+//
+// Steps follow "docs.rs memra-engine 0.130.0, src/forward.rs", Model::forward.
+#include <math.h>
+
+#include "internal.h"
+
+namespace dtp {
+
+static __device__ unsigned g_simt_err = 0;
+
+unsigned read_clear_simt_errors() {
+    unsigned v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_simt_err, sizeof(v)) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_simt_err, &z, sizeof(z));
+    return v;
+}
+
+__device__ __forceinline__ float ld_elt(const float* p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_elt(const __nv_bfloat16* p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_elt(float* p, size_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void st_elt(__nv_bfloat16* p, size_t i, float v) {
+    p[i] = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Block-wide sum in a fixed order (deterministic).
+__device__ float block_sum(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < nw; ++i) t += red[i];
+    return t;
+}
+
+// ----------------------------------------------------------------------------- embedding
+// forward.rs: `x = self.embed_tokens(e, tokens)` -- row t of x is row tokens[t]
+// of the embedding table.  An id >= V raises the token-range error bit and
+// leaves a zero row.
+template <typename Tt>
+__global__ void embed_kernel(const uint32_t* __restrict__ tokens, int V, int d,
+                             const Tt* __restrict__ table, float* __restrict__ x) {
+    const int t = blockIdx.x;
+    const uint32_t id = tokens[t];
+    float* xr = x + (size_t)t * d;
+    if (id >= (uint32_t)V) {
+        if (threadIdx.x == 0) atomicOr(&g_simt_err, ERRBIT_TOKEN_RANGE);
+        for (int c = threadIdx.x; c < d; c += blockDim.x) xr[c] = 0.f;
+        return;
+    }
+    const Tt* src = table + (size_t)id * d;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) xr[c] = ld_elt(src, c);
+}
+
+cudaError_t launch_embed(const uint32_t* tokens, int T, int V, int d, const void* table,
+                         int table_dtype, float* x, cudaStream_t s) {
+    LaunchScope ls(DTP_K_EMBED, s);
+    int threads = d >= 256 ? 256 : 64;
+    if (table_dtype == DTP_BF16)
+        embed_kernel<<<T, threads, 0, s>>>(tokens, V, d, (const __nv_bfloat16*)table, x);
+    else
+        embed_kernel<<<T, threads, 0, s>>>(tokens, V, d, (const float*)table, x);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- RMSNorm
+// forward.rs: `e.rms_norm(x, w, out, ncols, nrows, eps)` -- one block per row.
+template <typename To>
+__global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                               To* __restrict__ y, int cols, float eps) {
+    __shared__ float red[32];
+    const size_t r = blockIdx.x;
+    const float* xr = x + r * cols;
+    To* yr = y + r * cols;
+    float ss = 0.f;
+    const bool vec = (cols & 3) == 0;
+    if (vec) {
+        for (int c = threadIdx.x * 4; c < cols; c += blockDim.x * 4) {
+            float4 v = *reinterpret_cast<const float4*>(xr + c);
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+    } else {
+        for (int c = threadIdx.x; c < cols; c += blockDim.x) ss += xr[c] * xr[c];
+    }
+    ss = block_sum(ss, red);
+    const float rstd = 1.0f / sqrtf(ss / (float)cols + eps);
+    if (vec) {
+        for (int c = threadIdx.x * 4; c < cols; c += blockDim.x * 4) {
+            float4 v = *reinterpret_cast<const float4*>(xr + c);
+            float4 g = *reinterpret_cast<const float4*>(w + c);
+            st_elt(yr, c + 0, v.x * rstd * g.x);
+            st_elt(yr, c + 1, v.y * rstd * g.y);
+            st_elt(yr, c + 2, v.z * rstd * g.z);
+            st_elt(yr, c + 3, v.w * rstd * g.w);
+        }
+    } else {
+        for (int c = threadIdx.x; c < cols; c += blockDim.x) st_elt(yr, c, xr[c] * rstd * w[c]);
+    }
+}
+
+cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype, int rows,
+                           int cols, float eps, cudaStream_t s) {
+    LaunchScope ls(DTP_K_RMSNORM, s);
+    int threads = cols >= 1024 ? 256 : (cols >= 256 ? 128 : 32);
+    if (y_dtype == DTP_BF16)
+        rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (__nv_bfloat16*)y, cols, eps);
+    else
+        rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (float*)y, cols, eps);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- RoPE angles
+// cos/sin of angle = pos * base^(-2i/r), computed in float64 and rounded to
+// float32 (forward.rs `rope_neox(..., rope_dim_count, ..., freq_base, 1.0)`).
+__device__ __forceinline__ float2 rope_cs(double pos, int i, int rope_dims, double base) {
+    const double theta = pow(base, -2.0 * (double)i / (double)rope_dims);
+    double sn, cs;
+    sincos(pos * theta, &sn, &cs);
+    return make_float2((float)cs, (float)sn);
+}
+
+__global__ void rope_table_kernel(float2* tab, int T, int half, int rope_dims, double base) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= T * half) return;
+    const int t = idx / half, i = idx % half;
+    tab[idx] = rope_cs((double)t, i, rope_dims, base);
+}
+
+cudaError_t launch_rope_table(float2* tab, int T, int rope_dims, float freq_base,
+                              cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    const int half = rope_dims / 2, n = T * half;
+    rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(tab, T, half, rope_dims, (double)freq_base);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- QK-norm + RoPE
+// One block per token; one warp per (token, head) row.  forward.rs: q/k
+// `rms_norm(ncols = head_dim, nrows = heads*T)` then `rope_neox`.
+template <typename Tx>
+__global__ void qk_norm_rope_kernel(Tx* __restrict__ x, int ld, const float* __restrict__ w,
+                                    const int32_t* __restrict__ pos, int n_heads, int hd,
+                                    int rope_dims, double base, float eps) {
+    extern __shared__ float sm[];
+    const int t = blockIdx.x, half = rope_dims / 2;
+    float2* cs = reinterpret_cast<float2*>(sm);                 // [half]
+    float* rowbuf = sm + 2 * half;                              // [warps][hd]
+    const double p = pos ? (double)pos[t] : (double)t;
+    for (int i = threadIdx.x; i < half; i += blockDim.x) cs[i] = rope_cs(p, i, rope_dims, base);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    float* rb = rowbuf + warp * hd;
+    for (int h = warp; h < n_heads; h += nw) {
+        Tx* row = x + (size_t)t * ld + (size_t)h * hd;
+        float ss = 0.f;
+        for (int e = lane; e < hd; e += 32) {
+            float v = ld_elt(row, e);
+            rb[e] = v;
+            ss += v * v;
+        }
+        ss = warp_sum(ss);
+        const float rstd = w ? 1.0f / sqrtf(ss / (float)hd + eps) : 1.0f;
+        __syncwarp();
+        for (int e = lane; e < hd; e += 32) rb[e] = w ? rb[e] * rstd * w[e] : rb[e];
+        __syncwarp();
+        for (int e = lane; e < hd; e += 32) {
+            float y;
+            if (e < half) {
+                const float2 c = cs[e];
+                y = rb[e] * c.x - rb[e + half] * c.y;
+            } else if (e < rope_dims) {
+                const float2 c = cs[e - half];
+                y = rb[e - half] * c.y + rb[e] * c.x;
+            } else {
+                y = rb[e];
+            }
+            st_elt(row, e, y);
+        }
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
+                                const int32_t* pos, int T, int n_heads, int head_dim,
+                                int rope_dims, float freq_base, float eps, cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    int warps = n_heads < 8 ? n_heads : 8;
+    size_t smem = (size_t)(rope_dims + warps * head_dim) * sizeof(float);
+    if (dtype == DTP_BF16)
+        qk_norm_rope_kernel<<<T, warps * 32, smem, s>>>((__nv_bfloat16*)x, ld, w_norm, pos,
+                                                        n_heads, head_dim, rope_dims,
+                                                        (double)freq_base, eps);
+    else
+        qk_norm_rope_kernel<<<T, warps * 32, smem, s>>>((float*)x, ld, w_norm, pos, n_heads,
+                                                        head_dim, rope_dims, (double)freq_base,
+                                                        eps);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- SwiGLU
+// forward.rs `ffn_act`: act = silu(gate) * up, silu(x) = x / (1 + e^-x).
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+template <typename T>
+__global__ void swiglu_kernel(const T* __restrict__ g, const T* __restrict__ u, T* __restrict__ o,
+                              size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        st_elt(o, i, silu_f(ld_elt(g, i)) * ld_elt(u, i));
+}
+
+cudaError_t launch_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
+                          cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    size_t blocks = (n + 255) / 256;
+    if (blocks > 65535 * 8) blocks = 65535 * 8;
+    if (dtype == DTP_BF16)
+        swiglu_kernel<<<(unsigned)blocks, 256, 0, s>>>((const __nv_bfloat16*)gate,
+                                                       (const __nv_bfloat16*)up,
+                                                       (__nv_bfloat16*)out, n);
+    else
+        swiglu_kernel<<<(unsigned)blocks, 256, 0, s>>>((const float*)gate, (const float*)up,
+                                                       (float*)out, n);
+    return cudaGetLastError();
+}
+
+// gu [T, 2F] holds gate/up interleaved in 64-column blocks (block b: gate
+// columns 64b..64b+63 then up columns 64b..64b+63); act [T, F].
+__global__ void swiglu_interleaved64_kernel(const float* __restrict__ gu, float* __restrict__ act,
+                                            int T, int F) {
+    const size_t n = (size_t)T * F;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t t = i / F;
+        const int f = (int)(i % F);
+        const size_t base = t * 2 * F + (size_t)(f / 64) * 128 + (f % 64);
+        act[i] = silu_f(gu[base]) * gu[base + 64];
+    }
+}
+
+cudaError_t launch_swiglu_interleaved64(const float* gu, float* act, int T, int F,
+                                        cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    size_t n = (size_t)T * F, blocks = (n + 255) / 256;
+    if (blocks > 65535 * 8) blocks = 65535 * 8;
+    swiglu_interleaved64_kernel<<<(unsigned)blocks, 256, 0, s>>>(gu, act, T, F);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- f32 GEMM
+// y[M, N] = x[M, K] W[N, K]^T (+ residual): 64x64 tile per block, 256 threads,
+// 4x4 outputs per thread, K in steps of 16; accumulation order k = 0..K-1.
+constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16;
+
+template <typename To>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict__ x, int ldx,
+                                                        const float* __restrict__ W,
+                                                        To* __restrict__ y, int ldy, int M, int N,
+                                                        int K, const float* residual) {
+    __shared__ float As[SG_BK][SG_BM + 4];
+    __shared__ float Bs[SG_BK][SG_BN + 4];
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    const int m0 = blockIdx.y * SG_BM, n0 = blockIdx.x * SG_BN;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < K; k0 += SG_BK) {
+        for (int i = threadIdx.x; i < SG_BM * SG_BK; i += 256) {
+            const int r = i / SG_BK, c = i % SG_BK;
+            const int gm = m0 + r, gk = k0 + c;
+            As[c][r] = (gm < M && gk < K) ? x[(size_t)gm * ldx + gk] : 0.f;
+            const int gn = n0 + r;
+            Bs[c][r] = (gn < N && gk < K) ? W[(size_t)gn * K + gk] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < SG_BK; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int gm = m0 + ty * 4 + i;
+        if (gm >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gn = n0 + tx * 4 + j;
+            if (gn >= N) continue;
+            float v = acc[i][j];
+            if (residual) v += residual[(size_t)gm * ldy + gn];
+            st_elt(y, (size_t)gm * ldy + gn, v);
+        }
+    }
+}
+
+cudaError_t launch_gemm_simt(const float* x, int ldx, const float* W, void* y, int y_dtype,
+                             int ldy, int M, int N, int K, const float* residual,
+                             cudaStream_t s, int kind) {
+    LaunchScope ls(kind, s);
+    dim3 grid((N + SG_BN - 1) / SG_BN, (M + SG_BM - 1) / SG_BM);
+    if (y_dtype == DTP_BF16)
+        gemm_simt_kernel<<<grid, 256, 0, s>>>(x, ldx, W, (__nv_bfloat16*)y, ldy, M, N, K,
+                                              residual);
+    else
+        gemm_simt_kernel<<<grid, 256, 0, s>>>(x, ldx, W, (float*)y, ldy, M, N, K, residual);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- SIMT attention
+// forward.rs `e.sdpa_naive(q, k, v, attn, head_dim, n_head, n_head_kv, t, t,
+// scale, true)`: one warp per (query t, head i); keys in chunks of 32 (one
+// per lane), online softmax in float32 with expf.  kv head = i / (h / g).
+template <typename T, bool VT>
+__global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __restrict__ k,
+                                 int ldk, const T* __restrict__ v, int ldv, T* __restrict__ out,
+                                 int ldo, int Tn, int n_head, int n_head_kv, int hd, float scale) {
+    extern __shared__ float sm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+    const int head = blockIdx.y;
+    const int kvh = head / (n_head / n_head_kv);
+    float* qs = sm + warp * hd;
+    if (t >= Tn) return;
+    for (int e = lane; e < hd; e += 32) qs[e] = ld_elt(q, (size_t)t * ldq + (size_t)head * hd + e);
+    __syncwarp();
+    constexpr int MAXD = 8;                 // hd <= 256
+    float acc[MAXD];
+#pragma unroll
+    for (int j = 0; j < MAXD; ++j) acc[j] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    for (int s0 = 0; s0 <= t; s0 += 32) {
+        const int s = s0 + lane;
+        float sc = -INFINITY;
+        if (s <= t) {
+            const T* kr = k + (size_t)s * ldk + (size_t)kvh * hd;
+            float dot = 0.f;
+            for (int e = 0; e < hd; ++e) dot = fmaf(qs[e], ld_elt(kr, e), dot);
+            sc = dot * scale;
+        }
+        const float mc = warp_max(sc);
+        const float mn = fmaxf(m, mc);
+        const float alpha = expf(m - mn);     // m = -inf on the first chunk -> 0
+        const float p = (s <= t) ? expf(sc - mn) : 0.f;
+        l = l * alpha + warp_sum(p);
+#pragma unroll
+        for (int j = 0; j < MAXD; ++j) acc[j] *= alpha;
+        const int nk = min(32, t - s0 + 1);
+        for (int jj = 0; jj < nk; ++jj) {
+            const float pj = __shfl_sync(0xffffffffu, p, jj);
+            const int sk = s0 + jj;
+#pragma unroll
+            for (int j = 0; j < MAXD; ++j) {
+                const int e = lane + 32 * j;
+                if (e < hd) {
+                    const float vv = VT ? ld_elt(v, (size_t)(kvh * hd + e) * ldv + sk)
+                                        : ld_elt(v, (size_t)sk * ldv + (size_t)kvh * hd + e);
+                    acc[j] = fmaf(pj, vv, acc[j]);
+                }
+            }
+        }
+        m = mn;
+    }
+    const float inv = 1.0f / l;
+#pragma unroll
+    for (int j = 0; j < MAXD; ++j) {
+        const int e = lane + 32 * j;
+        if (e < hd) st_elt(out, (size_t)t * ldo + (size_t)head * hd + e, acc[j] * inv);
+    }
+}
+
+cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, const void* v,
+                             int ldv, int v_t, void* out, int ldo, int dtype, int T,
+                             int n_head, int n_head_kv, int head_dim, float scale,
+                             cudaStream_t s) {
+    LaunchScope ls(DTP_K_ATTN, s);
+    const int warps = 4;
+    dim3 grid((T + warps - 1) / warps, n_head);
+    size_t smem = (size_t)warps * head_dim * sizeof(float);
+    if (dtype == DTP_BF16) {
+        using B = __nv_bfloat16;
+        if (v_t)
+            attn_simt_kernel<B, true><<<grid, warps * 32, smem, s>>>(
+                (const B*)q, ldq, (const B*)k, ldk, (const B*)v, ldv, (B*)out, ldo, T, n_head,
+                n_head_kv, head_dim, scale);
+        else
+            attn_simt_kernel<B, false><<<grid, warps * 32, smem, s>>>(
+                (const B*)q, ldq, (const B*)k, ldk, (const B*)v, ldv, (B*)out, ldo, T, n_head,
+                n_head_kv, head_dim, scale);
+    } else {
+        if (v_t)
+            attn_simt_kernel<float, true><<<grid, warps * 32, smem, s>>>(
+                (const float*)q, ldq, (const float*)k, ldk, (const float*)v, ldv, (float*)out,
+                ldo, T, n_head, n_head_kv, head_dim, scale);
+        else
+            attn_simt_kernel<float, false><<<grid, warps * 32, smem, s>>>(
+                (const float*)q, ldq, (const float*)k, ldk, (const float*)v, ldv, (float*)out,
+                ldo, T, n_head, n_head_kv, head_dim, scale);
+    }
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- v transpose
+// v [T, width] -> vt [width, ldt] (key index contiguous), 32x32 tiles via smem.
+__global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v,
+                                   __nv_bfloat16* __restrict__ vt, int T, int width, int ldt) {
+    __shared__ __nv_bfloat16 tile[32][33];
+    const int t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int t = t0 + i, c = c0 + threadIdx.x;
+        tile[i][threadIdx.x] = (t < T && c < width) ? v[(size_t)t * width + c] : __float2bfloat16(0.f);
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i, t = t0 + threadIdx.x;
+        if (c < width && t < T) vt[(size_t)c * ldt + t] = tile[threadIdx.x][i];
+    }
+}
+
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, __nv_bfloat16* vt, int T, int width,
+                               int ldt, cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    dim3 grid((T + 31) / 32, (width + 31) / 32), block(32, 8);
+    transpose_v_kernel<<<grid, block, 0, s>>>(v, vt, T, width, ldt);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- packing
+// dst row for source row r: mode 0 -> r; mode 1 (gate) -> 128*(r/64) + r%64;
+// mode 2 (up) -> 128*(r/64) + 64 + r%64.
+template <typename To>
+__global__ void pack_matrix_kernel(const float* __restrict__ src, int rows, int cols,
+                                   To* __restrict__ dst, int mode) {
+    const size_t n = (size_t)rows * cols;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / cols), c = (int)(i % cols);
+        int dr = r;
+        if (mode == 1) dr = 128 * (r / 64) + (r % 64);
+        if (mode == 2) dr = 128 * (r / 64) + 64 + (r % 64);
+        st_elt(dst, (size_t)dr * cols + c, src[i]);
+    }
+}
+
+cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_bf16,
+                               int mode, cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    size_t n = (size_t)rows * cols, blocks = (n + 255) / 256;
+    if (blocks > 65535 * 16) blocks = 65535 * 16;
+    if (to_bf16)
+        pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (__nv_bfloat16*)dst,
+                                                            mode);
+    else
+        pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (float*)dst, mode);
+    return cudaGetLastError();
+}
+
+__global__ void copy_f32_kernel(const float* __restrict__ a, float* __restrict__ b, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        b[i] = a[i];
+}
+
+cudaError_t launch_copy_f32(const float* src, float* dst, size_t n, cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    size_t blocks = (n + 255) / 256;
+    if (blocks > 65535 * 8) blocks = 65535 * 8;
+    copy_f32_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, n);
+    return cudaGetLastError();
+}
+
+}  // namespace dtp

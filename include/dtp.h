@@ -1,0 +1,254 @@
+/*
+ * dtp.h -- C ABI of the GB300 (sm_103a) dense-transformer prefill library.
+ *
+ * The library computes the whole-sequence (prefill) forward pass of a
+ * Qwen3-style dense decoder stack as stated on the page "docs.rs memra-engine
+ * 0.130.0, src/forward.rs" (`Model::forward`):
+ *
+ *   x = tok_embd[tokens]                                  [T, n_embd]
+ *   per layer:
+ *     h    = rms_norm(x) * attn_norm
+ *     q,k,v = h Wq^T, h Wk^T, h Wv^T                      [T, heads*head_dim]
+ *     q,k  = rms_norm over each head_dim row * q_norm / k_norm
+ *     q,k  = NeoX RoPE at positions 0..T-1 (rope_dim_count, rope_freq_base)
+ *     attn = causal GQA softmax(q k^T / sqrt(head_dim)) v
+ *     x    = x + attn Wo^T
+ *     z    = rms_norm(x) * ffn_norm
+ *     x    = x + (silu(z Wg^T) * (z Wu^T)) Wd^T
+ *   logits = (rms_norm(x) * output_norm) Wout^T           [T, n_vocab] float32
+ *
+ * Conventions for every entry point:
+ *   - Pointers documented "device" point to device memory of the current CUDA
+ *     device; "host" pointers to host memory.  The caller allocates and owns
+ *     every buffer; the library never frees caller memory and allocates no
+ *     device memory on the forward path.
+ *   - Matrices are row-major.  Activations are token-major [T, features]; a
+ *     weight is [out_features, in_features] and a projection is y = x W^T.
+ *   - Work is enqueued asynchronously on `stream` (NULL = the legacy default
+ *     stream).  The return value reports argument validation and launch
+ *     errors only; faults detected on the device (a token id out of range, a
+ *     bounded pipeline wait that gave up) raise a device error word that
+ *     dtp_check() reports after synchronising the stream.
+ *   - Every function returns DTP_OK (0) or a negative DTP_ERR_* code and, on
+ *     error, sets a message readable with dtp_last_error() (per thread).
+ */
+#ifndef DTP_H
+#define DTP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* dtp_stream_t;
+
+enum {
+    DTP_OK = 0,
+    DTP_ERR_INVALID_ARG = -1,    /* null pointer, non-positive size, inconsistent shape       */
+    DTP_ERR_UNSUPPORTED = -2,    /* valid shape that this build's kernels do not tile         */
+    DTP_ERR_TOKEN_RANGE = -3,    /* a token id >= n_vocab                                     */
+    DTP_ERR_WORKSPACE = -4,      /* workspace or packed buffer smaller than required          */
+    DTP_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed                         */
+    DTP_ERR_DEVICE_TIMEOUT = -6  /* a kernel's bounded wait gave up (reported by dtp_check)   */
+};
+
+/* Element type of an activation buffer. */
+enum { DTP_F32 = 0, DTP_BF16 = 1 };
+
+/* Arithmetic of the forward pass.
+ *   DTP_PREC_F32:  float32 everywhere (SIMT kernels; the pages' "all f32" stage).
+ *   DTP_PREC_BF16: bf16 GEMM/attention operands, float32 accumulation, float32
+ *                  residual stream, norms, softmax and logits (tcgen05 tensor cores). */
+enum { DTP_PREC_F32 = 0, DTP_PREC_BF16 = 2 };
+
+typedef struct dtp_config {
+    int n_layer;          /* decoder layers                                         */
+    int n_embd;           /* model width d                                          */
+    int n_head;           /* query heads h                                          */
+    int n_head_kv;        /* key/value heads g; h % g == 0 (GQA group = h / g)      */
+    int head_dim;         /* per-head width hd (even)                               */
+    int rope_dim_count;   /* rotated dims r per head, even, r <= hd                 */
+    int n_ff;             /* SwiGLU hidden width F                                  */
+    int n_vocab;          /* vocabulary V                                           */
+    float rope_freq_base; /* RoPE base; theta_i = base^(-2i/r)                      */
+    float rms_eps;        /* epsilon inside every RMSNorm's square root             */
+    int precision;        /* DTP_PREC_F32 or DTP_PREC_BF16                          */
+} dtp_config;
+
+/* One layer's source weights: device float32, the pages' layouts. */
+typedef struct dtp_layer_src {
+    const float* attn_norm; /* [n_embd]                       */
+    const float* wq;        /* [n_head*head_dim, n_embd]      */
+    const float* wk;        /* [n_head_kv*head_dim, n_embd]   */
+    const float* wv;        /* [n_head_kv*head_dim, n_embd]   */
+    const float* q_norm;    /* [head_dim]                     */
+    const float* k_norm;    /* [head_dim]                     */
+    const float* wo;        /* [n_embd, n_head*head_dim]      */
+    const float* ffn_norm;  /* [n_embd]                       */
+    const float* w_gate;    /* [n_ff, n_embd]                 */
+    const float* w_up;      /* [n_ff, n_embd]                 */
+    const float* w_down;    /* [n_embd, n_ff]                 */
+} dtp_layer_src;
+
+/* ------------------------------------------------------------------------------------
+ * Model weights: packing
+ *
+ * The forward pass reads weights from one caller-owned device buffer in the
+ * library's packed format: per layer Wq;Wk;Wv concatenated into one [(h+2g)hd, d]
+ * matrix, Wgate and Wup interleaved in blocks of 64 rows into one [2F, d] matrix,
+ * Wo, Wdown, and the four norm vectors; then tok_embd [V, d], output_norm [d]
+ * and the lm_head [V, d].  Matrices are stored as bf16 (round to nearest even)
+ * under DTP_PREC_BF16 and float32 under DTP_PREC_F32; norm vectors are float32.
+ * ------------------------------------------------------------------------------------ */
+
+/* Bytes of the packed buffer for `cfg` (0 if cfg is invalid). */
+size_t dtp_packed_size(const dtp_config* cfg);
+
+/* Convert and write layer `layer` (0 <= layer < n_layer) from `src` (device
+ * float32, all 11 pointers non-null) into `packed` (device, packed_bytes >=
+ * dtp_packed_size(cfg)).  Asynchronous on `stream`; `src` must stay valid until
+ * the stream reaches this point. */
+int dtp_pack_layer(const dtp_config* cfg, int layer, const dtp_layer_src* src, void* packed,
+                   size_t packed_bytes, dtp_stream_t stream);
+
+/* Write the token embedding tok_embd [V, d], output_norm [d] and the lm_head
+ * output [V, d] (device float32) into `packed`. */
+int dtp_pack_globals(const dtp_config* cfg, const float* tok_embd, const float* output_norm,
+                     const float* output, void* packed, size_t packed_bytes, dtp_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Forward pass  (forward.rs, `Model::forward`)
+ * ------------------------------------------------------------------------------------ */
+
+/* Bytes of device workspace dtp_fwd_prefill needs for T tokens (0 if invalid). */
+size_t dtp_workspace_size(const dtp_config* cfg, int T);
+
+/* Prefill forward over T >= 1 tokens at positions 0..T-1.
+ *   tokens   device uint32 [T], each < n_vocab (checked on the device: an id out
+ *            of range raises DTP_ERR_TOKEN_RANGE in dtp_check and its row is zero).
+ *   logits   device float32 [T, n_vocab], written.
+ *   hidden   device float32 [n_layer + 1, T, n_embd] or NULL; if given, hidden[l]
+ *            is the residual stream entering layer l and hidden[n_layer] the
+ *            stream entering output_norm.
+ *   workspace device, >= dtp_workspace_size(cfg, T) bytes, 256-byte aligned,
+ *            owned by the caller; contents on entry are ignored.
+ * Buffers may not overlap. */
+int dtp_fwd_prefill(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                    const uint32_t* tokens, int T, float* logits, float* hidden, void* workspace,
+                    size_t ws_bytes, dtp_stream_t stream);
+
+/* Bytes of device workspace dtp_fwd_prefill_host needs (the forward workspace
+ * plus device staging for the tokens and logits). */
+size_t dtp_workspace_size_host(const dtp_config* cfg, int T);
+
+/* The same pass with HOST tokens (uint32 [T]) and HOST logits (float32
+ * [T, n_vocab]): copies the tokens in, runs dtp_fwd_prefill, copies the
+ * logits out, all enqueued on `stream`; the caller synchronises the stream
+ * before reading `logits_host`.  Token ids are range-checked on the host
+ * before anything is enqueued.  Page-locked host buffers make the copies
+ * asynchronous. */
+int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                         const uint32_t* tokens_host, int T, float* logits_host, void* workspace,
+                         size_t ws_bytes, dtp_stream_t stream);
+
+/* Synchronise `stream`, then report and clear the device error words raised
+ * by this library's kernels since the last call: DTP_OK,
+ * DTP_ERR_TOKEN_RANGE, DTP_ERR_DEVICE_TIMEOUT, or DTP_ERR_CUDA (a sticky
+ * CUDA error). */
+int dtp_check(dtp_stream_t stream);
+
+/* Message for the last error raised on the calling thread ("" if none). */
+const char* dtp_last_error(void);
+
+/* ------------------------------------------------------------------------------------
+ * Per-op entry points (the steps of forward.rs `Model::forward`)
+ * ------------------------------------------------------------------------------------ */
+
+/* rms_norm (forward.rs: `e.rms_norm(x, w, out, ncols, nrows, eps)`):
+ * y[r, c] = x[r, c] / sqrt(mean_c(x[r, :]^2) + eps) * w[c].
+ * x device float32 [rows, cols]; w device float32 [cols]; y device [rows, cols]
+ * of y_dtype (DTP_F32 or DTP_BF16, bf16 rounded to nearest even).  y may alias
+ * x when y_dtype is DTP_F32. */
+int dtp_rms_norm(const float* x, const float* w, void* y, int y_dtype, int rows, int cols,
+                 float eps, dtp_stream_t stream);
+
+/* Per-head QK-RMSNorm then NeoX RoPE, in place (forward.rs: the q/k `rms_norm`
+ * with ncols = head_dim, nrows = heads*T, then `e.rope_neox(x, pos, head_dim,
+ * rope_dim_count, heads, T, freq_base, 1.0)`).
+ * x device [T, n_heads*head_dim] of dtype (DTP_F32 or DTP_BF16);
+ * w_norm device float32 [head_dim], or NULL to apply RoPE only;
+ * pos device int32 [T] positions, or NULL for 0..T-1.
+ * For each (token t, head) row: y = rms_norm(row) * w_norm, then for
+ * i < r/2 the pair (i, i + r/2) is rotated by angle pos[t] * base^(-2i/r);
+ * dims >= r are unchanged.  Arithmetic in float32 (angles in float64). */
+int dtp_qk_norm_rope_neox(void* x, int dtype, const float* w_norm, const int32_t* pos, int T,
+                          int n_heads, int head_dim, int rope_dim_count, float freq_base,
+                          float eps, dtp_stream_t stream);
+
+/* Device workspace dtp_sdpa_causal_gqa needs (0 for DTP_F32). */
+size_t dtp_sdpa_workspace_size(int T, int n_head_kv, int head_dim, int dtype);
+
+/* Causal grouped-query attention (forward.rs: `e.sdpa_naive(q, k, v, attn,
+ * head_dim, n_head, n_head_kv, T, T, scale, true)`):
+ * out[t, i] = sum_{s<=t} softmax_s(scale * q[t,i].k[s,j]) v[s,j],
+ * j = i / (n_head / n_head_kv).
+ * q, out device [T, n_head*head_dim]; k, v device [T, n_head_kv*head_dim];
+ * all of dtype.  DTP_F32: float32 SIMT kernel.  DTP_BF16: tcgen05 flash
+ * attention (bf16 operands, float32 scores/softmax/accumulation, P rounded to
+ * bf16 for the PV product); requires head_dim 64 or 128 and an even group
+ * size n_head / n_head_kv, and a workspace of dtp_sdpa_workspace_size bytes
+ * (device, 256-byte aligned). */
+int dtp_sdpa_causal_gqa(const void* q, const void* k, const void* v, void* out, int dtype, int T,
+                        int n_head, int n_head_kv, int head_dim, float scale, void* workspace,
+                        size_t ws_bytes, dtp_stream_t stream);
+
+/* SwiGLU (forward.rs `ffn_act`; the T-parallel page's `silu_mul`):
+ * out[i] = silu(gate[i]) * up[i], silu(x) = x / (1 + e^-x); n elements of
+ * dtype, arithmetic in float32.  out may alias gate or up. */
+int dtp_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
+               dtp_stream_t stream);
+
+/* Linear (forward.rs `e.matmul(&w, &x, t)`): y[M, N] = x[M, K] W[N, K]^T
+ * (+ residual[M, N]).
+ * x, W device, both of dtype: DTP_F32 -> float32 SIMT kernel; DTP_BF16 ->
+ * tcgen05 tensor cores with float32 accumulation (K % 8 == 0).
+ * y device of y_dtype (DTP_F32 or DTP_BF16).  residual: device float32
+ * [M, N] or NULL; when given, y_dtype must be DTP_F32 and y = residual + x W^T;
+ * residual may alias y (in-place residual add). */
+int dtp_linear(const void* x, const void* W, void* y, int dtype, int y_dtype, int M, int N, int K,
+               const float* residual, dtp_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Kernel timing (measurement aid; off by default)
+ * ------------------------------------------------------------------------------------ */
+
+/* Kernel kinds of the forward pass. */
+enum {
+    DTP_K_EMBED = 0, DTP_K_RMSNORM = 1, DTP_K_GEMM_QKV = 2, DTP_K_ATTN = 3, DTP_K_GEMM_O = 4,
+    DTP_K_GEMM_GATEUP = 5, DTP_K_GEMM_DOWN = 6, DTP_K_GEMM_LMHEAD = 7, DTP_K_OTHER = 8,
+    DTP_K_COUNT = 9
+};
+
+/* Start recording a CUDA event pair around each launch of every kernel kind
+ * in `kind_mask` (bit k = kind k), up to `capacity` launches per kind.  Creates
+ * the events (no device memory).  Replaces any earlier recording. */
+int dtp_timer_enable(unsigned kind_mask, int capacity);
+
+/* Stop recording and destroy the events. */
+int dtp_timer_disable(void);
+
+/* After the recorded work has completed: number of recorded launches of
+ * `kind` and their summed duration in milliseconds. */
+int dtp_timer_read(int kind, int* count, float* total_ms);
+
+/* Launch counter: kernels this library has launched on the calling process
+ * since the last reset (every kernel of every entry point). */
+long long dtp_launch_count(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DTP_H */

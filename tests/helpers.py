@@ -1,0 +1,35 @@
+"""Shared test helpers: load synthetic weights into the GPU model, run the oracle,
+and the parity metrics (relative L2, max abs, argmax agreement)."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def argmax_agreement(gpu_logits, ref_logits) -> float:
+    return float(np.mean(np.argmax(np.asarray(gpu_logits), 1) == np.argmax(np.asarray(ref_logits), 1)))
+
+
+def load_model(dtp, cfg, seed=0):
+    """GPU Model with every tensor from the seeded generator."""
+    m = dtp.Model(cfg)
+    for l in range(cfg.n_layer):
+        m.load_layer(l, synth.layer_weights(cfg, l, seed))
+    m.load_globals(synth.tok_embd(cfg, seed), synth.output_norm(cfg, seed), synth.output_weight(cfg, seed))
+    return m
+
+
+def oracle_forward(cfg, seed=0, T=None, bf16=None):
+    bf16 = (cfg.precision == "bf16") if bf16 is None else bf16
+    w = synth.model_weights(cfg, seed)
+    toks = synth.tokens(cfg, seed, T)
+    logits, hidden = oracle.forward(cfg, w, toks, bf16_operands=bf16, return_hidden=True)
+    return toks, logits, hidden

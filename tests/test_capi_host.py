@@ -1,0 +1,82 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/dtp.h declares, and rejects bad arguments on the host before touching
+the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dtp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dtp_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("dtp_fwd_prefill", "dtp_rms_norm", "dtp_qk_norm_rope_neox", "dtp_sdpa_causal_gqa",
+              "dtp_swiglu", "dtp_linear", "dtp_check", "dtp_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(dtp):
+    lib = ctypes.CDLL(dtp.build())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def _cfg(dtp, name="small", **kw):
+    return dtp.config_from(synth.CONFIGS[name].replace(**kw))
+
+
+def test_sizes_and_config_validation(dtp):
+    c = _cfg(dtp)
+    assert dtp.packed_size(c) > 0 and dtp.workspace_size(c, 256) > 0
+    assert dtp.workspace_size_host(c, 256) > dtp.workspace_size(c, 256)
+    assert dtp.workspace_size(c, 0) == 0
+    for bad in (dict(n_head=7), dict(rope_dim_count=3), dict(rope_dim_count=200), dict(n_embd=0),
+                dict(head_dim=48)):   # 48: not tiled by the bf16 path
+        assert dtp.packed_size(_cfg(dtp, **bad)) == 0
+        assert dtp.last_error()
+    # float32 path accepts any even head_dim
+    assert dtp.packed_size(_cfg(dtp, head_dim=48, rope_dim_count=48, precision="f32")) > 0
+
+
+def test_packed_size_is_the_sum_of_tensors(dtp):
+    cfg = synth.CONFIGS["qwen3-8b-shape"]
+    n = dtp.packed_size(dtp.config_from(cfg))
+    params = cfg.n_layer * (cfg.n_qkv * cfg.n_embd + cfg.n_embd * cfg.n_head * cfg.head_dim
+                            + 3 * cfg.n_ff * cfg.n_embd) + 2 * cfg.n_vocab * cfg.n_embd
+    assert 2 * params <= n <= 2 * params + 4 * (cfg.n_layer * (2 * cfg.n_embd + 2 * cfg.head_dim)
+                                                + cfg.n_embd) + 256 * (12 * cfg.n_layer + 3)
+
+
+def test_host_side_rejections(dtp):
+    L = dtp.lib()
+    c = _cfg(dtp)
+    fake = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails validation first
+    assert L.dtp_fwd_prefill(None, fake, 1 << 40, fake, 4, fake, None, fake, 1 << 40, None) == -1
+    assert L.dtp_fwd_prefill(ctypes.byref(c), fake, 1 << 40, fake, 0, fake, None, fake, 1 << 40, None) == -1
+    assert L.dtp_fwd_prefill(ctypes.byref(c), None, 1 << 40, fake, 4, fake, None, fake, 1 << 40, None) == -1
+    assert L.dtp_fwd_prefill(ctypes.byref(c), fake, 16, fake, 4, fake, None, fake, 1 << 40, None) == -4
+    assert L.dtp_fwd_prefill(ctypes.byref(c), fake, 1 << 40, fake, 4, fake, None, fake, 16, None) == -4
+    assert "workspace" in dtp.last_error()
+    toks = (ctypes.c_uint32 * 4)(1, 2, 40000, 3)       # 40000 >= n_vocab 32000
+    logits = (ctypes.c_float * 4)()
+    assert L.dtp_fwd_prefill_host(ctypes.byref(c), fake, 1 << 40, toks, 4, logits, fake, 1 << 40, None) == -3
+    assert "40000" in dtp.last_error()
+    assert L.dtp_rms_norm(None, fake, fake, 0, 4, 4, 1e-6, None) == -1
+    assert L.dtp_rms_norm(fake, fake, fake, 0, 0, 4, 1e-6, None) == -1
+    assert L.dtp_qk_norm_rope_neox(fake, 0, None, None, 4, 2, 16, 17, 1e4, 1e-6, None) == -1
+    assert L.dtp_sdpa_causal_gqa(fake, fake, fake, fake, 0, 8, 6, 4, 16, 0.25, None, 0, None) == -1
+    assert L.dtp_sdpa_causal_gqa(fake, fake, fake, fake, 1, 8, 8, 8, 32, 0.25, None, 0, None) == -2
+    assert L.dtp_linear(fake, fake, fake, 0, 0, 0, 4, 4, None, None) == -1
+    assert L.dtp_linear(fake, fake, fake, 1, 1, 4, 4, 4, fake, None) == -1   # residual needs f32 out
+    assert L.dtp_linear(fake, fake, fake, 1, 0, 4, 4, 12, None, None) == -2  # K % 8
+    assert L.dtp_timer_read(99, None, None) == -1

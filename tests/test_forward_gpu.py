@@ -1,0 +1,109 @@
+"""Whole-forward parity: dtp_fwd_prefill against the oracle on every model
+configuration, plus properties that hold at any size (causality, determinism,
+device-side token checks).
+
+Bars: float32 path -- per-layer hidden-state relative L2 <= 1e-5.
+bf16 path (compared with the oracle's bf16-operand mode) -- per-layer relative
+L2 <= 2e-3, final-logit max |diff| <= 5e-2, argmax agreement >= 99.5%."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import argmax_agreement, load_model, oracle_forward, rel_l2
+
+pytestmark = pytest.mark.gpu
+dev = torch.device("cuda")
+
+
+def run_gpu(dtp, cfg, seed=0, T=None, model=None):
+    m = model or load_model(dtp, cfg, seed)
+    toks = torch.as_tensor(synth.tokens(cfg, seed, T).astype(np.int32), device=dev)
+    logits, hidden = m.forward(toks, hidden=True)
+    torch.cuda.synchronize()
+    dtp.check()
+    return m, logits.cpu().numpy(), hidden.cpu().numpy()
+
+
+def assert_parity(cfg, gl, gh, rl, rh):
+    layer_err = [rel_l2(gh[l], rh[l]) for l in range(cfg.n_layer + 1)]
+    if cfg.precision == "f32":
+        assert max(layer_err) <= 1e-5, layer_err
+        assert rel_l2(gl, rl) <= 1e-5
+    else:
+        assert max(layer_err) <= 2e-3, layer_err
+        assert np.max(np.abs(gl - rl)) <= 5e-2
+        assert argmax_agreement(gl, rl) >= 0.995
+
+
+def test_tiny_f32(dtp):
+    cfg = synth.CONFIGS["tiny"]
+    _, gl, gh = run_gpu(dtp, cfg)
+    _, rl, rh = oracle_forward(cfg)
+    assert_parity(cfg, gl, gh, rl, rh)
+
+
+@pytest.mark.parametrize("T", [1, 7, 129])
+def test_tiny_ragged_lengths(dtp, T):
+    cfg = synth.CONFIGS["tiny"]
+    _, gl, gh = run_gpu(dtp, cfg, T=T)
+    _, rl, rh = oracle_forward(cfg, T=T)
+    assert_parity(cfg, gl, gh, rl, rh)
+
+
+@pytest.mark.parametrize("prec", ["f32", "bf16"])
+def test_small(dtp, prec):
+    cfg = synth.CONFIGS["small"].replace(precision=prec)
+    _, gl, gh = run_gpu(dtp, cfg)
+    _, rl, rh = oracle_forward(cfg)
+    assert_parity(cfg, gl, gh, rl, rh)
+
+
+@pytest.mark.parametrize("T", [1, 100, 385])
+def test_small_bf16_ragged(dtp, T):
+    cfg = synth.CONFIGS["small"]
+    _, gl, gh = run_gpu(dtp, cfg, T=T)
+    _, rl, rh = oracle_forward(cfg, T=T)
+    assert_parity(cfg, gl, gh, rl, rh)
+
+
+def test_small_bf16_partial_rotary(dtp):
+    cfg = synth.CONFIGS["small"].replace(n_head=4, n_head_kv=2, head_dim=128, rope_dim_count=64,
+                                         n_layer=2)
+    _, gl, gh = run_gpu(dtp, cfg, T=200)
+    _, rl, rh = oracle_forward(cfg, T=200)
+    assert_parity(cfg, gl, gh, rl, rh)
+
+
+def test_qwen3_0p6b_shape(dtp):
+    cfg = synth.CONFIGS["qwen3-0.6b-shape"]
+    _, gl, gh = run_gpu(dtp, cfg)
+    _, rl, rh = oracle_forward(cfg)
+    assert_parity(cfg, gl, gh, rl, rh)
+
+
+def test_causality_and_determinism(dtp):
+    cfg = synth.CONFIGS["small"]
+    m = load_model(dtp, cfg)
+    toks = synth.tokens(cfg)
+    t1 = torch.as_tensor(toks.astype(np.int32), device=dev)
+    a = m.forward(t1).cpu().numpy()
+    b = m.forward(t1).cpu().numpy()
+    assert np.array_equal(a, b)                      # bit-identical reruns
+    toks2 = toks.copy()
+    toks2[100:] = (toks2[100:] + 17) % cfg.n_vocab
+    c = m.forward(torch.as_tensor(toks2.astype(np.int32), device=dev)).cpu().numpy()
+    assert np.array_equal(a[:100], c[:100])          # rows < 100 never see later tokens
+    assert not np.array_equal(a[100:], c[100:])
+
+
+def test_token_out_of_range_is_reported(dtp):
+    cfg = synth.CONFIGS["tiny"]
+    m = load_model(dtp, cfg)
+    toks = torch.as_tensor(np.array([1, 2, 999, 3], np.int32), device=dev)
+    m.forward(toks)
+    with pytest.raises(dtp.DtpError) as e:
+        dtp.check()
+    assert e.value.code == -3
+    dtp.check()                                      # the error word was cleared

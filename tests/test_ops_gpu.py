@@ -1,0 +1,180 @@
+"""Per-op parity: each C-ABI entry point against the oracle on seeded inputs.
+
+Tolerances: float32 kernels vs the float64 oracle at 2e-6 relative (a few
+float32 roundings); bf16-output kernels at 1 bf16 ulp (2^-8 relative) on top of
+that; the bf16 tensor-core GEMM gets exactly bf16 operands, so only the float32
+accumulation differs (K * 2^-24 relative bound, 1e-5 used)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+dev = torch.device("cuda")
+
+
+def t32(a):
+    return torch.as_tensor(np.ascontiguousarray(a, np.float32), device=dev)
+
+
+def bf16_round32(a):
+    """float32 array rounded to bf16 values (as float32), via torch on the host."""
+    return torch.as_tensor(np.asarray(a, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def max_rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+
+
+# ----------------------------------------------------------------------------- RMSNorm
+@pytest.mark.parametrize("rows,cols", [(1, 64), (7, 4096), (300, 1000), (5, 13)])
+@pytest.mark.parametrize("ydt", [torch.float32, torch.bfloat16])
+def test_rms_norm(dtp, rows, cols, ydt):
+    x = synth.normal(1, 100, (rows, cols)) * 3
+    w = synth.normal(1, 101, (cols,), mean=1.0, std=0.1)
+    y = torch.empty((rows, cols), dtype=ydt, device=dev)
+    dtp.rms_norm(t32(x), t32(w), y, 1e-6)
+    ref = oracle.rms_norm(x, w, 1e-6)
+    tol = 2e-6 if ydt == torch.float32 else 2 ** -8
+    np.testing.assert_allclose(y.float().cpu().numpy(), ref, rtol=tol, atol=tol * 1e-3)
+
+
+# ----------------------------------------------------------------------------- QK-norm + RoPE
+@pytest.mark.parametrize("T,nh,hd,r", [(1, 2, 16, 16), (37, 4, 64, 64), (300, 3, 128, 64), (129, 8, 128, 128)])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_qk_norm_rope(dtp, T, nh, hd, r, dt):
+    x = synth.normal(2, 200, (T, nh * hd))
+    w = synth.normal(2, 201, (hd,), mean=1.0, std=0.1)
+    xin = x if dt == torch.float32 else bf16_round32(x)
+    xt = t32(xin).to(dt)
+    dtp.qk_norm_rope_neox(xt, t32(w), None, nh, hd, r, 1e6, 1e-6)
+    ref = oracle.rope_neox(oracle.qk_norm(xin, w, hd, 1e-6), np.arange(T), nh, hd, r, 1e6)
+    tol = 3e-6 if dt == torch.float32 else 2 ** -8
+    np.testing.assert_allclose(xt.float().cpu().numpy(), ref, rtol=tol, atol=tol * 4)
+
+
+def test_rope_only_with_positions(dtp):
+    T, nh, hd = 50, 2, 32
+    x = synth.normal(3, 300, (T, nh * hd))
+    pos = (np.arange(T) * 37 + 5).astype(np.int32)
+    xt = t32(x)
+    dtp.qk_norm_rope_neox(xt, None, torch.as_tensor(pos, device=dev), nh, hd, hd, 1e4, 1e-6)
+    ref = oracle.rope_neox(x, pos, nh, hd, hd, 1e4)
+    np.testing.assert_allclose(xt.cpu().numpy(), ref, rtol=1e-5, atol=1e-5)
+
+
+def test_rope_position_and_pair_indexing_bit_exact(dtp):
+    """Recover, from the kernel's output alone, which position rotated each row
+    and which dims were paired: both must equal the definition exactly."""
+    T, nh, hd, r = 4096, 2, 16, 8
+    base = 1e8     # theta_i = 1e8^(-2i/8): theta_3 = 1e-6, so T*theta_3 < pi (no wrap)
+    half = r // 2
+    x = np.zeros((T, nh, hd), np.float32)
+    x[:, 0, 3] = 1.0          # one-hot at dim 3 (< half): pairs with dim 3 + half = 7
+    x[:, 1, 9] = 1.0          # dim 9 >= r: passes through
+    xt = t32(x.reshape(T, nh * hd))
+    dtp.qk_norm_rope_neox(xt, None, None, nh, hd, r, base, 0.0)
+    y = xt.cpu().numpy().reshape(T, nh, hd).astype(np.float64)
+    nz0 = sorted(set(np.nonzero(np.abs(y[1:, 0]) > 0)[1].tolist()))
+    assert nz0 == [3, 7]
+    assert np.array_equal(y[:, 1], x[:, 1])
+    theta = base ** (-2.0 * 3 / r)
+    recovered = np.rint(np.arctan2(y[:, 0, 7], y[:, 0, 3]) / theta).astype(np.int64)
+    assert np.array_equal(recovered, np.arange(T))
+
+
+# ----------------------------------------------------------------------------- SwiGLU
+@pytest.mark.parametrize("n", [1, 1000, 123457])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_swiglu(dtp, n, dt):
+    g = synth.normal(4, 400, (n,)) * 4
+    u = synth.normal(4, 401, (n,))
+    if dt == torch.bfloat16:
+        g, u = bf16_round32(g), bf16_round32(u)
+    out = torch.empty(n, dtype=dt, device=dev)
+    dtp.swiglu(t32(g).to(dt), t32(u).to(dt), out)
+    ref = oracle.swiglu(g, u)
+    tol = 2e-6 if dt == torch.float32 else 2 ** -8
+    np.testing.assert_allclose(out.float().cpu().numpy(), ref, rtol=tol, atol=tol * 1e-3)
+
+
+# ----------------------------------------------------------------------------- linear
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (130, 200, 72), (256, 512, 512), (77, 1000, 136)])
+@pytest.mark.parametrize("resid", [False, True])
+def test_linear_f32(dtp, M, N, K, resid):
+    x = synth.normal(5, 500, (M, K))
+    W = synth.normal(5, 501, (N, K), std=0.05)
+    r = synth.normal(5, 502, (M, N)) if resid else None
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    dtp.linear(t32(x), t32(W), y, residual=None if r is None else t32(r))
+    ref = oracle.linear(x, W) + (r if resid else 0)
+    np.testing.assert_allclose(y.cpu().numpy(), ref, rtol=0, atol=2e-6 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (128, 256, 64), (130, 200, 72), (256, 768, 512),
+                                   (300, 1000, 136), (513, 2048, 1024), (64, 384, 4096)])
+@pytest.mark.parametrize("mode", ["f32", "bf16", "resid"])
+def test_linear_bf16_tensor_core(dtp, M, N, K, mode):
+    x = bf16_round32(synth.normal(6, 600, (M, K)))
+    W = bf16_round32(synth.normal(6, 601, (N, K), std=0.05))
+    xt, Wt = t32(x).bfloat16(), t32(W).bfloat16()
+    ref = oracle.linear(x, W)
+    if mode == "bf16":
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        dtp.linear(xt, Wt, y)
+        np.testing.assert_allclose(y.float().cpu().numpy(), ref, rtol=2 ** -8,
+                                   atol=1e-5 * np.abs(ref).max())
+        return
+    r = synth.normal(6, 602, (M, N)) if mode == "resid" else None
+    y = t32(r) if r is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
+    dtp.linear(xt, Wt, y, residual=y if r is not None else None)     # in-place residual add
+    if r is not None:
+        ref = ref + r
+    torch.cuda.synchronize()
+    dtp.check()
+    np.testing.assert_allclose(y.cpu().numpy(), ref, rtol=0, atol=1e-5 * np.abs(ref).max())
+
+
+def test_linear_bf16_long_k_and_many_tiles(dtp):
+    # several persistent waves of 128x256 tiles and a 12288-long reduction
+    M, N, K = 1024, 4096, 12288
+    x = bf16_round32(synth.normal(7, 700, (M, K)))
+    W = bf16_round32(synth.normal(7, 701, (N, K), std=0.02))
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    dtp.linear(t32(x).bfloat16(), t32(W).bfloat16(), y)
+    rows = np.array([0, 1, 127, 128, 500, 1023])
+    ref = oracle.linear(x[rows], W)
+    np.testing.assert_allclose(y.cpu().numpy()[rows], ref, rtol=0, atol=1e-5 * np.abs(ref).max())
+
+
+# ----------------------------------------------------------------------------- attention
+@pytest.mark.parametrize("T,nh,nkv,hd", [(1, 4, 2, 16), (17, 4, 2, 64), (130, 8, 4, 64), (300, 4, 1, 128)])
+def test_sdpa_f32(dtp, T, nh, nkv, hd):
+    q = synth.normal(8, 800, (T, nh * hd))
+    k = synth.normal(8, 801, (T, nkv * hd))
+    v = synth.normal(8, 802, (T, nkv * hd))
+    out = torch.empty((T, nh * hd), dtype=torch.float32, device=dev)
+    sc = 1 / math.sqrt(hd)
+    dtp.sdpa_causal_gqa(t32(q), t32(k), t32(v), out, nh, nkv, hd, sc)
+    ref = oracle.sdpa_causal_gqa(q, k, v, nh, nkv, hd, sc)
+    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=0, atol=2e-6 * np.abs(ref).max())
+
+
+def test_sdpa_gqa_head_map_bit_exact(dtp):
+    """v of kv head j is the constant j, so each output head must read back
+    exactly the kv head the definition assigns: j = i // (n_head / n_head_kv)."""
+    T, nh, nkv, hd = 64, 8, 2, 16
+    q = synth.normal(9, 900, (T, nh * hd))
+    k = synth.normal(9, 901, (T, nkv * hd))
+    v = np.repeat(np.arange(nkv, dtype=np.float32), hd)[None, :].repeat(T, 0)
+    out = torch.empty((T, nh * hd), dtype=torch.float32, device=dev)
+    dtp.sdpa_causal_gqa(t32(q), t32(k), t32(v), out, nh, nkv, hd, 0.25)
+    got = np.rint(out.cpu().numpy().reshape(T, nh, hd)).astype(int)
+    want = (np.arange(nh) // (nh // nkv))[None, :, None].repeat(T, 0).repeat(hd, 2)
+    assert np.array_equal(got, want)
