@@ -149,6 +149,8 @@ def main():
     ap.add_argument("--workload", default="qwen3-8b-shape", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--n-layer", type=int, default=None,
+                    help="override the layer count (profiling captures of a small case)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -157,6 +159,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = synth.CONFIGS[args.workload]
+    if args.n_layer is not None:
+        cfg = cfg.replace(n_layer=args.n_layer)
     config = {"workload": cfg.name, "T": cfg.T, "n_layer": cfg.n_layer, "n_embd": cfg.n_embd,
               "n_head": cfg.n_head, "n_head_kv": cfg.n_head_kv, "head_dim": cfg.head_dim,
               "n_ff": cfg.n_ff, "n_vocab": cfg.n_vocab, "sequences_per_gpu": 1,

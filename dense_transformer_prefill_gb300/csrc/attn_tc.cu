@@ -1,5 +1,27 @@
-// tcgen05 flash attention (causal GQA).  Kernel lands in the next step; the
-// dispatcher reports it unsupported until then.
+// tcgen05 causal grouped-query flash attention (forward.rs, Model::forward:
+// `e.sdpa_naive(q, k, v, attn, head_dim, n_head, n_head_kv, t, t, scale, true)`,
+// restated as an online-softmax tiled kernel; the pages' naive kernel is prior
+// art only).
+//
+// One CTA = one 128-token query tile of TWO query heads of the same GQA group,
+// so every K/V tile brought into shared memory serves 256 query rows.
+//   warp 0      TMA: Q tiles of both heads once, then per 128-key tile K_j
+//               (one stage) and V_j^T (two stages; v is stored transposed,
+//               key index contiguous, so both MMAs read K-major operands)
+//   warp 1      one thread issues S_i = Q_i K_j^T (M=128, N=128 keys) into TMEM
+//               and O_i += P_i V_j (M=128, N=head_dim) into TMEM, ordered
+//               S0 S1 | PV0 S0' | PV1 S1' | ... so each head's softmax
+//               overlaps the other head's MMAs
+//   warps 2-5   softmax of head 0; warps 6-9 softmax of head 1: TMEM lane =
+//               query row; scores scaled into log2 units, running max kept
+//               unless it grows by more than 8 (then O is rescaled in TMEM),
+//               P = 2^(s - m) rounded to bf16 into 128-byte-swizzled shared
+//               memory, row sums in float32
+// Causality: key tiles 0..qt only; the diagonal tile masks key > query.
+// Query tiles are scheduled longest first.
+#include <math.h>
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -14,11 +36,391 @@ unsigned read_clear_attn_errors() {
     return v;
 }
 
-bool attn_tc_supported(int, int, int) { return false; }
+bool attn_tc_supported(int n_head, int n_head_kv, int head_dim) {
+    return (head_dim == 64 || head_dim == 128) && n_head_kv > 0 && n_head % n_head_kv == 0 &&
+           (n_head / n_head_kv) % 2 == 0;
+}
 
-cudaError_t launch_attn_tc(const __nv_bfloat16*, const __nv_bfloat16*, const __nv_bfloat16*,
-                           long long, __nv_bfloat16*, int, int, int, int, float, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int BQ = 128;          // query rows per tile
+constexpr int BKV = 128;         // keys per tile
+constexpr int kThreads = 320;    // 10 warps
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int HD>
+struct ACfg {
+    static constexpr int Q_BYTES = BQ * HD * 2;
+    static constexpr int K_BYTES = BKV * HD * 2;
+    static constexpr int V_BYTES = HD * BKV * 2;
+    static constexpr int P_BYTES = BQ * BKV * 2;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + K_BYTES;
+    static constexpr int OFF_P = OFF_V + 2 * V_BYTES;
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr uint32_t S_COL0 = 0, O_COL0 = 2 * BKV;
+};
+
+struct AParams {
+    int T, n_head, n_head_kv, n_qt;
+    float scale_log2;
+    __nv_bfloat16* out;
+    int ldo;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AParams p) {
+    using C = ACfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem + C::OFF_Q;
+    uint8_t* sK = smem + C::OFF_K;
+    uint8_t* sV = smem + C::OFF_V;
+    uint8_t* sP = smem + C::OFF_P;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* q_full = bars + 0;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = bars + 2;
+    uint64_t* v_full = bars + 3;      // [2]
+    uint64_t* v_empty = bars + 5;     // [2]
+    uint64_t* s_full = bars + 7;      // [2]
+    uint64_t* p_full = bars + 9;      // [2]
+    uint64_t* o_done = bars + 11;     // [2]
+    uint64_t* drain = bars + 13;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 14);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.n_head / p.n_head_kv, pairs = G / 2;
+    const int items_per_qt = p.n_head_kv * pairs;
+    const int qt = p.n_qt - 1 - (int)blockIdx.x / items_per_qt;
+    const int rem = (int)blockIdx.x % items_per_qt;
+    const int g = rem / pairs;
+    const int h0 = g * G + 2 * (rem % pairs);
+    const int n_kv = qt + 1;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(q_full, 1);
+        ptx::mbar_init(k_full, 1);
+        ptx::mbar_init(k_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&v_full[i], 1);
+            ptx::mbar_init(&v_empty[i], 1);
+            ptx::mbar_init(&s_full[i], 1);
+            ptx::mbar_init(&p_full[i], 128);
+            ptx::mbar_init(&o_done[i], 1);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            ptx::tma_prefetch_desc(&tmQ);
+            ptx::tma_prefetch_desc(&tmK);
+            ptx::tma_prefetch_desc(&tmV);
+            ptx::mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
+            for (int i = 0; i < 2; ++i)
+                for (int a = 0; a < HD / 64; ++a)
+                    ptx::tma_load_2d(&tmQ, q_full, sQ + i * C::Q_BYTES + a * BQ * 128,
+                                     (h0 + i) * HD + a * 64, qt * BQ);
+            int k_issued = 0, v_issued[2] = {0, 0};
+            for (int j = 0; j < n_kv; ++j) {
+                if (!ptx::wait_bounded(k_empty, (j & 1) ^ 1, abort_flag, &g_attn_err, ERRBIT_TIMEOUT))
+                    break;
+                ptx::mbar_arrive_expect_tx(k_full, C::K_BYTES);
+                for (int a = 0; a < HD / 64; ++a)
+                    ptx::tma_load_2d(&tmK, k_full, sK + a * BKV * 128, g * HD + a * 64, j * BKV);
+                ++k_issued;
+                const int vs = j & 1;
+                if (!ptx::wait_bounded(&v_empty[vs], ((j >> 1) & 1) ^ 1, abort_flag, &g_attn_err,
+                                       ERRBIT_TIMEOUT))
+                    break;
+                ptx::mbar_arrive_expect_tx(&v_full[vs], C::V_BYTES);
+                for (int a = 0; a < BKV / 64; ++a)
+                    ptx::tma_load_2d(&tmV, &v_full[vs], sV + vs * C::V_BYTES + a * HD * 128,
+                                     j * BKV + a * 64, g * HD);
+                ++v_issued[vs];
+            }
+            if (*abort_flag) {
+                // let the loads still in flight land before the CTA can exit: the
+                // latest phase of each barrier completes when its bytes arrive
+                volatile int never = 0;
+                ptx::wait_bounded(q_full, 0, &never, &g_attn_err, ERRBIT_TIMEOUT);
+                if (k_issued)
+                    ptx::wait_bounded(k_full, (k_issued - 1) & 1, &never, &g_attn_err,
+                                      ERRBIT_TIMEOUT);
+                for (int vs = 0; vs < 2; ++vs)
+                    if (v_issued[vs])
+                        ptx::wait_bounded(&v_full[vs], (v_issued[vs] - 1) & 1, &never, &g_attn_err,
+                                          ERRBIT_TIMEOUT);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            const uint32_t idS = ptx::idesc_bf16_f32(BQ, BKV);
+            const uint32_t idO = ptx::idesc_bf16_f32(BQ, HD);
+            auto issue_S = [&](int i) {
+                const uint32_t d = tmem_base + C::S_COL0 + i * BKV;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const int a = kk / 4, off = (kk % 4) * 32;
+                    const uint64_t da =
+                        ptx::sdesc_sw128(ptx::smem_u32(sQ + i * C::Q_BYTES + a * BQ * 128 + off));
+                    const uint64_t db = ptx::sdesc_sw128(ptx::smem_u32(sK + a * BKV * 128 + off));
+                    ptx::umma_bf16_ss(d, da, db, idS, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_PV = [&](int i, int vs, int j) {
+                const uint32_t d = tmem_base + C::O_COL0 + i * HD;
+#pragma unroll
+                for (int kk = 0; kk < BKV / 16; ++kk) {
+                    const int a = kk / 4, off = (kk % 4) * 32;
+                    const uint64_t da =
+                        ptx::sdesc_sw128(ptx::smem_u32(sP + i * C::P_BYTES + a * BQ * 128 + off));
+                    const uint64_t db = ptx::sdesc_sw128(
+                        ptx::smem_u32(sV + vs * C::V_BYTES + a * HD * 128 + off));
+                    ptx::umma_bf16_ss(d, da, db, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            auto W = [&](uint64_t* b, uint32_t par) {
+                return ptx::wait_bounded(b, par, abort_flag, &g_attn_err, ERRBIT_TIMEOUT);
+            };
+            bool ok = W(q_full, 0) && W(k_full, 0);
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_S(0);
+                ptx::umma_commit(&s_full[0]);
+                issue_S(1);
+                ptx::umma_commit(&s_full[1]);
+                ptx::umma_commit(k_empty);
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int vs = j & 1;
+                if (!(W(&v_full[vs], (j >> 1) & 1) && W(&p_full[0], j & 1))) break;
+                ptx::tc_fence_after();
+                issue_PV(0, vs, j);
+                ptx::umma_commit(&o_done[0]);
+                const bool more = j + 1 < n_kv;
+                if (more) {
+                    if (!W(k_full, (j + 1) & 1)) break;
+                    ptx::tc_fence_after();
+                    issue_S(0);
+                    ptx::umma_commit(&s_full[0]);
+                }
+                if (!W(&p_full[1], j & 1)) break;
+                ptx::tc_fence_after();
+                issue_PV(1, vs, j);
+                ptx::umma_commit(&o_done[1]);
+                ptx::umma_commit(&v_empty[vs]);
+                if (more) {
+                    issue_S(1);
+                    ptx::umma_commit(&s_full[1]);
+                    ptx::umma_commit(k_empty);
+                }
+            }
+            ptx::umma_commit(drain);
+            volatile int never = 0;
+            ptx::wait_bounded(drain, 0, &never, &g_attn_err, ERRBIT_TIMEOUT);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax warps
+        const int i = (warp - 2) / 4;            // which head of the pair
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int qrow = qt * BQ + row;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem_base + lane_off + C::S_COL0 + i * BKV;
+        const uint32_t tO = tmem_base + lane_off + C::O_COL0 + i * HD;
+        uint8_t* Prow = sP + i * C::P_BYTES + row * 128;
+        const int sw = row & 7;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            ok = ptx::wait_bounded(&s_full[i], j & 1, abort_flag, &g_attn_err, ERRBIT_TIMEOUT);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            float s[BKV];
+#pragma unroll
+            for (int c = 0; c < BKV / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld32(tS + c * 32, r);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(r[t]);
+            }
+            if (j == qt) {
+#pragma unroll
+                for (int c = 0; c < BKV; ++c)
+                    if (c > row) s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < BKV; ++c) mx = fmaxf(mx, s[c]);
+            const float m_tile = mx * p.scale_log2;
+            // O and P_i are still in use by PV_i(j-1) until o_done
+            if (j > 0) {
+                ok = ptx::wait_bounded(&o_done[i], (j - 1) & 1, abort_flag, &g_attn_err,
+                                       ERRBIT_TIMEOUT);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+            }
+            // keep the running max unless this tile raises it by more than 2^8;
+            // then rescale l and (warp-wide, lanes without a raise use 1) O in TMEM
+            const bool need = m_tile > m + kRescaleLog2;
+            float alpha = 1.f;
+            if (need) {
+                alpha = ex2(m - m_tile);       // 0 on the first tile (m = -inf)
+                m = m_tile;
+                l *= alpha;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                for (int c = 0; c < HD; c += 32) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    ptx::tmem_ld32(tO + c, r);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+                    ptx::tmem_st32(tO + c, r);
+                }
+            }
+            // P = 2^(s*scale_log2 - m), row sum, bf16 into swizzled shared memory
+            float rs = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < BKV / 8; ++c8) {
+                float e[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    e[t] = ex2(fmaf(s[c8 * 8 + t], p.scale_log2, -m));
+                    rs += e[t];
+                }
+                uint4 u;
+                u.x = ptx::pack_bf16x2(e[0], e[1]);
+                u.y = ptx::pack_bf16x2(e[2], e[3]);
+                u.z = ptx::pack_bf16x2(e[4], e[5]);
+                u.w = ptx::pack_bf16x2(e[6], e[7]);
+                const int atom = c8 >> 3, chunk = c8 & 7;
+                *reinterpret_cast<uint4*>(Prow + atom * BQ * 128 + ((chunk ^ sw) << 4)) = u;
+            }
+            l += rs;
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&p_full[i]);
+        }
+        if (ok) {
+            ok = ptx::wait_bounded(&o_done[i], (n_kv - 1) & 1, abort_flag, &g_attn_err,
+                                   ERRBIT_TIMEOUT);
+            if (__all_sync(0xffffffffu, ok)) {
+                ptx::tc_fence_after();
+                const float inv = 1.0f / l;
+                __nv_bfloat16* orow = p.out + (size_t)qrow * p.ldo + (size_t)(h0 + i) * HD;
+#pragma unroll 1
+                for (int c = 0; c < HD; c += 32) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    ptx::tmem_ld32(tO + c, r);
+                    if (qrow < p.T) {
+#pragma unroll
+                        for (int t = 0; t < 32; t += 8) {
+                            uint4 u;
+                            u.x = ptx::pack_bf16x2(__uint_as_float(r[t + 0]) * inv,
+                                                   __uint_as_float(r[t + 1]) * inv);
+                            u.y = ptx::pack_bf16x2(__uint_as_float(r[t + 2]) * inv,
+                                                   __uint_as_float(r[t + 3]) * inv);
+                            u.z = ptx::pack_bf16x2(__uint_as_float(r[t + 4]) * inv,
+                                                   __uint_as_float(r[t + 5]) * inv);
+                            u.w = ptx::pack_bf16x2(__uint_as_float(r[t + 6]) * inv,
+                                                   __uint_as_float(r[t + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + c + t) = u;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int HD>
+cudaError_t launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const AParams& p, cudaStream_t s) {
+    using C = ACfg<HD>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<HD>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int G = p.n_head / p.n_head_kv;
+    const int grid = p.n_qt * p.n_head_kv * (G / 2);
+    attn_tc_kernel<HD><<<grid, kThreads, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                           const __nv_bfloat16* vt, long long ldvt, __nv_bfloat16* out, int T,
+                           int n_head, int n_head_kv, int head_dim, float scale, cudaStream_t s) {
+    if (!attn_tc_supported(n_head, n_head_kv, head_dim)) return cudaErrorNotSupported;
+    CUtensorMap tq, tk, tv;
+    const int hd = head_dim;
+    if (!make_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, (uint64_t)n_head * hd,
+                      (uint64_t)n_head * hd, BQ, 64) ||
+        !make_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, (uint64_t)n_head_kv * hd,
+                      (uint64_t)n_head_kv * hd, BKV, 64) ||
+        !make_tmap_2d(&tv, vt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)n_head_kv * hd, T,
+                      (uint64_t)ldvt, hd, 64))
+        return cudaErrorInvalidValue;
+    AParams p;
+    p.T = T;
+    p.n_head = n_head;
+    p.n_head_kv = n_head_kv;
+    p.n_qt = (T + BQ - 1) / BQ;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = out;
+    p.ldo = n_head * hd;
+    LaunchScope ls(DTP_K_ATTN, s);
+    if (hd == 128) return launch_hd<128>(tq, tk, tv, p, s);
+    return launch_hd<64>(tq, tk, tv, p, s);
 }
 
 }  // namespace dtp

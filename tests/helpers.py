@@ -18,6 +18,21 @@ def argmax_agreement(gpu_logits, ref_logits) -> float:
     return float(np.mean(np.argmax(np.asarray(gpu_logits), 1) == np.argmax(np.asarray(ref_logits), 1)))
 
 
+def argmax_agreement_near_tie(gpu_logits, ref_logits, margin_bound: float):
+    """(agreement, structured_flips): a position agrees if the argmaxes match, or if
+    they differ and the reference's top1-top2 margin is <= margin_bound (a near-tie
+    flip in the sense of the forward.rs prime-gate verdict); a flip at a wider
+    margin is counted as structured."""
+    g = np.asarray(gpu_logits, np.float64)
+    r = np.asarray(ref_logits, np.float64)
+    ga, ra = np.argmax(g, 1), np.argmax(r, 1)
+    top2 = np.sort(r, axis=1)[:, -2:]
+    margin = top2[:, 1] - top2[:, 0]
+    flip = ga != ra
+    near = flip & (margin <= margin_bound)
+    return float(np.mean(~flip | near)), int(np.sum(flip & ~near))
+
+
 def load_model(dtp, cfg, seed=0):
     """GPU Model with every tensor from the seeded generator."""
     m = dtp.Model(cfg)

@@ -150,7 +150,10 @@ def test_linear_bf16_long_k_and_many_tiles(dtp):
     dtp.linear(t32(x).bfloat16(), t32(W).bfloat16(), y)
     rows = np.array([0, 1, 127, 128, 500, 1023])
     ref = oracle.linear(x[rows], W)
-    np.testing.assert_allclose(y.cpu().numpy()[rows], ref, rtol=0, atol=1e-5 * np.abs(ref).max())
+    # tensor-core accumulation adds each K=16 partial product into float32 with up
+    # to ~1 ulp of error per step: bound (K/16) * 2^-23 * max|y|, with a 2x margin
+    tol = 2 * (K / 16) * 2.0 ** -23 * np.abs(ref).max()
+    np.testing.assert_allclose(y.cpu().numpy()[rows], ref, rtol=0, atol=tol)
 
 
 # ----------------------------------------------------------------------------- attention
@@ -178,3 +181,84 @@ def test_sdpa_gqa_head_map_bit_exact(dtp):
     got = np.rint(out.cpu().numpy().reshape(T, nh, hd)).astype(int)
     want = (np.arange(nh) // (nh // nkv))[None, :, None].repeat(T, 0).repeat(hd, 2)
     assert np.array_equal(got, want)
+
+
+# ----------------------------------------------------------------------------- tcgen05 attention
+def _sdpa_bf16(dtp, q, k, v, nh, nkv, hd):
+    T = q.shape[0]
+    out = torch.empty((T, nh * hd), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(dtp.sdpa_workspace_size(T, nkv, hd, dtp.DTP_BF16), dtype=torch.uint8, device=dev)
+    dtp.sdpa_causal_gqa(t32(q).bfloat16(), t32(k).bfloat16(), t32(v).bfloat16(), out, nh, nkv, hd,
+                        1 / math.sqrt(hd), ws)
+    torch.cuda.synchronize()
+    dtp.check()
+    return out.float().cpu().numpy()
+
+
+def _attn_close(got, ref, vmax):
+    # P is rounded to bf16 for the PV product (2^-9 relative) and so is the output
+    err = np.abs(got - ref)
+    assert err.max() <= 8e-3 * vmax, err.max()
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 3e-3
+
+
+@pytest.mark.parametrize("T,nh,nkv,hd", [(1, 4, 2, 128), (100, 4, 2, 64), (128, 8, 4, 128),
+                                         (129, 4, 1, 64), (300, 8, 2, 128), (1024, 16, 8, 128)])
+def test_sdpa_bf16_tensor_core(dtp, T, nh, nkv, hd):
+    q = bf16_round32(synth.normal(10, 1000, (T, nh * hd)))
+    k = bf16_round32(synth.normal(10, 1001, (T, nkv * hd)))
+    v = bf16_round32(synth.normal(10, 1002, (T, nkv * hd)))
+    got = _sdpa_bf16(dtp, q, k, v, nh, nkv, hd)
+    ref = oracle.sdpa_causal_gqa(q, k, v, nh, nkv, hd, 1 / math.sqrt(hd))
+    _attn_close(got, ref, np.abs(v).max())
+
+
+def test_sdpa_bf16_large_scores_rescale(dtp):
+    # scores spread over hundreds of log2 units across key tiles: exercises the
+    # running-max rescale of O in TMEM
+    T, nh, nkv, hd = 640, 2, 1, 64
+    q = bf16_round32(synth.normal(11, 1100, (T, nh * hd)) * 6)
+    k = bf16_round32(synth.normal(11, 1101, (T, nkv * hd)) * 6 * np.linspace(0.2, 2.0, T)[:, None])
+    v = bf16_round32(synth.normal(11, 1102, (T, nkv * hd)))
+    got = _sdpa_bf16(dtp, q, k, v, nh, nkv, hd)
+    ref = oracle.sdpa_causal_gqa(q, k, v, nh, nkv, hd, 1 / math.sqrt(hd))
+    _attn_close(got, ref, np.abs(v).max())
+
+
+def test_sdpa_bf16_gqa_head_map_bit_exact(dtp):
+    T, nh, nkv, hd = 200, 8, 2, 64
+    q = bf16_round32(synth.normal(12, 1200, (T, nh * hd)))
+    k = bf16_round32(synth.normal(12, 1201, (T, nkv * hd)))
+    v = np.repeat(np.array([3.0, 7.0], np.float32), hd)[None, :].repeat(T, 0)
+    got = np.rint(_sdpa_bf16(dtp, q, k, v, nh, nkv, hd).reshape(T, nh, hd)).astype(int)
+    want = np.array([3, 3, 3, 3, 7, 7, 7, 7])[None, :, None].repeat(T, 0).repeat(hd, 2)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("T", [1024, 4096, 8192, 16384])
+@pytest.mark.parametrize("r", [64, 128])
+def test_attention_sweep(dtp, T, r):
+    """Causal GQA SDPA with QK-norm + NeoX RoPE, h=32, g=8, hd=128, q/k/v ~ N(0,1)
+    in bf16; checked on sampled query rows (each computed by the oracle from
+    all keys up to it) including the first and last tiles."""
+    sw = synth.ATTN_SWEEP
+    nh, nkv, hd = sw["n_head"], sw["n_head_kv"], sw["head_dim"]
+    inp = synth.attention_inputs(T, nh, nkv, hd)
+    q, k, v = (bf16_round32(inp[n]) for n in ("q", "k", "v"))
+    qt, kt, vt = t32(q).bfloat16(), t32(k).bfloat16(), t32(v).bfloat16()
+    base, eps = sw["rope_freq_base"], sw["rms_eps"]
+    dtp.qk_norm_rope_neox(qt, t32(inp["q_norm"]), None, nh, hd, r, base, eps)
+    dtp.qk_norm_rope_neox(kt, t32(inp["k_norm"]), None, nkv, hd, r, base, eps)
+    out = torch.empty((T, nh * hd), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(dtp.sdpa_workspace_size(T, nkv, hd, dtp.DTP_BF16), dtype=torch.uint8, device=dev)
+    dtp.sdpa_causal_gqa(qt, kt, vt, out, nh, nkv, hd, 1 / math.sqrt(hd), ws)
+    torch.cuda.synchronize()
+    dtp.check()
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, T // 2, T - 129, T - 2, T - 1],
+                                     np.random.default_rng(T + r).integers(0, T, 8)]))
+    pos = np.arange(T)
+    qr = oracle.round_bf16(oracle.rope_neox(oracle.qk_norm(q, inp["q_norm"], hd, eps), pos, nh, hd, r, base))
+    kr = oracle.round_bf16(oracle.rope_neox(oracle.qk_norm(k, inp["k_norm"], hd, eps), pos, nkv, hd, r, base))
+    ref = oracle.sdpa_causal_gqa(qr, kr, v, nh, nkv, hd, 1 / math.sqrt(hd), rows=rows)
+    got = out.float().cpu().numpy()[rows]
+    _attn_close(got, ref, np.abs(v).max())
