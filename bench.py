@@ -45,6 +45,41 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
+def profiled_traffic(profile: str, sources) -> float | None:
+    """DRAM bytes per launch recorded by an ncu capture under profiles/, or None if
+    the kernel sources changed since (their hash no longer matches) or there is none."""
+    import hashlib
+    import re
+
+    path = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(path):
+        return None
+    m = re.search(r"traffic_bytes_per_launch=(\d+) source_sha256_16=([0-9a-f]+)", open(path).read())
+    if not m:
+        return None
+    h = hashlib.sha256()
+    for f in sources:
+        h.update(open(os.path.join(ROOT, "dense_transformer_prefill_gb300", "csrc", f), "rb").read())
+    return float(m.group(1)) if h.hexdigest()[:16] == m.group(2) else None
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """Maximum of a per-rank float over the process group (identity when world == 1)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, tokens_per_rank_step: int, steps: int, max_ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / (max_ms / 1000.0)
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -246,13 +281,9 @@ def main():
     ms = start.elapsed_time(end)
     kstats = {k: dtp.timer_read(k) for k in kinds}
     dtp.timer_disable()
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_per_step = ms / args.steps
-    value = world * cfg.T * args.steps / (ms / 1000.0)
+    value = replica_throughput(world, cfg.T, args.steps, ms)
 
     # ------------------------------------------------------------------ end to end (host buffers)
     e2e = None
@@ -271,13 +302,8 @@ def main():
         e_end.record(stream)
         torch.cuda.synchronize(dev)
         dtp.check()
-        ems = e_start.elapsed_time(e_end)
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * cfg.T * args.steps / (ems / 1000.0), "unit": UNIT,
+        ems = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
+        e2e = {"value": replica_throughput(world, cfg.T, args.steps, ems), "unit": UNIT,
                "h2d_bytes_per_step": int(tok_h.numel() * 4),
                "d2h_bytes_per_step": int(log_h.numel() * 4),
                "path": "dtp_fwd_prefill_host (pinned host tokens in, pinned host logits out)"}
@@ -296,13 +322,26 @@ def main():
     gu_flops = 2.0 * T * (2 * F) * d
     achieved = gu_flops / (gu_ms / gu_n / 1000.0) / 1e12 if gu_n else None
     peak = peaks["bf16_tflops_sustained"] if cfg.precision == "bf16" else None
+    is8b = cfg.name == "qwen3-8b-shape" and cfg.T == 4096
     roofline = {"kernel": "gemm_tc_kernel<256, EPI_SWIGLU> (gate/up projection + SwiGLU)",
                 "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if (achieved and peak) else None,
-                "traffic": None,
+                "traffic": profiled_traffic("gemm_tc_gateup_qwen3-8b-shape.md",
+                                            ["gemm_tc.cu", "ptx.cuh", "internal.h"]) if is8b else None,
+                "algorithmic_bytes_per_launch": 2.0 * (T * d + 2 * F * d + T * F),
                 "flops_per_launch": gu_flops,
                 "peak_source": f"bf16_tflops_sustained of {peaks['source']} peaks",
                 "avg_launch_ms": gu_ms / gu_n if gu_n else None}
+    at_n, at_ms = kstats["attn"]
+    at_flops = cfg.attn_flops() / cfg.n_layer
+    at_ach = at_flops / (at_ms / at_n / 1000.0) / 1e12 if at_n else None
+    roofline_attn = {"kernel": "attn_tc_kernel<%d> (causal GQA flash attention, one layer)"
+                     % cfg.head_dim, "bound": "tensor", "achieved": at_ach, "peak": peak,
+                     "unit": "TFLOP/s", "frac": (at_ach / peak) if (at_ach and peak) else None,
+                     "traffic": profiled_traffic("attn_tc_qwen3-8b-shape.md",
+                                                 ["attn_tc.cu", "ptx.cuh", "internal.h"]) if is8b else None,
+                     "flops_per_launch": at_flops,
+                     "avg_launch_ms": at_ms / at_n if at_n else None}
     per_kernel = {}
     step_flops = 0.0
     for k, (n, kms) in kstats.items():
@@ -320,7 +359,7 @@ def main():
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if cfg.precision == "bf16" else "f32",
         "data": "synthetic (seeded random-init weights of the architecture, uniform token ids)",
-        "config": config, "roofline": roofline,
+        "config": config, "roofline": roofline, "roofline_attn": roofline_attn,
         "tflops": {"step": step_flops / (ms_per_step / 1000.0) / 1e12,
                    "gemm": gemm_flops / (gemm_ms / 1000.0) / 1e12 if gemm_ms else None,
                    "attn": attn_flops / (attn_ms / 1000.0) / 1e12 if attn_ms else None,
