@@ -174,6 +174,37 @@ class OracleSample:
                            f"{cfg.n_layer} layers x {T} tokens and the full {cfg.n_vocab} vocab")}
 
 
+def attention_sweep(dtp, dev, peak, Ts=(1024, 4096, 8192, 16384), reps=5) -> dict:
+    """Causal GQA flash attention alone at the sweep shape (h=32, g=8, hd=128,
+    q/k/v ~ N(0,1) bf16): mean kernel time over `reps` launches (CUDA events on the
+    launch stream, after warm-up) and TFLOP/s against h*2*hd*T*(T+1)."""
+    import torch
+
+    sw = synth.ATTN_SWEEP
+    nh, nkv, hd = sw["n_head"], sw["n_head_kv"], sw["head_dim"]
+    out = {}
+    for T in Ts:
+        inp = synth.attention_inputs(T, nh, nkv, hd)
+        q, k, v = (torch.as_tensor(inp[n], device=dev).bfloat16() for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        ws = torch.empty(dtp.sdpa_workspace_size(T, nkv, hd, dtp.DTP_BF16), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(3):
+            dtp.sdpa_causal_gqa(q, k, v, o, nh, nkv, hd, hd ** -0.5, ws)
+        torch.cuda.synchronize(dev)
+        dtp.timer_enable(["attn"], reps)
+        for _ in range(reps):
+            dtp.sdpa_causal_gqa(q, k, v, o, nh, nkv, hd, hd ** -0.5, ws)
+        torch.cuda.synchronize(dev)
+        n, ms = dtp.timer_read("attn")
+        dtp.timer_disable()
+        dtp.check()
+        flops = nh * 2.0 * hd * T * (T + 1)
+        tf = flops / (ms / n / 1000.0) / 1e12
+        out[str(T)] = {"ms": ms / n, "tflops": tf, "frac": tf / peak if peak else None}
+    return out
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -184,6 +215,7 @@ def main():
     ap.add_argument("--workload", default="qwen3-8b-shape", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-attn-sweep", action="store_true")
     ap.add_argument("--n-layer", type=int, default=None,
                     help="override the layer count (profiling captures of a small case)")
     args = ap.parse_args()
@@ -373,6 +405,9 @@ def main():
         "e2e": e2e,
         "setup_s": setup_s,
     }
+    if not args.no_attn_sweep and cfg.precision == "bf16":
+        out["attention_sweep"] = {"shape": "h=32, g=8, hd=128, bf16, causal; kernel time only",
+                                  "peak": peak, "T": attention_sweep(dtp, dev, peak)}
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = OracleSample(cfg).run()
     print(json.dumps(out), flush=True)
