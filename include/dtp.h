@@ -205,6 +205,29 @@ int dtp_sdpa_causal_gqa(const void* q, const void* k, const void* v, void* out, 
                         int n_head, int n_head_kv, int head_dim, float scale, void* workspace,
                         size_t ws_bytes, dtp_stream_t stream);
 
+/* Allocation-free variant of dtp_sdpa_causal_gqa for dtype DTP_BF16.  The
+ * paper has no counterpart: this entry point exists for callers that cannot
+ * allocate device memory where they call attention -- an op handed only its
+ * input and output tensors, code running inside a stream-ordered region it
+ * does not own, or a runtime that forbids cudaMalloc after start-up.
+ * Same arguments, layouts and result as dtp_sdpa_causal_gqa with dtype
+ * DTP_BF16, minus the workspace: the transposed-V scratch lives in a fixed
+ * 8 MiB device array inside the library (held on every GPU that loads the
+ * library until the process exits).
+ *   - Limit: n_head_kv * head_dim * (T rounded up to 8) * 2 bytes must not
+ *     exceed 8 MiB (e.g. 8 kv heads x 128 dims x 4096 tokens); larger calls
+ *     return DTP_ERR_WORKSPACE without launching anything.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture.
+ *   - All calls share the one array: calls that overlap on the GPU (for
+ *     example on two streams at once) race on it.  Each call rewrites every
+ *     scratch element it reads, so nothing needs clearing between calls.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+int dtp_sdpa_causal_gqa_noalloc(const void* q, const void* k, const void* v, void* out, int T,
+                                int n_head, int n_head_kv, int head_dim, float scale,
+                                dtp_stream_t stream);
+
 /* SwiGLU (forward.rs `ffn_act`; the T-parallel page's `silu_mul`):
  * out[i] = silu(gate[i]) * up[i], silu(x) = x / (1 + e^-x); n elements of
  * dtype, arithmetic in float32.  out may alias gate or up. */
