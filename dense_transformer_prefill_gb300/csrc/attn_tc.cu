@@ -77,6 +77,46 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// One pass over a 128-key score row of S in TMEM (64 columns per load):
+// mx <- max(mx, unmasked scores) and, when WRITE, P = 2^(s*sl2 - m_ref) rounded
+// to bf16 into the row's 128-byte-swizzled shared-memory slots, rs += sum(P).
+// DIAG masks keys past the query (col > row) on the diagonal tile.
+template <bool DIAG, bool WRITE>
+__device__ __forceinline__ void tile_pass(uint32_t tS, uint8_t* Prow, int sw, int row, float sl2,
+                                          float m_ref, float& mx, float& rs) {
+#pragma unroll
+    for (int c = 0; c < BKV; c += 64) {
+        uint32_t r[64];
+        __syncwarp();
+        ptx::tmem_ld64(tS + c, r);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            float e[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int col = c + c8 * 8 + t;
+                const float sv = __uint_as_float(r[c8 * 8 + t]);
+                const bool masked = DIAG && col > row;
+                mx = masked ? mx : fmaxf(mx, sv);
+                if (WRITE) {
+                    e[t] = masked ? 0.f : ex2(fmaf(sv, sl2, -m_ref));
+                    rs += e[t];
+                }
+            }
+            if (WRITE) {
+                uint4 u;
+                u.x = ptx::pack_bf16x2(e[0], e[1]);
+                u.y = ptx::pack_bf16x2(e[2], e[3]);
+                u.z = ptx::pack_bf16x2(e[4], e[5]);
+                u.w = ptx::pack_bf16x2(e[6], e[7]);
+                const int chunk_all = (c >> 3) + c8;          // 16-byte chunk index 0..15
+                const int atom = chunk_all >> 3, chunk = chunk_all & 7;
+                *reinterpret_cast<uint4*>(Prow + atom * BQ * 128 + ((chunk ^ sw) << 4)) = u;
+            }
+        }
+    }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -266,24 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-            float s[BKV];
-#pragma unroll
-            for (int c = 0; c < BKV / 32; ++c) {
-                uint32_t r[32];
-                ptx::tmem_ld32(tS + c * 32, r);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(r[t]);
-            }
-            if (j == qt) {
-#pragma unroll
-                for (int c = 0; c < BKV; ++c)
-                    if (c > row) s[c] = -INFINITY;
-            }
-            float mx = s[0];
-#pragma unroll
-            for (int c = 1; c < BKV; ++c) mx = fmaxf(mx, s[c]);
-            const float m_tile = mx * p.scale_log2;
-            // O and P_i are still in use by PV_i(j-1) until o_done
+            // P_i and O_i are free once PV_i(j-1) has completed (it precedes S_i(j)
+            // on the tensor pipe, so this wait normally returns at once)
             if (j > 0) {
                 ok = ptx::wait_bounded(&o_done[i], (j - 1) & 1, abort_flag, &g_attn_err,
                                        ERRBIT_TIMEOUT);
@@ -293,44 +317,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tc_fence_after();
             }
-            // keep the running max unless this tile raises it by more than 2^8;
-            // then rescale l and (warp-wide, lanes without a raise use 1) O in TMEM
-            const bool need = m_tile > m + kRescaleLog2;
-            float alpha = 1.f;
-            if (need) {
-                alpha = ex2(m - m_tile);       // 0 on the first tile (m = -inf)
-                m = m_tile;
-                l *= alpha;
+            const bool diag = (j == qt);
+            const float sl2 = p.scale_log2;
+            // Speculative single pass: P against the running max m while finding the
+            // tile max.  If the tile raises a row's max by more than 2^8 (always on
+            // the first tile), that row takes the new max, l and O are rescaled and
+            // the warp redoes the pass.
+            float mx = -INFINITY, rs = 0.f;
+            if (j > 0) {
+                if (diag) tile_pass<true, true>(tS, Prow, sw, row, sl2, m, mx, rs);
+                else tile_pass<false, true>(tS, Prow, sw, row, sl2, m, mx, rs);
+            } else {
+                if (diag) tile_pass<true, false>(tS, Prow, sw, row, sl2, m, mx, rs);
+                else tile_pass<false, false>(tS, Prow, sw, row, sl2, m, mx, rs);
             }
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
+            const float m_tile = mx * sl2;
+            const bool need = (j == 0) || (m_tile > m + kRescaleLog2);
+            if (__any_sync(0xffffffffu, need)) {
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2(m - m_tile);       // 0 on the first tile (m = -inf)
+                    m = m_tile;
+                    l *= alpha;
+                }
+                if (j > 0) {
 #pragma unroll 1
-                for (int c = 0; c < HD; c += 32) {
-                    uint32_t r[32];
-                    __syncwarp();
-                    ptx::tmem_ld32(tO + c, r);
+                    for (int c = 0; c < HD; c += 32) {
+                        uint32_t r[32];
+                        __syncwarp();
+                        ptx::tmem_ld32(tO + c, r);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t)
-                        r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
-                    ptx::tmem_st32(tO + c, r);
+                        for (int t = 0; t < 32; ++t)
+                            r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+                        ptx::tmem_st32(tO + c, r);
+                    }
                 }
-            }
-            // P = 2^(s*scale_log2 - m), row sum, bf16 into swizzled shared memory
-            float rs = 0.f;
-#pragma unroll
-            for (int c8 = 0; c8 < BKV / 8; ++c8) {
-                float e[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    e[t] = ex2(fmaf(s[c8 * 8 + t], p.scale_log2, -m));
-                    rs += e[t];
-                }
-                uint4 u;
-                u.x = ptx::pack_bf16x2(e[0], e[1]);
-                u.y = ptx::pack_bf16x2(e[2], e[3]);
-                u.z = ptx::pack_bf16x2(e[4], e[5]);
-                u.w = ptx::pack_bf16x2(e[6], e[7]);
-                const int atom = c8 >> 3, chunk = c8 & 7;
-                *reinterpret_cast<uint4*>(Prow + atom * BQ * 128 + ((chunk ^ sw) << 4)) = u;
+                rs = 0.f;
+                float unused = -INFINITY;
+                if (diag) tile_pass<true, true>(tS, Prow, sw, row, sl2, m, unused, rs);
+                else tile_pass<false, true>(tS, Prow, sw, row, sl2, m, unused, rs);
             }
             l += rs;
             ptx::fence_proxy_async_smem();

@@ -43,8 +43,10 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
-    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int STAGES = BN == 256 ? 4 : (BN == 224 ? 5 : 6);
+    // two accumulators; the second starts at a 256-column boundary when BN > 128
+    static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;
+    static constexpr int TMEM_COLS = 2 * ACC_STRIDE;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 };
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        ERRBIT_TIMEOUT))
                     break;
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t d_tmem = tmem_base + acc * C::ACC_STRIDE;
                 bool ok = true;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!ptx::wait_bounded(&full[stage], phase, abort_flag, &g_gemm_err,
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               ERRBIT_TIMEOUT);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
-            const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+            const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_STRIDE;
             const int grow = mb * BM + row, n0 = nb * BN;
             if (EPI == EPI_STORE) epi_store<BN>(p, tbase, grow, n0);
             if (EPI == EPI_QKV) epi_qkv<BN>(p, tbase, grow, n0);
@@ -408,9 +410,29 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const Para
 
 }  // namespace
 
+// Tile width: the fused QKV and SwiGLU epilogues need 256 (whole heads / whole
+// 128-column gate-up blocks).  A plain store picks the width whose persistent
+// schedule finishes first: waves(BN) * BN, waves = ceil(tiles / SMs).
+static int pick_bn(int M, int N, GemmEpi epi) {
+    if (epi != EPI_STORE) return 256;
+    if (N <= 128) return 128;
+    const long long tm = (M + BM - 1) / BM, sms = num_sms();
+    int best = 256;
+    long long best_cost = -1;
+    for (int bn : {256, 224}) {
+        const long long tiles = tm * ((N + bn - 1) / bn);
+        const long long cost = (tiles + sms - 1) / sms * bn;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
 cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,
                            GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind) {
-    const int BN = (N >= 256 || epi != EPI_STORE) ? 256 : 128;
+    const int BN = pick_bn(M, N, epi);
     CUtensorMap ta, tb;
     if (!make_tmap_2d(&ta, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, K, BM, BK))
         return cudaErrorInvalidValue;
@@ -437,6 +459,7 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M
         if (epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU>(ta, tb, p, s);
         return launch_impl<256, EPI_STORE>(ta, tb, p, s);
     }
+    if (BN == 224) return launch_impl<224, EPI_STORE>(ta, tb, p, s);
     return launch_impl<128, EPI_STORE>(ta, tb, p, s);
 }
 

@@ -116,9 +116,69 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
     }
 }
 
+// Register-resident variant for cols % 4 == 0 and cols <= 16 * blockDim: each
+// thread holds up to 4 float4 of the row, so x is read from memory once.
+template <typename To>
+__device__ __forceinline__ void store4(To* y, int c, float a, float b, float cc, float d) {
+    st_elt(y, c + 0, a);
+    st_elt(y, c + 1, b);
+    st_elt(y, c + 2, cc);
+    st_elt(y, c + 3, d);
+}
+template <>
+__device__ __forceinline__ void store4(__nv_bfloat16* y, int c, float a, float b, float cc,
+                                       float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(cc, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(y + c) = u;
+}
+
+template <typename To>
+__global__ void rmsnorm_reg_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                   To* __restrict__ y, int cols, float eps) {
+    __shared__ float red[32];
+    const size_t r = blockIdx.x;
+    const float4* xr = reinterpret_cast<const float4*>(x + r * cols);
+    To* yr = y + r * cols;
+    const int n4 = cols >> 2;
+    float4 v[4];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c4 = threadIdx.x + i * blockDim.x;
+        if (c4 < n4) {
+            v[i] = xr[c4];
+            ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+        }
+    }
+    ss = block_sum(ss, red);
+    const float rstd = 1.0f / sqrtf(ss / (float)cols + eps);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c4 = threadIdx.x + i * blockDim.x;
+        if (c4 < n4) {
+            const float4 g = reinterpret_cast<const float4*>(w)[c4];
+            store4(yr, 4 * c4, v[i].x * rstd * g.x, v[i].y * rstd * g.y, v[i].z * rstd * g.z,
+                   v[i].w * rstd * g.w);
+        }
+    }
+}
+
 cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype, int rows,
                            int cols, float eps, cudaStream_t s) {
     LaunchScope ls(DTP_K_RMSNORM, s);
+    const bool vec_ok = (cols % 4 == 0) && cols <= 16 * 1024;
+    if (vec_ok) {
+        int threads = ((cols + 15) / 16 + 31) / 32 * 32;     // threads * 16 >= cols
+        if (threads < 32) threads = 32;
+        if (y_dtype == DTP_BF16)
+            rmsnorm_reg_kernel<<<rows, threads, 0, s>>>(x, w, (__nv_bfloat16*)y, cols, eps);
+        else
+            rmsnorm_reg_kernel<<<rows, threads, 0, s>>>(x, w, (float*)y, cols, eps);
+        return cudaGetLastError();
+    }
     int threads = cols >= 1024 ? 256 : (cols >= 256 ? 128 : 32);
     if (y_dtype == DTP_BF16)
         rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (__nv_bfloat16*)y, cols, eps);
