@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     config_from,
     fwd_prefill,
     fwd_prefill_host,
+    gate_up_swiglu,
     last_error,
     launch_count,
     linear,
@@ -26,9 +27,11 @@ from ._binding import (  # noqa: F401
     pack_layer,
     packed_size,
     qk_norm_rope_neox,
+    qkv_norm_rope,
     rms_norm,
     sdpa_causal_gqa,
     sdpa_workspace_size,
+    selftest_wait_timeout,
     swiglu,
     timer_disable,
     timer_enable,

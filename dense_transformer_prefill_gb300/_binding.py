@@ -64,6 +64,12 @@ _SIGS = {
     "dtp_swiglu": ([c_void_p, c_void_p, c_void_p, c_int, c_size_t, c_void_p], c_int),
     "dtp_linear": ([c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p,
                     c_void_p], c_int),
+    "dtp_qkv_norm_rope_workspace_size": ([c_int, c_int], c_size_t),
+    "dtp_qkv_norm_rope": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                           c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_float,
+                           c_void_p, c_size_t, c_void_p], c_int),
+    "dtp_gate_up_swiglu": ([c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p], c_int),
+    "dtp_selftest_wait_timeout": ([c_void_p], c_int),
     "dtp_timer_enable": ([ctypes.c_uint, c_int], c_int),
     "dtp_timer_disable": ([], c_int),
     "dtp_timer_read": ([c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_float)], c_int),
@@ -210,6 +216,30 @@ def linear(x, W, y, residual=None, stream=None) -> None:
     N = W.shape[0]
     _ok(lib().dtp_linear(x.data_ptr(), W.data_ptr(), y.data_ptr(), _dtype_code(x), _dtype_code(y),
                          M, N, K, _ptr(residual), _stream(stream)))
+
+
+def qkv_norm_rope(h, w_qkv, q_norm, k_norm, q, k, vt, n_head: int, n_head_kv: int,
+                  head_dim: int, rope_dim_count: int, freq_base: float, eps: float,
+                  workspace=None, stream=None) -> None:
+    T, d = h.shape
+    if workspace is None:
+        workspace = torch.empty(lib().dtp_qkv_norm_rope_workspace_size(T, rope_dim_count),
+                                dtype=torch.uint8, device=h.device)
+    _ok(lib().dtp_qkv_norm_rope(h.data_ptr(), w_qkv.data_ptr(), q_norm.data_ptr(), k_norm.data_ptr(),
+                                q.data_ptr(), k.data_ptr(), vt.data_ptr(), vt.shape[1], T, d, n_head,
+                                n_head_kv, head_dim, rope_dim_count, freq_base, eps,
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream(stream)))
+
+
+def gate_up_swiglu(z, w_gu, act, stream=None) -> None:
+    T, d = z.shape
+    _ok(lib().dtp_gate_up_swiglu(z.data_ptr(), w_gu.data_ptr(), act.data_ptr(), T, d, act.shape[1],
+                                 _stream(stream)))
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    _ok(lib().dtp_selftest_wait_timeout(_stream(stream)))
 
 
 def timer_enable(kinds, capacity: int) -> None:

@@ -606,6 +606,77 @@ int dtp_linear(const void* x, const void* W, void* y, int dtype, int y_dtype, in
     return DTP_OK;
 }
 
+size_t dtp_qkv_norm_rope_workspace_size(int T, int rope_dim_count) {
+    if (T <= 0 || rope_dim_count <= 0 || rope_dim_count % 2) return 0;
+    return align_up((size_t)T * (rope_dim_count / 2) * sizeof(float2), 256);
+}
+
+int dtp_qkv_norm_rope(const void* h, const void* w_qkv, const float* q_norm, const float* k_norm,
+                      void* q, void* k, void* vt, int ldvt, int T, int d, int n_head,
+                      int n_head_kv, int head_dim, int rope_dim_count, float freq_base, float eps,
+                      void* workspace, size_t ws_bytes, dtp_stream_t stream) {
+    if (!h || !w_qkv || !q_norm || !k_norm || !q || !k || !vt || !workspace)
+        return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    if (T <= 0 || d <= 0 || n_head <= 0 || n_head_kv <= 0 || n_head % n_head_kv)
+        return fail(DTP_ERR_INVALID_ARG, "bad sizes (T, d, n_head, n_head_kv)");
+    if (rope_dim_count <= 0 || rope_dim_count % 2 || rope_dim_count > head_dim)
+        return fail(DTP_ERR_INVALID_ARG, "rope_dim_count must be even and in [2, head_dim]");
+    if (!(freq_base > 0.f) || !(eps >= 0.f))
+        return fail(DTP_ERR_INVALID_ARG, "freq_base must be > 0 and eps >= 0");
+    if (ldvt < T || ldvt % 8) return fail(DTP_ERR_INVALID_ARG, "ldvt must be >= T and a multiple of 8");
+    if (d % 8 || (head_dim != 64 && head_dim != 128) || (rope_dim_count / 2) % 32 ||
+        (head_dim - rope_dim_count) % 32)
+        return fail(DTP_ERR_UNSUPPORTED,
+                    "needs d %% 8 == 0, head_dim 64 or 128, rope_dim_count/2 and "
+                    "head_dim-rope_dim_count multiples of 32");
+    if (ws_bytes < dtp_qkv_norm_rope_workspace_size(T, rope_dim_count))
+        return fail(DTP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes,
+                    dtp_qkv_norm_rope_workspace_size(T, rope_dim_count));
+    if (!aligned(h, 16) || !aligned(w_qkv, 16) || !aligned(q, 16) || !aligned(k, 16) ||
+        !aligned(workspace, 16))
+        return fail(DTP_ERR_INVALID_ARG, "h, w_qkv, q, k and workspace must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    float2* rope = (float2*)workspace;
+    DTP_CUDA_CHECK(launch_rope_table(rope, T, rope_dim_count, freq_base, s));
+    GemmEpiArgs e;
+    e.q = (__nv_bfloat16*)q;
+    e.k = (__nv_bfloat16*)k;
+    e.vt = (__nv_bfloat16*)vt;
+    e.ldvt = ldvt;
+    e.q_norm = q_norm;
+    e.k_norm = k_norm;
+    e.rope = rope;
+    e.n_head = n_head;
+    e.n_head_kv = n_head_kv;
+    e.head_dim = head_dim;
+    e.rope_dims = rope_dim_count;
+    e.eps = eps;
+    const int nqkv = (n_head + 2 * n_head_kv) * head_dim;
+    DTP_CUDA_CHECK(launch_gemm_tc((const __nv_bfloat16*)h, (const __nv_bfloat16*)w_qkv, T, nqkv,
+                                  d, EPI_QKV, e, s, DTP_K_GEMM_QKV));
+    return DTP_OK;
+}
+
+int dtp_gate_up_swiglu(const void* z, const void* w_gu, void* act, int T, int d, int n_ff,
+                       dtp_stream_t stream) {
+    if (!z || !w_gu || !act) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    if (T <= 0 || d <= 0 || n_ff <= 0) return fail(DTP_ERR_INVALID_ARG, "sizes must be >= 1");
+    if (d % 8 || n_ff % 64)
+        return fail(DTP_ERR_UNSUPPORTED, "needs d %% 8 == 0 and n_ff %% 64 == 0");
+    if (!aligned(z, 16) || !aligned(w_gu, 16) || !aligned(act, 16))
+        return fail(DTP_ERR_INVALID_ARG, "z, w_gu and act must be 16-byte aligned");
+    GemmEpiArgs e;
+    e.act = (__nv_bfloat16*)act;
+    DTP_CUDA_CHECK(launch_gemm_tc((const __nv_bfloat16*)z, (const __nv_bfloat16*)w_gu, T, 2 * n_ff,
+                                  d, EPI_SWIGLU, e, (cudaStream_t)stream, DTP_K_GEMM_GATEUP));
+    return DTP_OK;
+}
+
+int dtp_selftest_wait_timeout(dtp_stream_t stream) {
+    DTP_CUDA_CHECK(launch_selftest_wait((cudaStream_t)stream));
+    return DTP_OK;
+}
+
 // ------------------------------------------------------------------------- timers
 int dtp_timer_enable(unsigned kind_mask, int capacity) {
     if (capacity <= 0 || capacity > 1 << 20) return fail(DTP_ERR_INVALID_ARG, "bad capacity");

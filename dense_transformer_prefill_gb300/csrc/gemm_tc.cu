@@ -32,6 +32,25 @@ unsigned read_clear_gemm_errors() {
     return v;
 }
 
+// One thread waits on an mbarrier nothing arrives at: the bounded wait gives up,
+// raises the error word and the kernel returns.
+__global__ void selftest_wait_kernel() {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::wait_bounded(&bar, 0, &abort_flag, &g_gemm_err, ERRBIT_TIMEOUT);
+    }
+}
+
+cudaError_t launch_selftest_wait(cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    selftest_wait_kernel<<<1, 32, 0, s>>>();
+    return cudaGetLastError();
+}
+
 namespace {
 
 constexpr int BM = 128;

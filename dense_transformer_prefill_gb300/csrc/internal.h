@@ -110,6 +110,8 @@ struct GemmEpiArgs {
 cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,
                            GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind);
 
+cudaError_t launch_selftest_wait(cudaStream_t s);
+
 // ----------------------------------------------------------------------------- tcgen05 attention
 // q [T, n_head*hd] bf16, k [T, n_head_kv*hd] bf16, vt [n_head_kv*hd, ldvt] bf16,
 // out [T, n_head*hd] bf16.

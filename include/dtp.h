@@ -244,6 +244,46 @@ int dtp_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
 int dtp_linear(const void* x, const void* W, void* y, int dtype, int y_dtype, int M, int N, int K,
                const float* residual, dtp_stream_t stream);
 
+/* Fused QKV projection with per-head QK-RMSNorm and NeoX RoPE: the bf16 path's
+ * first GEMM of a layer (forward.rs: the wq/wk/wv `e.matmul`s, the q/k
+ * `rms_norm` over head_dim rows and `e.rope_neox`, as one tcgen05 GEMM whose
+ * epilogue normalises and rotates each head at positions 0..T-1).
+ *   h      device bf16 [T, d] (the normed layer input)
+ *   w_qkv  device bf16 [(n_head + 2 n_head_kv) * head_dim, d]: Wq rows, then Wk, then Wv
+ *   q_norm, k_norm  device float32 [head_dim]
+ *   q      device bf16 [T, n_head*head_dim]     (written)
+ *   k      device bf16 [T, n_head_kv*head_dim]  (written)
+ *   vt     device bf16 [n_head_kv*head_dim, ldvt], v transposed (written; columns
+ *          T..ldvt-1 untouched); ldvt >= T, ldvt % 8 == 0
+ *   workspace  device, >= dtp_qkv_norm_rope_workspace_size(T, rope_dim_count)
+ *          bytes, 16-byte aligned (the cos/sin table).
+ * Requires d % 8 == 0, head_dim 64 or 128, (rope_dim_count/2) % 32 == 0 and
+ * (head_dim - rope_dim_count) % 32 == 0. */
+size_t dtp_qkv_norm_rope_workspace_size(int T, int rope_dim_count);
+int dtp_qkv_norm_rope(const void* h, const void* w_qkv, const float* q_norm, const float* k_norm,
+                      void* q, void* k, void* vt, int ldvt, int T, int d, int n_head,
+                      int n_head_kv, int head_dim, int rope_dim_count, float freq_base, float eps,
+                      void* workspace, size_t ws_bytes, dtp_stream_t stream);
+
+/* Fused gate/up projection and SwiGLU: the bf16 path's FFN GEMM (forward.rs:
+ * the ffn_gate / ffn_up `e.matmul`s and `ffn_act`).
+ *   z      device bf16 [T, d]
+ *   w_gu   device bf16 [2*n_ff, d]: gate and up rows interleaved in blocks of 64
+ *          (rows 128b..128b+63 = gate rows 64b..64b+63, rows 128b+64..128b+127 =
+ *          up rows 64b..64b+63), the layout dtp_pack_layer writes
+ *   act    device bf16 [T, n_ff]: act = silu(z Wgate^T) * (z Wup^T)  (written)
+ * Requires d % 8 == 0 and n_ff % 64 == 0. */
+int dtp_gate_up_swiglu(const void* z, const void* w_gu, void* act, int T, int d, int n_ff,
+                       dtp_stream_t stream);
+
+/* Failure-detection self-test.  Launches one CTA whose thread waits, through
+ * the same bounded wait every pipeline kernel uses, on an mbarrier that nothing
+ * arrives at.  After about one second the wait gives up, raises the device
+ * error word and the kernel returns; dtp_check then reports
+ * DTP_ERR_DEVICE_TIMEOUT and the CUDA context stays usable.  Returns the
+ * launch status. */
+int dtp_selftest_wait_timeout(dtp_stream_t stream);
+
 /* ------------------------------------------------------------------------------------
  * Kernel timing (measurement aid; off by default)
  * ------------------------------------------------------------------------------------ */

@@ -262,3 +262,68 @@ def test_attention_sweep(dtp, T, r):
     ref = oracle.sdpa_causal_gqa(qr, kr, v, nh, nkv, hd, 1 / math.sqrt(hd), rows=rows)
     got = out.float().cpu().numpy()[rows]
     _attn_close(got, ref, np.abs(v).max())
+
+
+# ----------------------------------------------------------------------------- fused epilogues
+@pytest.mark.parametrize("T,d,nh,nkv,hd,r", [(1, 64, 2, 1, 64, 64), (130, 512, 8, 4, 64, 64),
+                                              (300, 1024, 4, 2, 128, 64), (257, 512, 8, 2, 128, 128)])
+def test_qkv_norm_rope_fused(dtp, T, d, nh, nkv, hd, r):
+    """QKV GEMM with per-head RMSNorm + NeoX RoPE in its epilogue, against the oracle
+    on the same bf16 operands; outputs agree to one bf16 rounding."""
+    nq, nk = nh * hd, nkv * hd
+    h = bf16_round32(synth.normal(13, 1300, (T, d)))
+    W = bf16_round32(synth.normal(13, 1301, (nq + 2 * nk, d), std=0.05))
+    qn = synth.normal(13, 1302, (hd,), mean=1.0, std=0.1)
+    kn = synth.normal(13, 1303, (hd,), mean=1.0, std=0.1)
+    q = torch.empty((T, nq), dtype=torch.bfloat16, device=dev)
+    k = torch.empty((T, nk), dtype=torch.bfloat16, device=dev)
+    ldvt = (T + 7) // 8 * 8
+    vt = torch.zeros((nk, ldvt), dtype=torch.bfloat16, device=dev)
+    dtp.qkv_norm_rope(t32(h).bfloat16(), t32(W).bfloat16(), t32(qn), t32(kn), q, k, vt, nh, nkv, hd,
+                      r, 1e6, 1e-6)
+    torch.cuda.synchronize()
+    dtp.check()
+    qkv = oracle.linear(h, W)
+    pos = np.arange(T)
+    rq = oracle.round_bf16(oracle.rope_neox(oracle.qk_norm(qkv[:, :nq], qn, hd, 1e-6), pos, nh, hd, r, 1e6))
+    rk = oracle.round_bf16(oracle.rope_neox(oracle.qk_norm(qkv[:, nq:nq + nk], kn, hd, 1e-6), pos, nkv, hd, r, 1e6))
+    rv = oracle.round_bf16(qkv[:, nq + nk:])
+    np.testing.assert_allclose(q.float().cpu().numpy(), rq, rtol=2 ** -7, atol=1e-5)
+    np.testing.assert_allclose(k.float().cpu().numpy(), rk, rtol=2 ** -7, atol=1e-5)
+    np.testing.assert_allclose(vt.float().cpu().numpy()[:, :T].T, rv, rtol=2 ** -7, atol=1e-5)
+    assert not vt[:, T:].any()                       # padding columns untouched
+
+
+@pytest.mark.parametrize("T,d,F", [(1, 64, 64), (200, 512, 1536), (513, 1024, 3072)])
+def test_gate_up_swiglu_fused(dtp, T, d, F):
+    """gate/up GEMM with SwiGLU in its epilogue on the interleaved weight layout."""
+    z = bf16_round32(synth.normal(14, 1400, (T, d)))
+    Wg = bf16_round32(synth.normal(14, 1401, (F, d), std=0.05))
+    Wu = bf16_round32(synth.normal(14, 1402, (F, d), std=0.05))
+    W = np.empty((2 * F, d), np.float32)
+    for b in range(F // 64):                          # the layout dtp_pack_layer writes
+        W[128 * b:128 * b + 64] = Wg[64 * b:64 * b + 64]
+        W[128 * b + 64:128 * b + 128] = Wu[64 * b:64 * b + 64]
+    act = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
+    dtp.gate_up_swiglu(t32(z).bfloat16(), t32(W).bfloat16(), act)
+    torch.cuda.synchronize()
+    dtp.check()
+    ref = oracle.round_bf16(oracle.swiglu(oracle.linear(z, Wg), oracle.linear(z, Wu)))
+    np.testing.assert_allclose(act.float().cpu().numpy(), ref, rtol=2 ** -7, atol=1e-5)
+
+
+def test_bounded_wait_gives_up_and_context_survives(dtp):
+    """A pipeline wait on a barrier nothing arrives at ends with an error status
+    instead of a hang; the context stays usable afterwards."""
+    dtp.selftest_wait_timeout()
+    with pytest.raises(dtp.DtpError) as e:
+        dtp.check()
+    assert e.value.code == -6
+    dtp.check()                                      # cleared
+    x = bf16_round32(synth.normal(15, 1500, (64, 128)))
+    W = bf16_round32(synth.normal(15, 1501, (256, 128)))
+    y = torch.empty((64, 256), dtype=torch.float32, device=dev)
+    dtp.linear(t32(x).bfloat16(), t32(W).bfloat16(), y)
+    torch.cuda.synchronize()
+    dtp.check()
+    np.testing.assert_allclose(y.cpu().numpy(), oracle.linear(x, W), rtol=0, atol=1e-4)
