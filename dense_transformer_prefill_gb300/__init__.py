@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     check,
     config_from,
     fwd_prefill,
+    fwd_prefill_ex,
     fwd_prefill_host,
     gate_up_swiglu,
     last_error,

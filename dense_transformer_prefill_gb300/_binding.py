@@ -37,6 +37,11 @@ class LayerSrc(ctypes.Structure):
                                        "ffn_norm", "w_gate", "w_up", "w_down")]
 
 
+class FwdOutputs(ctypes.Structure):
+    _fields_ = [("logits", c_void_p), ("last_only", c_int), ("hidden", c_void_p),
+                ("k_cache", c_void_p), ("v_cache", c_void_p)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -52,6 +57,8 @@ _SIGS = {
     "dtp_workspace_size_host": ([ctypes.POINTER(Config), c_int], c_size_t),
     "dtp_fwd_prefill": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int, c_void_p,
                          c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "dtp_fwd_prefill_ex": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int,
+                            ctypes.POINTER(FwdOutputs), c_void_p, c_size_t, c_void_p], c_int),
     "dtp_fwd_prefill_host": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int,
                               c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "dtp_check": ([c_void_p], c_int),
@@ -165,6 +172,16 @@ def fwd_prefill(c: Config, packed: torch.Tensor, tokens: torch.Tensor, logits: t
                               tokens.numel(), logits.data_ptr(), _ptr(hidden),
                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                               _stream(stream)))
+
+
+def fwd_prefill_ex(c: Config, packed: torch.Tensor, tokens: torch.Tensor, workspace: torch.Tensor,
+                   logits=None, last_only: bool = False, hidden=None, k_cache=None, v_cache=None,
+                   stream=None) -> None:
+    o = FwdOutputs(_ptr(logits), 1 if last_only else 0, _ptr(hidden), _ptr(k_cache), _ptr(v_cache))
+    _ok(lib().dtp_fwd_prefill_ex(ctypes.byref(c), packed.data_ptr(),
+                                 packed.numel() * packed.element_size(), tokens.data_ptr(),
+                                 tokens.numel(), ctypes.byref(o), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def fwd_prefill_host(c: Config, packed: torch.Tensor, tokens_host: torch.Tensor,

@@ -221,8 +221,10 @@ static bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t
 
 // ----------------------------------------------------------------------------- forward
 static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
-                   const uint32_t* tokens, int T, float* logits, float* hidden, uint8_t* ws,
+                   const uint32_t* tokens, int T, const dtp_fwd_outputs& o, uint8_t* ws,
                    const Workspace& W, cudaStream_t s) {
+    float* logits = o.logits;
+    float* hidden = o.hidden;
     const int d = c->n_embd, hd = c->head_dim, h = c->n_head, g = c->n_head_kv, F = c->n_ff;
     const int nq = h * hd, nk = g * hd, nqkv = nq + 2 * nk;
     float* x = (float*)(ws + W.x);
@@ -247,6 +249,12 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
         DTP_CUDA_CHECK(launch_qk_norm_rope(qkv + nq, DTP_F32, nqkv, (const float*)(lp + L.k_norm),
                                            nullptr, T, g, hd, c->rope_dim_count,
                                            c->rope_freq_base, c->rms_eps, s));
+        if (o.k_cache)
+            DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nq, nqkv, (float*)o.k_cache + (size_t)l * T * nk,
+                                                nk, T, nk, s));
+        if (o.v_cache)
+            DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nq + nk, nqkv,
+                                                (float*)o.v_cache + (size_t)l * T * nk, nk, T, nk, s));
         DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, qkv + nq, nqkv, qkv + nq + nk, nqkv, 0, attn,
                                         nq, DTP_F32, T, h, g, hd, scale, s));
         DTP_CUDA_CHECK(launch_gemm_simt(attn, nq, (const float*)(lp + L.wo), x, DTP_F32, d, T, d,
@@ -262,16 +270,21 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
     if (hidden)
         DTP_CUDA_CHECK(
             launch_copy_f32(x, hidden + (size_t)c->n_layer * T * d, (size_t)T * d, s));
-    DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(P + L.output_norm), hb, DTP_F32, T, d,
+    if (!logits) return DTP_OK;
+    const int rows = o.last_only ? 1 : T;
+    const float* xf = x + (size_t)(T - rows) * d;
+    DTP_CUDA_CHECK(launch_rmsnorm(xf, (const float*)(P + L.output_norm), hb, DTP_F32, rows, d,
                                   c->rms_eps, s));
     DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(P + L.output), logits, DTP_F32,
-                                    c->n_vocab, T, c->n_vocab, d, nullptr, s, DTP_K_GEMM_LMHEAD));
+                                    c->n_vocab, rows, c->n_vocab, d, nullptr, s, DTP_K_GEMM_LMHEAD));
     return DTP_OK;
 }
 
 static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
-                    const uint32_t* tokens, int T, float* logits, float* hidden, uint8_t* ws,
+                    const uint32_t* tokens, int T, const dtp_fwd_outputs& o, uint8_t* ws,
                     const Workspace& W, cudaStream_t s) {
+    float* logits = o.logits;
+    float* hidden = o.hidden;
     typedef __nv_bfloat16 bf;
     const int d = c->n_embd, hd = c->head_dim, h = c->n_head, g = c->n_head_kv, F = c->n_ff;
     const int nq = h * hd, nk = g * hd, nqkv = nq + 2 * nk;
@@ -294,10 +307,13 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.attn_norm), hb, DTP_BF16, T, d,
                                       c->rms_eps, s));
         GemmEpiArgs e;
+        // with a KV cache the keys are written straight into it (attention reads them there)
+        bf* kl = o.k_cache ? (bf*)o.k_cache + (size_t)l * T * nk : k;
         e.q = q;
-        e.k = k;
+        e.k = kl;
         e.vt = vt;
         e.ldvt = W.ldvt;
+        e.v_rows = o.v_cache ? (bf*)o.v_cache + (size_t)l * T * nk : nullptr;
         e.q_norm = (const float*)(lp + L.q_norm);
         e.k_norm = (const float*)(lp + L.k_norm);
         e.rope = rope;
@@ -309,9 +325,9 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(lp + L.w_qkv), T, nqkv, d, EPI_QKV, e, s,
                                       DTP_K_GEMM_QKV));
         if (fa)
-            DTP_CUDA_CHECK(launch_attn_tc(q, k, vt, W.ldvt, attn, T, h, g, hd, scale, s));
+            DTP_CUDA_CHECK(launch_attn_tc(q, kl, vt, W.ldvt, attn, T, h, g, hd, scale, s));
         else
-            DTP_CUDA_CHECK(launch_attn_simt(q, nq, k, nk, vt, (int)W.ldvt, 1, attn, nq, DTP_BF16,
+            DTP_CUDA_CHECK(launch_attn_simt(q, nq, kl, nk, vt, (int)W.ldvt, 1, attn, nq, DTP_BF16,
                                             T, h, g, hd, scale, s));
         GemmEpiArgs eo;
         eo.y = x;
@@ -332,13 +348,16 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
     if (hidden)
         DTP_CUDA_CHECK(
             launch_copy_f32(x, hidden + (size_t)c->n_layer * T * d, (size_t)T * d, s));
-    DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(P + L.output_norm), hb, DTP_BF16, T, d,
-                                  c->rms_eps, s));
+    if (!logits) return DTP_OK;
+    // forward.rs `forward_last`: only the last position's logits
+    const int rows = o.last_only ? 1 : T;
+    DTP_CUDA_CHECK(launch_rmsnorm(x + (size_t)(T - rows) * d, (const float*)(P + L.output_norm), hb,
+                                  DTP_BF16, rows, d, c->rms_eps, s));
     GemmEpiArgs el;
     el.y = logits;
     el.y_dtype = DTP_F32;
     el.ldy = c->n_vocab;
-    DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(P + L.output), T, c->n_vocab, d, EPI_STORE, el,
+    DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(P + L.output), rows, c->n_vocab, d, EPI_STORE, el,
                                   s, DTP_K_GEMM_LMHEAD));
     return DTP_OK;
 }
@@ -427,38 +446,52 @@ size_t dtp_workspace_size_host(const dtp_config* cfg, int T) {
 }
 
 static int fwd_checked(const dtp_config* cfg, const void* packed, size_t packed_bytes,
-                       const uint32_t* tokens, int T, float* logits, float* hidden,
+                       const uint32_t* tokens, int T, const dtp_fwd_outputs& out,
                        void* workspace, size_t ws_bytes, bool host_layout, dtp_stream_t stream) {
+    float* logits = out.logits;
+    float* hidden = out.hidden;
     int rc = validate_config(cfg);
     if (rc) return rc;
     if (T <= 0) return fail(DTP_ERR_INVALID_ARG, "T must be >= 1 (got %d)", T);
-    if (!packed || !tokens || !logits || !workspace)
-        return fail(DTP_ERR_INVALID_ARG, "NULL packed, tokens, logits or workspace");
+    if (!packed || !tokens || !workspace)
+        return fail(DTP_ERR_INVALID_ARG, "NULL packed, tokens or workspace");
+    if (!logits && !hidden && !out.k_cache && !out.v_cache)
+        return fail(DTP_ERR_INVALID_ARG, "no output requested");
     PackedLayout L = packed_layout(cfg);
     if (packed_bytes < L.total)
         return fail(DTP_ERR_WORKSPACE, "packed buffer %zu < %zu bytes", packed_bytes, L.total);
     Workspace W = workspace_layout(cfg, T, host_layout);
     if (ws_bytes < W.total)
         return fail(DTP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, W.total);
-    if (!aligned(workspace, 256) || !aligned(packed, 256) || !aligned(logits, 16) ||
-        (hidden && !aligned(hidden, 16)))
+    if (!aligned(workspace, 256) || !aligned(packed, 256) || (logits && !aligned(logits, 16)) ||
+        (hidden && !aligned(hidden, 16)) || (out.k_cache && !aligned(out.k_cache, 16)) ||
+        (out.v_cache && !aligned(out.v_cache, 16)))
         return fail(DTP_ERR_INVALID_ARG,
-                    "workspace/packed must be 256-byte aligned, logits/hidden 16-byte aligned");
+                    "workspace/packed must be 256-byte aligned, outputs 16-byte aligned");
     if (cfg->precision == DTP_PREC_BF16 && (cfg->n_vocab % 4))
         return fail(DTP_ERR_UNSUPPORTED, "bf16 path: n_vocab must be a multiple of 4");
     cudaStream_t s = (cudaStream_t)stream;
     if (cfg->precision == DTP_PREC_BF16)
-        return fwd_bf16(cfg, (const uint8_t*)packed, L, tokens, T, logits, hidden,
-                        (uint8_t*)workspace, W, s);
-    return fwd_f32(cfg, (const uint8_t*)packed, L, tokens, T, logits, hidden, (uint8_t*)workspace,
-                   W, s);
+        return fwd_bf16(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, s);
+    return fwd_f32(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, s);
 }
 
 int dtp_fwd_prefill(const dtp_config* cfg, const void* packed, size_t packed_bytes,
                     const uint32_t* tokens, int T, float* logits, float* hidden, void* workspace,
                     size_t ws_bytes, dtp_stream_t stream) {
-    return fwd_checked(cfg, packed, packed_bytes, tokens, T, logits, hidden, workspace, ws_bytes,
-                       false, stream);
+    if (!logits) return fail(DTP_ERR_INVALID_ARG, "NULL logits");
+    dtp_fwd_outputs o = {};
+    o.logits = logits;
+    o.hidden = hidden;
+    return fwd_checked(cfg, packed, packed_bytes, tokens, T, o, workspace, ws_bytes, false, stream);
+}
+
+int dtp_fwd_prefill_ex(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                       const uint32_t* tokens, int T, const dtp_fwd_outputs* out, void* workspace,
+                       size_t ws_bytes, dtp_stream_t stream) {
+    if (!out) return fail(DTP_ERR_INVALID_ARG, "NULL outputs");
+    return fwd_checked(cfg, packed, packed_bytes, tokens, T, *out, workspace, ws_bytes, false,
+                       stream);
 }
 
 int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packed_bytes,
@@ -482,8 +515,9 @@ int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packe
     uint32_t* tok_d = (uint32_t*)(ws + W.tokens);
     float* logit_d = (float*)(ws + W.logits);
     DTP_CUDA_CHECK(cudaMemcpyAsync(tok_d, tokens_host, (size_t)T * 4, cudaMemcpyHostToDevice, s));
-    rc = fwd_checked(cfg, packed, packed_bytes, tok_d, T, logit_d, nullptr, workspace, ws_bytes,
-                     true, stream);
+    dtp_fwd_outputs o = {};
+    o.logits = logit_d;
+    rc = fwd_checked(cfg, packed, packed_bytes, tok_d, T, o, workspace, ws_bytes, true, stream);
     if (rc) return rc;
     DTP_CUDA_CHECK(cudaMemcpyAsync(logits_host, logit_d, (size_t)T * cfg->n_vocab * 4,
                                    cudaMemcpyDeviceToHost, s));

@@ -213,6 +213,12 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         dst[(size_t)j * ea.ldvt] = __float2bfloat16_rn(f32(r[j]));
+                    if (ea.v_rows) {            // token-major copy (a decode KV cache)
+                        float y[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) y[j] = f32(r[j]);
+                        store_row32(ea.v_rows + (size_t)grow * nk + vcol + c, y);
+                    }
                 }
             }
         }

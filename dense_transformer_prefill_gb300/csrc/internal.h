@@ -78,6 +78,9 @@ cudaError_t launch_transpose_v(const __nv_bfloat16* v, __nv_bfloat16* vt, int T,
 cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_bf16,
                                int mode, cudaStream_t s);
 cudaError_t launch_copy_f32(const float* src, float* dst, size_t n, cudaStream_t s);
+// dst[r, 0:cols] = src[r, 0:cols] for r < rows (float32, row strides lds / ldd)
+cudaError_t launch_copy_rows_f32(const float* src, int lds, float* dst, int ldd, int rows,
+                                 int cols, cudaStream_t s);
 
 // ----------------------------------------------------------------------------- tcgen05 GEMM
 enum GemmEpi {
@@ -97,6 +100,7 @@ struct GemmEpiArgs {
     __nv_bfloat16* k = nullptr;         // [M, n_head_kv*hd]
     __nv_bfloat16* vt = nullptr;        // [n_head_kv*hd, ldvt]
     long long ldvt = 0;
+    __nv_bfloat16* v_rows = nullptr;    // optional token-major v [M, n_head_kv*hd]
     const float* q_norm = nullptr;
     const float* k_norm = nullptr;
     const float2* rope = nullptr;       // [M, rope_dims/2] (cos, sin)

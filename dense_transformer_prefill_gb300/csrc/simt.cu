@@ -553,4 +553,23 @@ cudaError_t launch_copy_f32(const float* src, float* dst, size_t n, cudaStream_t
     return cudaGetLastError();
 }
 
+__global__ void copy_rows_f32_kernel(const float* __restrict__ a, int lda, float* __restrict__ b,
+                                     int ldb, int rows, int cols) {
+    const size_t n = (size_t)rows * cols;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / cols, c = i % cols;
+        b[r * ldb + c] = a[r * lda + c];
+    }
+}
+
+cudaError_t launch_copy_rows_f32(const float* src, int lds, float* dst, int ldd, int rows,
+                                 int cols, cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    size_t n = (size_t)rows * cols, blocks = (n + 255) / 256;
+    if (blocks > 65535 * 8) blocks = 65535 * 8;
+    copy_rows_f32_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, lds, dst, ldd, rows, cols);
+    return cudaGetLastError();
+}
+
 }  // namespace dtp

@@ -140,6 +140,26 @@ int dtp_fwd_prefill(const dtp_config* cfg, const void* packed, size_t packed_byt
                     const uint32_t* tokens, int T, float* logits, float* hidden, void* workspace,
                     size_t ws_bytes, dtp_stream_t stream);
 
+/* Outputs of dtp_fwd_prefill_ex; every pointer may be NULL (at least one given). */
+typedef struct dtp_fwd_outputs {
+    float* logits;   /* device float32 [T, n_vocab], or [1, n_vocab] with last_only;
+                        NULL skips the output norm and the lm_head                        */
+    int last_only;   /* nonzero: logits of position T-1 only (forward.rs `forward_last`) */
+    float* hidden;   /* device float32 [n_layer + 1, T, n_embd], as in dtp_fwd_prefill      */
+    void* k_cache;   /* device [n_layer, T, n_head_kv*head_dim]: every layer's keys after
+                        QK-norm and RoPE (what attention consumed), token-major; bf16 under
+                        DTP_PREC_BF16, float32 under DTP_PREC_F32 -- a decode KV cache     */
+    void* v_cache;   /* device [n_layer, T, n_head_kv*head_dim]: every layer's values, same
+                        dtype and layout as k_cache                                         */
+} dtp_fwd_outputs;
+
+/* dtp_fwd_prefill with a choice of outputs: last-position logits only
+ * (forward.rs `forward_last`), and/or the per-layer K/V a decode step continues
+ * from.  Same workspace as dtp_fwd_prefill. */
+int dtp_fwd_prefill_ex(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                       const uint32_t* tokens, int T, const dtp_fwd_outputs* out, void* workspace,
+                       size_t ws_bytes, dtp_stream_t stream);
+
 /* Bytes of device workspace dtp_fwd_prefill_host needs (the forward workspace
  * plus device staging for the tokens and logits). */
 size_t dtp_workspace_size_host(const dtp_config* cfg, int T);

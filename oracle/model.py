@@ -152,9 +152,10 @@ def _mats(w: dict, bf16: bool) -> dict:
     return out
 
 
-def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False) -> np.ndarray:
+def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=None) -> np.ndarray:
     """One decoder layer, forward.rs `Model::forward` loop body, on the residual
-    stream x [T, n_embd]; returns the new x."""
+    stream x [T, n_embd]; returns the new x.  If `kv_out` is a list, the layer's
+    attention inputs (k after QK-norm and RoPE, and v) are appended to it."""
     op = round_bf16 if bf16_operands else (lambda a: a)
     L = _mats(lw, bf16_operands)
     d, h, g, hd = cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim
@@ -170,6 +171,8 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False) -> np.ndar
     q = op(rope_neox(q, pos, h, hd, cfg.rope_dim_count, cfg.rope_freq_base))
     k = op(rope_neox(k, pos, g, hd, cfg.rope_dim_count, cfg.rope_freq_base))
     v = op(v)
+    if kv_out is not None:
+        kv_out.append((k, v))
     attn = op(sdpa_causal_gqa(q, k, v, h, g, hd, scale))
     x1 = x + linear(attn, L["wo"])
     # ffn block (dense SwiGLU)
@@ -179,12 +182,13 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False) -> np.ndar
 
 
 def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidden: bool = False,
-            layer_source=None):
+            layer_source=None, kv_out=None):
     """forward.rs `Model::forward`: logits [T, n_vocab] for `tokens`, positions 0..T-1.
 
     weights: {"tok_embd" [V,d], "layers": [dict per layer], "output_norm" [d],
     "output" [V,d]}.  `layer_source(l)` may replace weights["layers"][l] (lets a
-    caller stream layers of a large model).  With return_hidden, also returns
+    caller stream layers of a large model).  `kv_out` (a list) collects every
+    layer's (k, v) as in forward_layer.  With return_hidden, also returns
     hidden [n_layer+1, T, d]: the residual stream entering each layer, then the
     stream entering output_norm."""
     tokens = np.asarray(tokens, dtype=np.int64)
@@ -200,7 +204,7 @@ def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidd
     hidden = [x.copy()] if return_hidden else None
     for l in range(cfg.n_layer):
         lw = layer_source(l) if layer_source is not None else weights["layers"][l]
-        x = forward_layer(cfg, lw, x, pos, bf16_operands)
+        x = forward_layer(cfg, lw, x, pos, bf16_operands, kv_out)
         if return_hidden:
             hidden.append(x.copy())
     hn = op(rms_norm(x, np.asarray(weights["output_norm"], dtype=F64), cfg.rms_eps))

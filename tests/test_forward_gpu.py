@@ -167,3 +167,47 @@ def test_qwen3_8b_shape_prefix_rows(dtp):
     gl = logits[:R].cpu().numpy()
     sub = cfg.replace(T=R)
     assert_parity(sub, gl, gh, ref_logits, np.stack(ref_hidden))
+
+
+@pytest.mark.parametrize("prec", ["f32", "bf16"])
+def test_forward_last_and_kv_cache(dtp, prec):
+    """dtp_fwd_prefill_ex: last-position logits (forward.rs `forward_last`) and the
+    per-layer K (after QK-norm + RoPE) / V a decode step continues from."""
+    cfg = synth.CONFIGS["small"].replace(precision=prec)
+    m = load_model(dtp, cfg)
+    T, L, nk = cfg.T, cfg.n_layer, cfg.n_head_kv * cfg.head_dim
+    toks = torch.as_tensor(synth.tokens(cfg).astype(np.int32), device=dev)
+    full = m.forward(toks)
+    cdt = torch.float32 if prec == "f32" else torch.bfloat16
+    last = torch.empty((1, cfg.n_vocab), dtype=torch.float32, device=dev)
+    kc = torch.empty((L, T, nk), dtype=cdt, device=dev)
+    vc = torch.empty((L, T, nk), dtype=cdt, device=dev)
+    dtp.fwd_prefill_ex(m.c, m.packed, toks, m.workspace(T), logits=last, last_only=True,
+                       k_cache=kc, v_cache=vc)
+    torch.cuda.synchronize()
+    dtp.check()
+    # the last-row lm_head is the same kernel arithmetic on the same row
+    np.testing.assert_allclose(last.cpu().numpy()[0], full.cpu().numpy()[-1], rtol=0, atol=1e-6)
+    w = synth.model_weights(cfg)
+    kv = []
+    ref = oracle.forward(cfg, w, synth.tokens(cfg), bf16_operands=(prec == "bf16"), kv_out=kv)
+    got_k, got_v = kc.float().cpu().numpy(), vc.float().cpu().numpy()
+    u = 2.0 ** -8
+    for l, (rk, rv) in enumerate(kv):
+        if prec == "f32":
+            assert rel_l2(got_k[l], rk) <= 1e-5 and rel_l2(got_v[l], rv) <= 1e-5, l
+        elif l == 0:
+            # same layer input on both sides; the only differences are bf16 rounding
+            # flips of the normed GEMM input h (each shifts a whole row of k/v by
+            # ~|W| * ulp(h)) and of k/v themselves: within one bf16 ulp in rel L2
+            assert rel_l2(got_k[0], rk) <= u and rel_l2(got_v[0], rv) <= u
+        else:             # the layer input carries the drift bounded in assert_parity
+            assert rel_l2(got_k[l], rk) <= 2 * u * np.sqrt(l) + u, l
+            assert rel_l2(got_v[l], rv) <= 2 * u * np.sqrt(l) + u, l
+    tol = 1e-5 if prec == "f32" else 2 * u * np.sqrt(L + 1) + u
+    assert rel_l2(last.cpu().numpy()[0], ref[-1]) <= tol
+    # logits-free call: KV only
+    kc2 = torch.zeros_like(kc)
+    dtp.fwd_prefill_ex(m.c, m.packed, toks, m.workspace(T), k_cache=kc2)
+    torch.cuda.synchronize()
+    assert torch.equal(kc2, kc)
