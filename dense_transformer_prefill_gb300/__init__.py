@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     fwd_prefill,
     fwd_prefill_ex,
     fwd_prefill_host,
+    fwd_prefill_varlen,
     gate_up_swiglu,
     last_error,
     launch_count,
@@ -39,4 +40,5 @@ from ._binding import (  # noqa: F401
     timer_read,
     workspace_size,
     workspace_size_host,
+    workspace_size_varlen,
 )

@@ -59,6 +59,10 @@ _SIGS = {
                          c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "dtp_fwd_prefill_ex": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int,
                             ctypes.POINTER(FwdOutputs), c_void_p, c_size_t, c_void_p], c_int),
+    "dtp_workspace_size_varlen": ([ctypes.POINTER(Config), c_int, c_int], c_size_t),
+    "dtp_fwd_prefill_varlen": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_void_p, c_int,
+                                c_int, ctypes.POINTER(FwdOutputs), c_void_p, c_size_t, c_void_p],
+                               c_int),
     "dtp_fwd_prefill_host": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int,
                               c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "dtp_check": ([c_void_p], c_int),
@@ -182,6 +186,23 @@ def fwd_prefill_ex(c: Config, packed: torch.Tensor, tokens: torch.Tensor, worksp
                                  packed.numel() * packed.element_size(), tokens.data_ptr(),
                                  tokens.numel(), ctypes.byref(o), workspace.data_ptr(),
                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def workspace_size_varlen(c: Config, total: int, n_seq: int) -> int:
+    return lib().dtp_workspace_size_varlen(ctypes.byref(c), total, n_seq)
+
+
+def fwd_prefill_varlen(c: Config, packed: torch.Tensor, tokens: torch.Tensor,
+                       cu_seqlens: torch.Tensor, workspace: torch.Tensor, logits=None,
+                       last_only: bool = False, hidden=None, k_cache=None, v_cache=None,
+                       stream=None) -> None:
+    assert cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous()
+    o = FwdOutputs(_ptr(logits), 1 if last_only else 0, _ptr(hidden), _ptr(k_cache), _ptr(v_cache))
+    _ok(lib().dtp_fwd_prefill_varlen(ctypes.byref(c), packed.data_ptr(),
+                                     packed.numel() * packed.element_size(), tokens.data_ptr(),
+                                     cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, tokens.numel(),
+                                     ctypes.byref(o), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def fwd_prefill_host(c: Config, packed: torch.Tensor, tokens_host: torch.Tensor,
@@ -312,6 +333,15 @@ class Model:
         key = (T, host)
         if key not in self._ws:
             n = (workspace_size_host if host else workspace_size)(self.c, T)
+            if n == 0:
+                raise DtpError(-1, last_error())
+            self._ws[key] = torch.empty(n, dtype=torch.uint8, device=self.device)
+        return self._ws[key]
+
+    def workspace_varlen(self, total: int, n_seq: int) -> torch.Tensor:
+        key = ("varlen", total, n_seq)
+        if key not in self._ws:
+            n = workspace_size_varlen(self.c, total, n_seq)
             if n == 0:
                 raise DtpError(-1, last_error())
             self._ws[key] = torch.empty(n, dtype=torch.uint8, device=self.device)

@@ -65,10 +65,15 @@ struct ACfg {
 };
 
 struct AParams {
-    int T, n_head, n_head_kv, n_qt;
+    int T, n_head, n_head_kv, n_qt;   // n_qt: query tiles in the schedule (an upper bound for varlen)
     float scale_log2;
     __nv_bfloat16* out;
     int ldo;
+    // several sequences packed along the token axis (n_seq == 0: one sequence of T tokens)
+    int n_seq;
+    const int* cu_seqlens;   // [n_seq + 1] token offsets
+    const int* tile_start;   // [n_seq + 1] prefix of ceil(len / 128)
+    const int* vcol_start;   // [n_seq] first v^T column of each sequence (multiple of 8)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -145,10 +150,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.n_head / p.n_head_kv, pairs = G / 2;
     const int items_per_qt = p.n_head_kv * pairs;
-    const int qt = p.n_qt - 1 - (int)blockIdx.x / items_per_qt;
+    const int tile_idx = p.n_qt - 1 - (int)blockIdx.x / items_per_qt;   // longest tiles first
     const int rem = (int)blockIdx.x % items_per_qt;
     const int g = rem / pairs;
     const int h0 = g * G + 2 * (rem % pairs);
+    int qt = tile_idx, seq_start = 0, seq_len = p.T, vstart = 0;
+    if (p.n_seq > 0) {
+        if (tile_idx >= p.tile_start[p.n_seq]) return;      // beyond the schedule: whole CTA
+        int lo = 0, hi = p.n_seq - 1;                        // last b with tile_start[b] <= tile_idx
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.tile_start[mid] <= tile_idx) lo = mid;
+            else hi = mid - 1;
+        }
+        qt = tile_idx - p.tile_start[lo];
+        seq_start = p.cu_seqlens[lo];
+        seq_len = p.cu_seqlens[lo + 1] - seq_start;
+        vstart = p.vcol_start[lo];
+    }
     const int n_kv = qt + 1;
 
     if (threadIdx.x == 0) {
@@ -185,14 +204,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 2; ++i)
                 for (int a = 0; a < HD / 64; ++a)
                     ptx::tma_load_2d(&tmQ, q_full, sQ + i * C::Q_BYTES + a * BQ * 128,
-                                     (h0 + i) * HD + a * 64, qt * BQ);
+                                     (h0 + i) * HD + a * 64, seq_start + qt * BQ);
             int k_issued = 0, v_issued[2] = {0, 0};
             for (int j = 0; j < n_kv; ++j) {
                 if (!ptx::wait_bounded(k_empty, (j & 1) ^ 1, abort_flag, &g_attn_err, ERRBIT_TIMEOUT))
                     break;
                 ptx::mbar_arrive_expect_tx(k_full, C::K_BYTES);
                 for (int a = 0; a < HD / 64; ++a)
-                    ptx::tma_load_2d(&tmK, k_full, sK + a * BKV * 128, g * HD + a * 64, j * BKV);
+                    ptx::tma_load_2d(&tmK, k_full, sK + a * BKV * 128, g * HD + a * 64,
+                                     seq_start + j * BKV);
                 ++k_issued;
                 const int vs = j & 1;
                 if (!ptx::wait_bounded(&v_empty[vs], ((j >> 1) & 1) ^ 1, abort_flag, &g_attn_err,
@@ -201,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive_expect_tx(&v_full[vs], C::V_BYTES);
                 for (int a = 0; a < BKV / 64; ++a)
                     ptx::tma_load_2d(&tmV, &v_full[vs], sV + vs * C::V_BYTES + a * HD * 128,
-                                     j * BKV + a * 64, g * HD);
+                                     vstart + j * BKV + a * 64, g * HD);
                 ++v_issued[vs];
             }
             if (*abort_flag) {
@@ -291,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = (warp - 2) / 4;            // which head of the pair
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        const int qrow = qt * BQ + row;
+        const int qrel = qt * BQ + row;                      // position within the sequence
+        const int qrow = seq_start + qrel;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem_base + lane_off + C::S_COL0 + i * BKV;
         const uint32_t tO = tmem_base + lane_off + C::O_COL0 + i * HD;
@@ -374,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[32];
                     __syncwarp();
                     ptx::tmem_ld32(tO + c, r);
-                    if (qrow < p.T) {
+                    if (qrel < seq_len && qrow < p.T) {
 #pragma unroll
                         for (int t = 0; t < 32; t += 8) {
                             uint4 u;
@@ -425,6 +446,16 @@ cudaError_t launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
 cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                            const __nv_bfloat16* vt, long long ldvt, __nv_bfloat16* out, int T,
                            int n_head, int n_head_kv, int head_dim, float scale, cudaStream_t s) {
+    AttnVarlen none;
+    return launch_attn_tc_varlen(q, k, vt, ldvt, T, out, T, n_head, n_head_kv, head_dim, scale,
+                                 none, s);
+}
+
+cudaError_t launch_attn_tc_varlen(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                  const __nv_bfloat16* vt, long long ldvt, long long vt_cols,
+                                  __nv_bfloat16* out, int T, int n_head, int n_head_kv,
+                                  int head_dim, float scale, const AttnVarlen& vl,
+                                  cudaStream_t s) {
     if (!attn_tc_supported(n_head, n_head_kv, head_dim)) return cudaErrorNotSupported;
     CUtensorMap tq, tk, tv;
     const int hd = head_dim;
@@ -432,17 +463,21 @@ cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                       (uint64_t)n_head * hd, BQ, 64) ||
         !make_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, (uint64_t)n_head_kv * hd,
                       (uint64_t)n_head_kv * hd, BKV, 64) ||
-        !make_tmap_2d(&tv, vt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)n_head_kv * hd, T,
-                      (uint64_t)ldvt, hd, 64))
+        !make_tmap_2d(&tv, vt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)n_head_kv * hd,
+                      (uint64_t)vt_cols, (uint64_t)ldvt, hd, 64))
         return cudaErrorInvalidValue;
     AParams p;
     p.T = T;
     p.n_head = n_head;
     p.n_head_kv = n_head_kv;
-    p.n_qt = (T + BQ - 1) / BQ;
+    p.n_qt = vl.n_seq > 0 ? (T + BQ - 1) / BQ + vl.n_seq : (T + BQ - 1) / BQ;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out = out;
     p.ldo = n_head * hd;
+    p.n_seq = vl.n_seq;
+    p.cu_seqlens = vl.cu_seqlens;
+    p.tile_start = vl.tile_start;
+    p.vcol_start = vl.vcol_start;
     LaunchScope ls(DTP_K_ATTN, s);
     if (hd == 128) return launch_hd<128>(tq, tk, tv, p, s);
     return launch_hd<64>(tq, tk, tv, p, s);

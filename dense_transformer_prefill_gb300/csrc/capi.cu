@@ -180,10 +180,13 @@ struct Workspace {
     size_t q, k, vt, rope;                       // bf16 path
     long long ldvt;
     size_t tokens, logits;                       // _host staging
+    size_t tile_start, vcol_start, last_row, tok_pos, tok_vcol;   // packed sequences
     size_t total;
 };
 
-static Workspace workspace_layout(const dtp_config* c, int T, bool host) {
+// Workspace for T tokens; n_seq > 0 adds the packed-sequence schedule and pads
+// each sequence's v^T block to a multiple of 8 columns.
+static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_seq = 0) {
     Workspace W = {};
     const size_t d = c->n_embd, hd = c->head_dim, nq = (size_t)c->n_head * hd,
                  nk = (size_t)c->n_head_kv * hd, F = c->n_ff;
@@ -200,7 +203,7 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host) {
     W.attn = take((size_t)T * nq * e);
     W.act = take((size_t)T * F * e);
     if (bf) {
-        W.ldvt = (long long)align_up(T, 8);
+        W.ldvt = (long long)align_up((size_t)T + (n_seq > 0 ? 7 * (size_t)n_seq : 0), 8);
         W.q = take((size_t)T * nq * 2);
         W.k = take((size_t)T * nk * 2);
         W.vt = take(nk * (size_t)W.ldvt * 2);
@@ -213,8 +216,39 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host) {
         W.tokens = take((size_t)T * 4);
         W.logits = take((size_t)T * c->n_vocab * 4);
     }
+    if (n_seq > 0) {
+        W.tile_start = take(((size_t)n_seq + 2) * 4);
+        W.vcol_start = take((size_t)n_seq * 4);
+        W.last_row = take((size_t)n_seq * 4);
+        W.tok_pos = take((size_t)T * 4);
+        W.tok_vcol = take((size_t)T * 4);
+    }
     W.total = o;
     return W;
+}
+
+// Packed-sequence context of one forward call (n_seq == 0: a single sequence).
+struct VarlenCtx {
+    int n_seq = 0;
+    const int* cu = nullptr;
+    int* tile_start = nullptr;
+    int* vcol_start = nullptr;
+    int* last_row = nullptr;
+    int* tok_pos = nullptr;
+    int* tok_vcol = nullptr;
+};
+
+static VarlenCtx varlen_ctx(const Workspace& W, uint8_t* ws, int n_seq, const int* cu) {
+    VarlenCtx V;
+    if (n_seq <= 0) return V;
+    V.n_seq = n_seq;
+    V.cu = cu;
+    V.tile_start = (int*)(ws + W.tile_start);
+    V.vcol_start = (int*)(ws + W.vcol_start);
+    V.last_row = (int*)(ws + W.last_row);
+    V.tok_pos = (int*)(ws + W.tok_pos);
+    V.tok_vcol = (int*)(ws + W.tok_vcol);
+    return V;
 }
 
 static bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
@@ -222,7 +256,7 @@ static bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t
 // ----------------------------------------------------------------------------- forward
 static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
                    const uint32_t* tokens, int T, const dtp_fwd_outputs& o, uint8_t* ws,
-                   const Workspace& W, cudaStream_t s) {
+                   const Workspace& W, const VarlenCtx& V, cudaStream_t s) {
     float* logits = o.logits;
     float* hidden = o.hidden;
     const int d = c->n_embd, hd = c->head_dim, h = c->n_head, g = c->n_head_kv, F = c->n_ff;
@@ -234,6 +268,9 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
     float* gu = (float*)(ws + W.gu);
     float* act = (float*)(ws + W.act);
     const float scale = 1.0f / sqrtf((float)hd);
+    if (V.n_seq)
+        DTP_CUDA_CHECK(launch_seq_meta(V.cu, V.n_seq, T, V.tile_start, V.vcol_start, V.last_row,
+                                       V.tok_pos, V.tok_vcol, T, s));
     DTP_CUDA_CHECK(launch_embed(tokens, T, c->n_vocab, d, P + L.tok_embd, DTP_F32, x, s));
     for (int l = 0; l < c->n_layer; ++l) {
         const uint8_t* lp = P + (size_t)l * L.layer_bytes;
@@ -244,10 +281,10 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
         DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(lp + L.w_qkv), qkv, DTP_F32, nqkv,
                                         T, nqkv, d, nullptr, s, DTP_K_GEMM_QKV));
         DTP_CUDA_CHECK(launch_qk_norm_rope(qkv, DTP_F32, nqkv, (const float*)(lp + L.q_norm),
-                                           nullptr, T, h, hd, c->rope_dim_count,
+                                           V.tok_pos, T, h, hd, c->rope_dim_count,
                                            c->rope_freq_base, c->rms_eps, s));
         DTP_CUDA_CHECK(launch_qk_norm_rope(qkv + nq, DTP_F32, nqkv, (const float*)(lp + L.k_norm),
-                                           nullptr, T, g, hd, c->rope_dim_count,
+                                           V.tok_pos, T, g, hd, c->rope_dim_count,
                                            c->rope_freq_base, c->rms_eps, s));
         if (o.k_cache)
             DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nq, nqkv, (float*)o.k_cache + (size_t)l * T * nk,
@@ -256,7 +293,7 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
             DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nq + nk, nqkv,
                                                 (float*)o.v_cache + (size_t)l * T * nk, nk, T, nk, s));
         DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, qkv + nq, nqkv, qkv + nq + nk, nqkv, 0, attn,
-                                        nq, DTP_F32, T, h, g, hd, scale, s));
+                                        nq, DTP_F32, T, h, g, hd, scale, s, V.tok_pos));
         DTP_CUDA_CHECK(launch_gemm_simt(attn, nq, (const float*)(lp + L.wo), x, DTP_F32, d, T, d,
                                         nq, x, s, DTP_K_GEMM_O));
         DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.ffn_norm), hb, DTP_F32, T, d,
@@ -271,6 +308,14 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
         DTP_CUDA_CHECK(
             launch_copy_f32(x, hidden + (size_t)c->n_layer * T * d, (size_t)T * d, s));
     if (!logits) return DTP_OK;
+    if (o.last_only && V.n_seq) {            // the last position of every sequence
+        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(P + L.output_norm), hb, DTP_F32, V.n_seq,
+                                      d, c->rms_eps, s, V.last_row));
+        DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(P + L.output), logits, DTP_F32,
+                                        c->n_vocab, V.n_seq, c->n_vocab, d, nullptr, s,
+                                        DTP_K_GEMM_LMHEAD));
+        return DTP_OK;
+    }
     const int rows = o.last_only ? 1 : T;
     const float* xf = x + (size_t)(T - rows) * d;
     DTP_CUDA_CHECK(launch_rmsnorm(xf, (const float*)(P + L.output_norm), hb, DTP_F32, rows, d,
@@ -282,7 +327,7 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
 
 static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
                     const uint32_t* tokens, int T, const dtp_fwd_outputs& o, uint8_t* ws,
-                    const Workspace& W, cudaStream_t s) {
+                    const Workspace& W, const VarlenCtx& V, cudaStream_t s) {
     float* logits = o.logits;
     float* hidden = o.hidden;
     typedef __nv_bfloat16 bf;
@@ -298,6 +343,20 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
     float2* rope = (float2*)(ws + W.rope);
     const float scale = 1.0f / sqrtf((float)hd);
     const bool fa = attn_tc_supported(h, g, hd);
+    // packed sequences: v^T blocks start on 8-column boundaries; the padding
+    // columns between them are read by attention (with P = 0), so they are zeroed
+    long long vt_cols = T;
+    AttnVarlen vl;
+    if (V.n_seq) {
+        vt_cols = W.ldvt;
+        DTP_CUDA_CHECK(cudaMemsetAsync(vt, 0, (size_t)nk * W.ldvt * 2, s));
+        DTP_CUDA_CHECK(launch_seq_meta(V.cu, V.n_seq, T, V.tile_start, V.vcol_start, V.last_row,
+                                       V.tok_pos, V.tok_vcol, vt_cols, s));
+        vl.n_seq = V.n_seq;
+        vl.cu_seqlens = V.cu;
+        vl.tile_start = V.tile_start;
+        vl.vcol_start = V.vcol_start;
+    }
     DTP_CUDA_CHECK(launch_rope_table(rope, T, c->rope_dim_count, c->rope_freq_base, s));
     DTP_CUDA_CHECK(launch_embed(tokens, T, c->n_vocab, d, P + L.tok_embd, DTP_BF16, x, s));
     for (int l = 0; l < c->n_layer; ++l) {
@@ -314,6 +373,8 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         e.vt = vt;
         e.ldvt = W.ldvt;
         e.v_rows = o.v_cache ? (bf*)o.v_cache + (size_t)l * T * nk : nullptr;
+        e.tok_pos = V.tok_pos;
+        e.tok_vcol = V.tok_vcol;
         e.q_norm = (const float*)(lp + L.q_norm);
         e.k_norm = (const float*)(lp + L.k_norm);
         e.rope = rope;
@@ -325,10 +386,11 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(lp + L.w_qkv), T, nqkv, d, EPI_QKV, e, s,
                                       DTP_K_GEMM_QKV));
         if (fa)
-            DTP_CUDA_CHECK(launch_attn_tc(q, kl, vt, W.ldvt, attn, T, h, g, hd, scale, s));
+            DTP_CUDA_CHECK(launch_attn_tc_varlen(q, kl, vt, W.ldvt, vt_cols, attn, T, h, g, hd,
+                                                 scale, vl, s));
         else
-            DTP_CUDA_CHECK(launch_attn_simt(q, nq, kl, nk, vt, (int)W.ldvt, 1, attn, nq, DTP_BF16,
-                                            T, h, g, hd, scale, s));
+            return fail(DTP_ERR_UNSUPPORTED,
+                        "bf16 path: attention needs an even n_head/n_head_kv group");
         GemmEpiArgs eo;
         eo.y = x;
         eo.y_dtype = DTP_F32;
@@ -349,10 +411,17 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         DTP_CUDA_CHECK(
             launch_copy_f32(x, hidden + (size_t)c->n_layer * T * d, (size_t)T * d, s));
     if (!logits) return DTP_OK;
-    // forward.rs `forward_last`: only the last position's logits
-    const int rows = o.last_only ? 1 : T;
-    DTP_CUDA_CHECK(launch_rmsnorm(x + (size_t)(T - rows) * d, (const float*)(P + L.output_norm), hb,
-                                  DTP_BF16, rows, d, c->rms_eps, s));
+    // forward.rs `forward_last`: only the last position's logits (of every sequence)
+    int rows = o.last_only ? 1 : T;
+    if (o.last_only && V.n_seq) {
+        rows = V.n_seq;
+        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(P + L.output_norm), hb, DTP_BF16, rows, d,
+                                      c->rms_eps, s, V.last_row));
+    } else {
+        DTP_CUDA_CHECK(launch_rmsnorm(x + (size_t)(T - rows) * d,
+                                      (const float*)(P + L.output_norm), hb, DTP_BF16, rows, d,
+                                      c->rms_eps, s));
+    }
     GemmEpiArgs el;
     el.y = logits;
     el.y_dtype = DTP_F32;
@@ -447,7 +516,8 @@ size_t dtp_workspace_size_host(const dtp_config* cfg, int T) {
 
 static int fwd_checked(const dtp_config* cfg, const void* packed, size_t packed_bytes,
                        const uint32_t* tokens, int T, const dtp_fwd_outputs& out,
-                       void* workspace, size_t ws_bytes, bool host_layout, dtp_stream_t stream) {
+                       void* workspace, size_t ws_bytes, bool host_layout, dtp_stream_t stream,
+                       int n_seq = 0, const int* cu_seqlens = nullptr) {
     float* logits = out.logits;
     float* hidden = out.hidden;
     int rc = validate_config(cfg);
@@ -460,9 +530,12 @@ static int fwd_checked(const dtp_config* cfg, const void* packed, size_t packed_
     PackedLayout L = packed_layout(cfg);
     if (packed_bytes < L.total)
         return fail(DTP_ERR_WORKSPACE, "packed buffer %zu < %zu bytes", packed_bytes, L.total);
-    Workspace W = workspace_layout(cfg, T, host_layout);
+    Workspace W = workspace_layout(cfg, T, host_layout, n_seq);
     if (ws_bytes < W.total)
         return fail(DTP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, W.total);
+    if (cfg->precision == DTP_PREC_BF16 && !attn_tc_supported(cfg->n_head, cfg->n_head_kv,
+                                                              cfg->head_dim))
+        return fail(DTP_ERR_UNSUPPORTED, "bf16 path: n_head / n_head_kv must be even");
     if (!aligned(workspace, 256) || !aligned(packed, 256) || (logits && !aligned(logits, 16)) ||
         (hidden && !aligned(hidden, 16)) || (out.k_cache && !aligned(out.k_cache, 16)) ||
         (out.v_cache && !aligned(out.v_cache, 16)))
@@ -471,9 +544,11 @@ static int fwd_checked(const dtp_config* cfg, const void* packed, size_t packed_
     if (cfg->precision == DTP_PREC_BF16 && (cfg->n_vocab % 4))
         return fail(DTP_ERR_UNSUPPORTED, "bf16 path: n_vocab must be a multiple of 4");
     cudaStream_t s = (cudaStream_t)stream;
+    const VarlenCtx V = varlen_ctx(W, (uint8_t*)workspace, n_seq, cu_seqlens);
     if (cfg->precision == DTP_PREC_BF16)
-        return fwd_bf16(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, s);
-    return fwd_f32(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, s);
+        return fwd_bf16(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, V,
+                        s);
+    return fwd_f32(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, V, s);
 }
 
 int dtp_fwd_prefill(const dtp_config* cfg, const void* packed, size_t packed_bytes,
@@ -492,6 +567,23 @@ int dtp_fwd_prefill_ex(const dtp_config* cfg, const void* packed, size_t packed_
     if (!out) return fail(DTP_ERR_INVALID_ARG, "NULL outputs");
     return fwd_checked(cfg, packed, packed_bytes, tokens, T, *out, workspace, ws_bytes, false,
                        stream);
+}
+
+size_t dtp_workspace_size_varlen(const dtp_config* cfg, int total, int n_seq) {
+    if (validate_config(cfg) != DTP_OK || total <= 0 || n_seq <= 0) return 0;
+    return workspace_layout(cfg, total, false, n_seq).total;
+}
+
+int dtp_fwd_prefill_varlen(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                           const uint32_t* tokens, const int32_t* cu_seqlens, int n_seq, int total,
+                           const dtp_fwd_outputs* out, void* workspace, size_t ws_bytes,
+                           dtp_stream_t stream) {
+    if (!out) return fail(DTP_ERR_INVALID_ARG, "NULL outputs");
+    if (!cu_seqlens || n_seq <= 0)
+        return fail(DTP_ERR_INVALID_ARG, "cu_seqlens must be given with n_seq >= 1");
+    if (n_seq > (1 << 20)) return fail(DTP_ERR_UNSUPPORTED, "n_seq > 2^20");
+    return fwd_checked(cfg, packed, packed_bytes, tokens, total, *out, workspace, ws_bytes, false,
+                       stream, n_seq, cu_seqlens);
 }
 
 int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packed_bytes,
@@ -530,6 +622,10 @@ int dtp_check(dtp_stream_t stream) {
     unsigned bits = read_clear_simt_errors() | read_clear_gemm_errors() | read_clear_attn_errors();
     if (bits & ERRBIT_TIMEOUT)
         return fail(DTP_ERR_DEVICE_TIMEOUT, "a kernel's bounded pipeline wait gave up");
+    if (bits & ERRBIT_SEQLENS)
+        return fail(DTP_ERR_INVALID_ARG,
+                    "cu_seqlens was not 0 = cu[0] <= cu[1] <= ... <= cu[n_seq] = total (no "
+                    "attention was computed)");
     if (bits & ERRBIT_TOKEN_RANGE)
         return fail(DTP_ERR_TOKEN_RANGE, "a token id was >= n_vocab (its row was zeroed)");
     return DTP_OK;

@@ -175,7 +175,8 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
                 ptx::tmem_ld32(th + i0, ra);
                 ptx::tmem_ld32(th + half + i0, rb);
                 if (live) {
-                    const float2* cs = ea.rope + (size_t)grow * half + i0;
+                    const int pos = ea.tok_pos ? ea.tok_pos[grow] : grow;
+                    const float2* cs = ea.rope + (size_t)pos * half + i0;
                     float ya[32], yb[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -209,7 +210,8 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
                 __syncwarp();
                 ptx::tmem_ld32(th + c, r);
                 if (live) {
-                    __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + grow;
+                    const int tcol = ea.tok_vcol ? ea.tok_vcol[grow] : grow;
+                    __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         dst[(size_t)j * ea.ldvt] = __float2bfloat16_rn(f32(r[j]));

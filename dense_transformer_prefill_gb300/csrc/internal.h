@@ -23,7 +23,7 @@ void clear_error();
     } while (0)
 
 // Device error word bits (each kernel family keeps its own word).
-enum : unsigned { ERRBIT_TOKEN_RANGE = 1u, ERRBIT_TIMEOUT = 2u };
+enum : unsigned { ERRBIT_TOKEN_RANGE = 1u, ERRBIT_TIMEOUT = 2u, ERRBIT_SEQLENS = 4u };
 
 // Read and clear the error words of every kernel family on the current device.
 unsigned read_clear_simt_errors();
@@ -54,7 +54,7 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
 cudaError_t launch_embed(const uint32_t* tokens, int T, int V, int d, const void* table,
                          int table_dtype, float* x, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype, int rows,
-                           int cols, float eps, cudaStream_t s);
+                           int cols, float eps, cudaStream_t s, const int* row_idx = nullptr);
 cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
                                 const int32_t* pos, int T, int n_heads, int head_dim,
                                 int rope_dims, float freq_base, float eps, cudaStream_t s);
@@ -69,10 +69,19 @@ cudaError_t launch_gemm_simt(const float* x, int ldx, const float* W, void* y, i
                              cudaStream_t s, int kind);
 // Causal GQA attention on SIMT cores.  dtype of q/k/v/out: DTP_F32 or DTP_BF16.
 // v_t != 0: v is stored transposed [n_head_kv*head_dim, ldv_t] (key index contiguous).
+// tok_pos (optional): position of each query within its sequence; the keys of
+// query t are then t - tok_pos[t] .. t (sequences packed along the token axis).
 cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, const void* v,
                              int ldv, int v_t, void* out, int ldo, int dtype, int T,
                              int n_head, int n_head_kv, int head_dim, float scale,
-                             cudaStream_t s);
+                             cudaStream_t s, const int* tok_pos = nullptr);
+// Per-sequence schedule for packed sequences: tile_start [n_seq+1] (prefix of
+// ceil(len/128)), vcol_start [n_seq] (prefix of len rounded up to 8),
+// last_row [n_seq] (cu[b+1]-1); then per-token tok_pos / tok_vcol [total].
+// Invalid cu_seqlens raise ERRBIT_SEQLENS and leave an empty, in-bounds schedule.
+cudaError_t launch_seq_meta(const int* cu_seqlens, int n_seq, int total, int* tile_start,
+                            int* vcol_start, int* last_row, int* tok_pos, int* tok_vcol,
+                            long long vt_cols, cudaStream_t s);
 cudaError_t launch_transpose_v(const __nv_bfloat16* v, __nv_bfloat16* vt, int T, int width,
                                int ldt, cudaStream_t s);
 cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_bf16,
@@ -101,6 +110,8 @@ struct GemmEpiArgs {
     __nv_bfloat16* vt = nullptr;        // [n_head_kv*hd, ldvt]
     long long ldvt = 0;
     __nv_bfloat16* v_rows = nullptr;    // optional token-major v [M, n_head_kv*hd]
+    const int* tok_pos = nullptr;       // optional per-row RoPE position (default: the row)
+    const int* tok_vcol = nullptr;      // optional per-row v^T column (default: the row)
     const float* q_norm = nullptr;
     const float* k_norm = nullptr;
     const float2* rope = nullptr;       // [M, rope_dims/2] (cos, sin)
@@ -122,6 +133,18 @@ cudaError_t launch_selftest_wait(cudaStream_t s);
 cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                            const __nv_bfloat16* vt, long long ldvt, __nv_bfloat16* out, int T,
                            int n_head, int n_head_kv, int head_dim, float scale, cudaStream_t s);
+// Several sequences packed along the token axis (see seq_meta in simt.cu).
+struct AttnVarlen {
+    int n_seq = 0;
+    const int* cu_seqlens = nullptr;   // [n_seq + 1]
+    const int* tile_start = nullptr;   // [n_seq + 1]
+    const int* vcol_start = nullptr;   // [n_seq]
+};
+cudaError_t launch_attn_tc_varlen(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                  const __nv_bfloat16* vt, long long ldvt, long long vt_cols,
+                                  __nv_bfloat16* out, int T, int n_head, int n_head_kv,
+                                  int head_dim, float scale, const AttnVarlen& vl,
+                                  cudaStream_t s);
 bool attn_tc_supported(int n_head, int n_head_kv, int head_dim);
 
 }  // namespace dtp

@@ -85,10 +85,11 @@ cudaError_t launch_embed(const uint32_t* tokens, int T, int V, int d, const void
 // forward.rs: `e.rms_norm(x, w, out, ncols, nrows, eps)` -- one block per row.
 template <typename To>
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
-                               To* __restrict__ y, int cols, float eps) {
+                               To* __restrict__ y, int cols, float eps,
+                               const int* __restrict__ row_idx) {
     __shared__ float red[32];
     const size_t r = blockIdx.x;
-    const float* xr = x + r * cols;
+    const float* xr = x + (size_t)(row_idx ? row_idx[r] : r) * cols;
     To* yr = y + r * cols;
     float ss = 0.f;
     const bool vec = (cols & 3) == 0;
@@ -137,10 +138,12 @@ __device__ __forceinline__ void store4(__nv_bfloat16* y, int c, float a, float b
 
 template <typename To>
 __global__ void rmsnorm_reg_kernel(const float* __restrict__ x, const float* __restrict__ w,
-                                   To* __restrict__ y, int cols, float eps) {
+                                   To* __restrict__ y, int cols, float eps,
+                                   const int* __restrict__ row_idx) {
     __shared__ float red[32];
     const size_t r = blockIdx.x;
-    const float4* xr = reinterpret_cast<const float4*>(x + r * cols);
+    const float4* xr =
+        reinterpret_cast<const float4*>(x + (size_t)(row_idx ? row_idx[r] : r) * cols);
     To* yr = y + r * cols;
     const int n4 = cols >> 2;
     float4 v[4];
@@ -167,23 +170,24 @@ __global__ void rmsnorm_reg_kernel(const float* __restrict__ x, const float* __r
 }
 
 cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype, int rows,
-                           int cols, float eps, cudaStream_t s) {
+                           int cols, float eps, cudaStream_t s, const int* row_idx) {
     LaunchScope ls(DTP_K_RMSNORM, s);
     const bool vec_ok = (cols % 4 == 0) && cols <= 16 * 1024;
     if (vec_ok) {
         int threads = ((cols + 15) / 16 + 31) / 32 * 32;     // threads * 16 >= cols
         if (threads < 32) threads = 32;
         if (y_dtype == DTP_BF16)
-            rmsnorm_reg_kernel<<<rows, threads, 0, s>>>(x, w, (__nv_bfloat16*)y, cols, eps);
+            rmsnorm_reg_kernel<<<rows, threads, 0, s>>>(x, w, (__nv_bfloat16*)y, cols, eps,
+                                                        row_idx);
         else
-            rmsnorm_reg_kernel<<<rows, threads, 0, s>>>(x, w, (float*)y, cols, eps);
+            rmsnorm_reg_kernel<<<rows, threads, 0, s>>>(x, w, (float*)y, cols, eps, row_idx);
         return cudaGetLastError();
     }
     int threads = cols >= 1024 ? 256 : (cols >= 256 ? 128 : 32);
     if (y_dtype == DTP_BF16)
-        rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (__nv_bfloat16*)y, cols, eps);
+        rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (__nv_bfloat16*)y, cols, eps, row_idx);
     else
-        rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (float*)y, cols, eps);
+        rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (float*)y, cols, eps, row_idx);
     return cudaGetLastError();
 }
 
@@ -398,7 +402,8 @@ cudaError_t launch_gemm_simt(const float* x, int ldx, const float* W, void* y, i
 template <typename T, bool VT>
 __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __restrict__ k,
                                  int ldk, const T* __restrict__ v, int ldv, T* __restrict__ out,
-                                 int ldo, int Tn, int n_head, int n_head_kv, int hd, float scale) {
+                                 int ldo, int Tn, int n_head, int n_head_kv, int hd, float scale,
+                                 const int* __restrict__ tok_pos) {
     extern __shared__ float sm[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -413,7 +418,8 @@ __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __re
 #pragma unroll
     for (int j = 0; j < MAXD; ++j) acc[j] = 0.f;
     float m = -INFINITY, l = 0.f;
-    for (int s0 = 0; s0 <= t; s0 += 32) {
+    const int k0 = tok_pos ? t - tok_pos[t] : 0;       // first key of this query's sequence
+    for (int s0 = k0; s0 <= t; s0 += 32) {
         const int s = s0 + lane;
         float sc = -INFINITY;
         if (s <= t) {
@@ -456,7 +462,7 @@ __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __re
 cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, const void* v,
                              int ldv, int v_t, void* out, int ldo, int dtype, int T,
                              int n_head, int n_head_kv, int head_dim, float scale,
-                             cudaStream_t s) {
+                             cudaStream_t s, const int* tok_pos) {
     LaunchScope ls(DTP_K_ATTN, s);
     const int warps = 4;
     dim3 grid((T + warps - 1) / warps, n_head);
@@ -466,20 +472,20 @@ cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, con
         if (v_t)
             attn_simt_kernel<B, true><<<grid, warps * 32, smem, s>>>(
                 (const B*)q, ldq, (const B*)k, ldk, (const B*)v, ldv, (B*)out, ldo, T, n_head,
-                n_head_kv, head_dim, scale);
+                n_head_kv, head_dim, scale, tok_pos);
         else
             attn_simt_kernel<B, false><<<grid, warps * 32, smem, s>>>(
                 (const B*)q, ldq, (const B*)k, ldk, (const B*)v, ldv, (B*)out, ldo, T, n_head,
-                n_head_kv, head_dim, scale);
+                n_head_kv, head_dim, scale, tok_pos);
     } else {
         if (v_t)
             attn_simt_kernel<float, true><<<grid, warps * 32, smem, s>>>(
                 (const float*)q, ldq, (const float*)k, ldk, (const float*)v, ldv, (float*)out,
-                ldo, T, n_head, n_head_kv, head_dim, scale);
+                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos);
         else
             attn_simt_kernel<float, false><<<grid, warps * 32, smem, s>>>(
                 (const float*)q, ldq, (const float*)k, ldk, (const float*)v, ldv, (float*)out,
-                ldo, T, n_head, n_head_kv, head_dim, scale);
+                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos);
     }
     return cudaGetLastError();
 }
@@ -550,6 +556,107 @@ cudaError_t launch_copy_f32(const float* src, float* dst, size_t n, cudaStream_t
     size_t blocks = (n + 255) / 256;
     if (blocks > 65535 * 8) blocks = 65535 * 8;
     copy_f32_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, n);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- packed sequences
+// One block: checks cu_seqlens (cu[0] = 0, non-decreasing, cu[n] = total) and
+// writes the exclusive prefixes tile_start (ceil(len/128)) and vcol_start
+// (len rounded up to 8, so every sequence's v^T block starts on a 16-byte
+// boundary), and last_row[b] = cu[b+1] - 1 (clamped to >= 0).  On invalid input
+// it raises ERRBIT_SEQLENS and writes an empty schedule (all zeros).
+__global__ void seq_meta_kernel(const int* __restrict__ cu, int n, int total,
+                                int* __restrict__ tile_start, int* __restrict__ vcol_start,
+                                int* __restrict__ last_row, int* __restrict__ bad_flag) {
+    __shared__ int s_tiles[1024], s_cols[1024];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    if (tid == 0) s_bad = (cu[0] != 0 || cu[n] != total);
+    __syncthreads();
+    const int per = (n + nt - 1) / nt, b0 = tid * per, b1 = min(n, b0 + per);
+    int tiles = 0, cols = 0, bad = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int len = cu[b + 1] - cu[b];
+        if (len < 0) bad = 1;
+        const int L = len < 0 ? 0 : len;
+        tiles += (L + 127) / 128;
+        cols += (L + 7) / 8 * 8;
+    }
+    if (bad) atomicOr(&s_bad, 1);
+    s_tiles[tid] = tiles;
+    s_cols[tid] = cols;
+    __syncthreads();
+    if (tid == 0) {            // exclusive scan of the per-thread sums (nt <= 1024)
+        int a = 0, c = 0;
+        for (int i = 0; i < nt; ++i) {
+            const int ta = s_tiles[i], tc = s_cols[i];
+            s_tiles[i] = a;
+            s_cols[i] = c;
+            a += ta;
+            c += tc;
+        }
+    }
+    __syncthreads();
+    const int badall = s_bad;
+    int a = badall ? 0 : s_tiles[tid], c = badall ? 0 : s_cols[tid];
+    for (int b = b0; b < b1; ++b) {
+        tile_start[b] = a;
+        vcol_start[b] = c;
+        last_row[b] = badall ? 0 : max(cu[b + 1] - 1, 0);
+        if (!badall) {
+            const int L = cu[b + 1] - cu[b];
+            a += (L + 127) / 128;
+            c += (L + 7) / 8 * 8;
+        }
+    }
+    if (b0 < b1 && b1 == n) tile_start[n] = a;      // the thread whose range ends at n
+    if (tid == 0) {
+        *bad_flag = badall;
+        if (badall) {
+            tile_start[n] = 0;
+            atomicOr(&g_simt_err, ERRBIT_SEQLENS);
+        }
+    }
+}
+
+// Per token t of sequence b: tok_pos = t - cu[b], tok_vcol = vcol_start[b] + tok_pos,
+// both clamped in bounds; with an invalid schedule every token maps to itself.
+__global__ void tok_meta_kernel(const int* __restrict__ cu, const int* __restrict__ vcol_start,
+                                const int* __restrict__ bad_flag, int n, int total,
+                                long long vt_cols, int* __restrict__ tok_pos,
+                                int* __restrict__ tok_vcol) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= total) return;
+    int pos = t, col = t;
+    if (!*bad_flag) {
+        int lo = 0, hi = n - 1;            // last b with cu[b] <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cu[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        pos = t - cu[lo];
+        col = vcol_start[lo] + pos;
+    }
+    tok_pos[t] = min(max(pos, 0), total - 1);
+    tok_vcol[t] = (int)min((long long)max(col, 0), vt_cols - 1);
+}
+
+cudaError_t launch_seq_meta(const int* cu_seqlens, int n_seq, int total, int* tile_start,
+                            int* vcol_start, int* last_row, int* tok_pos, int* tok_vcol,
+                            long long vt_cols, cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    // the flag shares tile_start's allocation tail: tile_start has n_seq + 2 slots
+    int* bad = tile_start + n_seq + 1;
+    int threads = n_seq < 1024 ? ((n_seq + 31) / 32) * 32 : 1024;
+    if (threads < 32) threads = 32;
+    seq_meta_kernel<<<1, threads, 0, s>>>(cu_seqlens, n_seq, total, tile_start, vcol_start,
+                                          last_row, bad);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    LaunchScope ls2(DTP_K_OTHER, s);
+    tok_meta_kernel<<<(total + 255) / 256, 256, 0, s>>>(cu_seqlens, vcol_start, bad, n_seq, total,
+                                                         vt_cols, tok_pos, tok_vcol);
     return cudaGetLastError();
 }
 

@@ -160,6 +160,24 @@ int dtp_fwd_prefill_ex(const dtp_config* cfg, const void* packed, size_t packed_
                        const uint32_t* tokens, int T, const dtp_fwd_outputs* out, void* workspace,
                        size_t ws_bytes, dtp_stream_t stream);
 
+/* Several independent sequences in one pass ("varlen" prefill).  Sequence b
+ * holds tokens[cu_seqlens[b] .. cu_seqlens[b+1]) at positions 0..len_b-1 and
+ * attends only to itself; the projections, norms and FFN run over all `total`
+ * tokens at once.
+ *   tokens      device uint32 [total]
+ *   cu_seqlens  device int32 [n_seq + 1], 0 = cu[0] <= cu[1] <= ... <= cu[n_seq] =
+ *               total (checked on the device: otherwise dtp_check reports
+ *               DTP_ERR_INVALID_ARG and no attention is computed)
+ *   out         as for dtp_fwd_prefill_ex over the `total` packed tokens, except
+ *               that last_only gives logits [n_seq, n_vocab], one row per
+ *               sequence (an empty sequence's row is unspecified)
+ *   workspace   >= dtp_workspace_size_varlen(cfg, total, n_seq) bytes. */
+size_t dtp_workspace_size_varlen(const dtp_config* cfg, int total, int n_seq);
+int dtp_fwd_prefill_varlen(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                           const uint32_t* tokens, const int32_t* cu_seqlens, int n_seq, int total,
+                           const dtp_fwd_outputs* out, void* workspace, size_t ws_bytes,
+                           dtp_stream_t stream);
+
 /* Bytes of device workspace dtp_fwd_prefill_host needs (the forward workspace
  * plus device staging for the tokens and logits). */
 size_t dtp_workspace_size_host(const dtp_config* cfg, int T);

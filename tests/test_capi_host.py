@@ -80,3 +80,10 @@ def test_host_side_rejections(dtp):
     assert L.dtp_linear(fake, fake, fake, 1, 1, 4, 4, 4, fake, None) == -1   # residual needs f32 out
     assert L.dtp_linear(fake, fake, fake, 1, 0, 4, 4, 12, None, None) == -2  # K % 8
     assert L.dtp_timer_read(99, None, None) == -1
+    assert dtp.workspace_size_varlen(c, 256, 4) > dtp.workspace_size(c, 256)
+    assert dtp.workspace_size_varlen(c, 256, 0) == 0
+    outs = dtp._binding.FwdOutputs(0x10000, 0, None, None, None)
+    assert L.dtp_fwd_prefill_varlen(ctypes.byref(c), fake, 1 << 40, fake, None, 2, 256,
+                                    ctypes.byref(outs), fake, 1 << 40, None) == -1
+    assert L.dtp_fwd_prefill_varlen(ctypes.byref(c), fake, 1 << 40, fake, fake, 0, 256,
+                                    ctypes.byref(outs), fake, 1 << 40, None) == -1

@@ -211,3 +211,69 @@ def test_forward_last_and_kv_cache(dtp, prec):
     dtp.fwd_prefill_ex(m.c, m.packed, toks, m.workspace(T), k_cache=kc2)
     torch.cuda.synchronize()
     assert torch.equal(kc2, kc)
+
+
+@pytest.mark.parametrize("prec", ["f32", "bf16"])
+def test_varlen_packed_sequences(dtp, prec):
+    """dtp_fwd_prefill_varlen: sequences packed along the token axis, each at
+    positions 0..len-1 attending only to itself, equal the oracle run on every
+    sequence alone (hidden rows, all logits, last-position logits, KV)."""
+    cfg = synth.CONFIGS["small"].replace(precision=prec, n_layer=2)
+    lens = [100, 1, 0, 300, 57]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total = int(cu[-1])
+    toks = synth.uniform_int(5, 77, total, cfg.n_vocab)
+    m = load_model(dtp, cfg)
+    L, nk = cfg.n_layer, cfg.n_head_kv * cfg.head_dim
+    tt = torch.as_tensor(toks.astype(np.int32), device=dev)
+    ct = torch.as_tensor(cu, device=dev)
+    ws = m.workspace_varlen(total, len(lens))
+    logits = torch.empty((total, cfg.n_vocab), dtype=torch.float32, device=dev)
+    hidden = torch.empty((L + 1, total, cfg.n_embd), dtype=torch.float32, device=dev)
+    dtp.fwd_prefill_varlen(m.c, m.packed, tt, ct, ws, logits=logits, hidden=hidden)
+    last = torch.empty((len(lens), cfg.n_vocab), dtype=torch.float32, device=dev)
+    cdt = torch.float32 if prec == "f32" else torch.bfloat16
+    kc = torch.empty((L, total, nk), dtype=cdt, device=dev)
+    dtp.fwd_prefill_varlen(m.c, m.packed, tt, ct, ws, logits=last, last_only=True, k_cache=kc)
+    torch.cuda.synchronize()
+    dtp.check()
+    gl, gh, glast = logits.cpu().numpy(), hidden.cpu().numpy(), last.cpu().numpy()
+    w = synth.model_weights(cfg)
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        a = cu[b]
+        kv = []
+        rl, rh = oracle.forward(cfg, w, toks[a:a + n], bf16_operands=(prec == "bf16"),
+                                return_hidden=True, kv_out=kv)
+        assert_parity(cfg.replace(T=n), gl[a:a + n], gh[:, a:a + n], rl, rh)
+        np.testing.assert_allclose(glast[b], gl[a + n - 1], rtol=0, atol=1e-6)
+        k0 = kc[0, a:a + n].float().cpu().numpy()
+        assert rel_l2(k0, kv[0][0]) <= (1e-5 if prec == "f32" else 2.0 ** -8)
+
+
+def test_varlen_single_sequence_matches_plain_forward(dtp):
+    cfg = synth.CONFIGS["small"].replace(n_layer=2)
+    m = load_model(dtp, cfg)
+    tt = torch.as_tensor(synth.tokens(cfg).astype(np.int32), device=dev)
+    plain = m.forward(tt)
+    ct = torch.as_tensor(np.array([0, cfg.T], np.int32), device=dev)
+    out = torch.empty_like(plain)
+    dtp.fwd_prefill_varlen(m.c, m.packed, tt, ct, m.workspace_varlen(cfg.T, 1), logits=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, plain)
+
+
+def test_varlen_bad_offsets_are_reported(dtp):
+    cfg = synth.CONFIGS["small"].replace(n_layer=1)
+    m = load_model(dtp, cfg)
+    tt = torch.as_tensor(synth.tokens(cfg).astype(np.int32), device=dev)
+    logits = torch.empty((cfg.T, cfg.n_vocab), dtype=torch.float32, device=dev)
+    for bad in ([0, 200, 100, 256], [0, 100, 300], [5, 100, 256]):
+        ct = torch.as_tensor(np.array(bad, np.int32), device=dev)
+        dtp.fwd_prefill_varlen(m.c, m.packed, tt, ct, m.workspace_varlen(cfg.T, len(bad) - 1),
+                               logits=logits)
+        with pytest.raises(dtp.DtpError) as e:
+            dtp.check()
+        assert e.value.code == -1
+    dtp.check()
