@@ -29,7 +29,7 @@ class Config(ctypes.Structure):
     _fields_ = [("n_layer", c_int), ("n_embd", c_int), ("n_head", c_int), ("n_head_kv", c_int),
                 ("head_dim", c_int), ("rope_dim_count", c_int), ("n_ff", c_int),
                 ("n_vocab", c_int), ("rope_freq_base", c_float), ("rms_eps", c_float),
-                ("precision", c_int)]
+                ("precision", c_int), ("attn_gate", c_int)]
 
 
 class LayerSrc(ctypes.Structure):
@@ -137,9 +137,13 @@ def config_from(cfg) -> Config:
     prec = get("precision")
     if isinstance(prec, str):
         prec = {"f32": DTP_PREC_F32, "bf16": DTP_PREC_BF16}[prec]
+    try:
+        gate = int(bool(get("attn_gate")))
+    except (KeyError, AttributeError):
+        gate = 0
     return Config(get("n_layer"), get("n_embd"), get("n_head"), get("n_head_kv"), get("head_dim"),
                   get("rope_dim_count"), get("n_ff"), get("n_vocab"), float(get("rope_freq_base")),
-                  float(get("rms_eps")), prec)
+                  float(get("rms_eps")), prec, gate)
 
 
 # ----------------------------------------------------------------------------- entry points

@@ -74,6 +74,7 @@ struct AParams {
     const int* cu_seqlens;   // [n_seq + 1] token offsets
     const int* tile_start;   // [n_seq + 1] prefix of ceil(len / 128)
     const int* vcol_start;   // [n_seq] first v^T column of each sequence (multiple of 8)
+    const __nv_bfloat16* gate;   // optional [T, n_head*hd]: out *= sigmoid(gate)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -398,15 +399,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (qrel < seq_len && qrow < p.T) {
 #pragma unroll
                         for (int t = 0; t < 32; t += 8) {
+                            float o[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(r[t + e]) * inv;
+                            if (p.gate) {      // gated attention: out *= sigmoid(gate)
+                                const uint4 gv = *reinterpret_cast<const uint4*>(
+                                    p.gate + (size_t)qrow * p.ldo + (size_t)(h0 + i) * HD + c + t);
+                                const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&gv);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    o[e] = o[e] / (1.0f + expf(-__bfloat162float(gb[e])));
+                            }
                             uint4 u;
-                            u.x = ptx::pack_bf16x2(__uint_as_float(r[t + 0]) * inv,
-                                                   __uint_as_float(r[t + 1]) * inv);
-                            u.y = ptx::pack_bf16x2(__uint_as_float(r[t + 2]) * inv,
-                                                   __uint_as_float(r[t + 3]) * inv);
-                            u.z = ptx::pack_bf16x2(__uint_as_float(r[t + 4]) * inv,
-                                                   __uint_as_float(r[t + 5]) * inv);
-                            u.w = ptx::pack_bf16x2(__uint_as_float(r[t + 6]) * inv,
-                                                   __uint_as_float(r[t + 7]) * inv);
+                            u.x = ptx::pack_bf16x2(o[0], o[1]);
+                            u.y = ptx::pack_bf16x2(o[2], o[3]);
+                            u.z = ptx::pack_bf16x2(o[4], o[5]);
+                            u.w = ptx::pack_bf16x2(o[6], o[7]);
                             *reinterpret_cast<uint4*>(orow + c + t) = u;
                         }
                     }
@@ -478,6 +486,7 @@ cudaError_t launch_attn_tc_varlen(const __nv_bfloat16* q, const __nv_bfloat16* k
     p.cu_seqlens = vl.cu_seqlens;
     p.tile_start = vl.tile_start;
     p.vcol_start = vl.vcol_start;
+    p.gate = vl.gate;
     LaunchScope ls(DTP_K_ATTN, s);
     if (hd == 128) return launch_hd<128>(tq, tk, tv, p, s);
     return launch_hd<64>(tq, tk, tv, p, s);

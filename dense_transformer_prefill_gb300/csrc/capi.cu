@@ -126,6 +126,8 @@ static int validate_config(const dtp_config* c) {
         return fail(DTP_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_freq_base > 0");
     if (c->precision != DTP_PREC_F32 && c->precision != DTP_PREC_BF16)
         return fail(DTP_ERR_INVALID_ARG, "unknown precision %d", c->precision);
+    if (c->attn_gate != 0 && c->attn_gate != 1)
+        return fail(DTP_ERR_INVALID_ARG, "attn_gate must be 0 or 1");
     if (c->n_embd % 8 || c->n_ff % 64)
         return fail(DTP_ERR_UNSUPPORTED, "n_embd must be a multiple of 8 and n_ff of 64");
     if (c->precision == DTP_PREC_BF16) {
@@ -151,7 +153,8 @@ static PackedLayout packed_layout(const dtp_config* c) {
     PackedLayout L;
     L.elt = c->precision == DTP_PREC_BF16 ? 2 : 4;
     const size_t d = c->n_embd, hd = c->head_dim, nq = (size_t)c->n_head * hd,
-                 nqkv = (size_t)(c->n_head + 2 * c->n_head_kv) * hd, F = c->n_ff;
+                 nqkv = (size_t)(c->n_head * (1 + c->attn_gate) + 2 * c->n_head_kv) * hd,
+                 F = c->n_ff;
     size_t o = 0;
     auto take = [&](size_t bytes) {
         size_t at = o;
@@ -177,7 +180,7 @@ static PackedLayout packed_layout(const dtp_config* c) {
 
 struct Workspace {
     size_t x, h, qkv, attn, gu, act;            // f32 path
-    size_t q, k, vt, rope;                       // bf16 path
+    size_t q, k, vt, rope, gate;                 // bf16 path
     long long ldvt;
     size_t tokens, logits;                       // _host staging
     size_t tile_start, vcol_start, last_row, tok_pos, tok_vcol;   // packed sequences
@@ -208,8 +211,9 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_s
         W.k = take((size_t)T * nk * 2);
         W.vt = take(nk * (size_t)W.ldvt * 2);
         W.rope = take((size_t)T * (c->rope_dim_count / 2) * sizeof(float2));
+        if (c->attn_gate) W.gate = take((size_t)T * nq * 2);
     } else {
-        W.qkv = take((size_t)T * (nq + 2 * nk) * 4);
+        W.qkv = take((size_t)T * (nq * (1 + c->attn_gate) + 2 * nk) * 4);
         W.gu = take((size_t)T * 2 * F * 4);
     }
     if (host) {
@@ -260,7 +264,10 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
     float* logits = o.logits;
     float* hidden = o.hidden;
     const int d = c->n_embd, hd = c->head_dim, h = c->n_head, g = c->n_head_kv, F = c->n_ff;
-    const int nq = h * hd, nk = g * hd, nqkv = nq + 2 * nk;
+    const int nq = h * hd, nk = g * hd;
+    const int nqc = nq * (1 + c->attn_gate);            // q region, with the gate rows
+    const int nqkv = nqc + 2 * nk;
+    const int qstride = c->attn_gate ? 2 * hd : hd;     // q head stride within the q region
     float* x = (float*)(ws + W.x);
     float* hb = (float*)(ws + W.h);
     float* qkv = (float*)(ws + W.qkv);
@@ -282,18 +289,20 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
                                         T, nqkv, d, nullptr, s, DTP_K_GEMM_QKV));
         DTP_CUDA_CHECK(launch_qk_norm_rope(qkv, DTP_F32, nqkv, (const float*)(lp + L.q_norm),
                                            V.tok_pos, T, h, hd, c->rope_dim_count,
-                                           c->rope_freq_base, c->rms_eps, s));
-        DTP_CUDA_CHECK(launch_qk_norm_rope(qkv + nq, DTP_F32, nqkv, (const float*)(lp + L.k_norm),
+                                           c->rope_freq_base, c->rms_eps, s, qstride));
+        DTP_CUDA_CHECK(launch_qk_norm_rope(qkv + nqc, DTP_F32, nqkv, (const float*)(lp + L.k_norm),
                                            V.tok_pos, T, g, hd, c->rope_dim_count,
                                            c->rope_freq_base, c->rms_eps, s));
         if (o.k_cache)
-            DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nq, nqkv, (float*)o.k_cache + (size_t)l * T * nk,
-                                                nk, T, nk, s));
+            DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc, nqkv,
+                                                (float*)o.k_cache + (size_t)l * T * nk, nk, T, nk, s));
         if (o.v_cache)
-            DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nq + nk, nqkv,
+            DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc + nk, nqkv,
                                                 (float*)o.v_cache + (size_t)l * T * nk, nk, T, nk, s));
-        DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, qkv + nq, nqkv, qkv + nq + nk, nqkv, 0, attn,
-                                        nq, DTP_F32, T, h, g, hd, scale, s, V.tok_pos));
+        DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, qkv + nqc, nqkv, qkv + nqc + nk, nqkv, 0, attn,
+                                        nq, DTP_F32, T, h, g, hd, scale, s, V.tok_pos, qstride));
+        if (c->attn_gate)
+            DTP_CUDA_CHECK(launch_gate_mul_f32(attn, nq, qkv + hd, nqkv, 2 * hd, T, h, hd, s));
         DTP_CUDA_CHECK(launch_gemm_simt(attn, nq, (const float*)(lp + L.wo), x, DTP_F32, d, T, d,
                                         nq, x, s, DTP_K_GEMM_O));
         DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.ffn_norm), hb, DTP_F32, T, d,
@@ -332,9 +341,10 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
     float* hidden = o.hidden;
     typedef __nv_bfloat16 bf;
     const int d = c->n_embd, hd = c->head_dim, h = c->n_head, g = c->n_head_kv, F = c->n_ff;
-    const int nq = h * hd, nk = g * hd, nqkv = nq + 2 * nk;
+    const int nq = h * hd, nk = g * hd, nqkv = nq * (1 + c->attn_gate) + 2 * nk;
     float* x = (float*)(ws + W.x);
     bf* hb = (bf*)(ws + W.h);
+    bf* gate = c->attn_gate ? (bf*)(ws + W.gate) : nullptr;
     bf* q = (bf*)(ws + W.q);
     bf* k = (bf*)(ws + W.k);
     bf* vt = (bf*)(ws + W.vt);
@@ -347,6 +357,7 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
     // columns between them are read by attention (with P = 0), so they are zeroed
     long long vt_cols = T;
     AttnVarlen vl;
+    vl.gate = gate;
     if (V.n_seq) {
         vt_cols = W.ldvt;
         DTP_CUDA_CHECK(cudaMemsetAsync(vt, 0, (size_t)nk * W.ldvt * 2, s));
@@ -375,6 +386,8 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         e.v_rows = o.v_cache ? (bf*)o.v_cache + (size_t)l * T * nk : nullptr;
         e.tok_pos = V.tok_pos;
         e.tok_vcol = V.tok_vcol;
+        e.q_gated = c->attn_gate;
+        e.gate = gate;
         e.q_norm = (const float*)(lp + L.q_norm);
         e.k_norm = (const float*)(lp + L.k_norm);
         e.rope = rope;
@@ -469,9 +482,10 @@ int dtp_pack_layer(const dtp_config* cfg, int layer, const dtp_layer_src* src, v
     const int bf = cfg->precision == DTP_PREC_BF16;
     const int d = cfg->n_embd, hd = cfg->head_dim, nq = cfg->n_head * hd,
               nk = cfg->n_head_kv * hd, F = cfg->n_ff;
-    DTP_CUDA_CHECK(launch_pack_matrix(src->wq, nq, d, lp + L.w_qkv, bf, 0, s));
-    DTP_CUDA_CHECK(launch_pack_matrix(src->wk, nk, d, lp + L.w_qkv + (size_t)nq * d * L.elt, bf, 0, s));
-    DTP_CUDA_CHECK(launch_pack_matrix(src->wv, nk, d, lp + L.w_qkv + (size_t)(nq + nk) * d * L.elt,
+    const int nqc = nq * (1 + cfg->attn_gate);      // q rows (with the per-head gate rows)
+    DTP_CUDA_CHECK(launch_pack_matrix(src->wq, nqc, d, lp + L.w_qkv, bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->wk, nk, d, lp + L.w_qkv + (size_t)nqc * d * L.elt, bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->wv, nk, d, lp + L.w_qkv + (size_t)(nqc + nk) * d * L.elt,
                                       bf, 0, s));
     DTP_CUDA_CHECK(launch_pack_matrix(src->wo, d, nq, lp + L.wo, bf, 0, s));
     DTP_CUDA_CHECK(launch_pack_matrix(src->w_gate, F, d, lp + L.w_gu, bf, 1, s));

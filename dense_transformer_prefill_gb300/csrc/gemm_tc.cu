@@ -148,13 +148,32 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
     const int hd = ea.head_dim, half = ea.rope_dims / 2;
     const int nq = ea.n_head * hd, nk = ea.n_head_kv * hd;
     const bool live = grow < p.M;
+    const int nqc = ea.q_gated ? 2 * nq : nq;      // q region (with the gate rows)
 #pragma unroll 1
     for (int h0 = 0; h0 < BN; h0 += hd) {
         const int col = n0 + h0;
         if (col >= p.N) break;
         const uint32_t th = tbase + h0;
-        if (col < nq + nk) {
-            const bool isq = col < nq;
+        const int blk = col / hd;
+        if (ea.q_gated && col < nqc && (blk & 1)) {
+            // gate block of head blk/2: stored raw (bf16) for the attention output
+#pragma unroll 1
+            for (int c = 0; c < hd; c += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + c, r);
+                if (live) {
+                    float y[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[j] = f32(r[j]);
+                    store_row32(ea.gate + (size_t)grow * nq + (blk >> 1) * hd + c, y);
+                }
+            }
+            continue;
+        }
+        if (col < nqc + nk) {
+            const bool isq = col < nqc;
+            const int qcol = ea.q_gated ? (blk >> 1) * hd : col;    // column in q
             const float* w = isq ? ea.q_norm : ea.k_norm;
             float ss = 0.f;
 #pragma unroll 1
@@ -166,8 +185,8 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
                 for (int j = 0; j < 32; ++j) ss = fmaf(f32(r[j]), f32(r[j]), ss);
             }
             const float rstd = 1.0f / sqrtf(ss / (float)hd + ea.eps);
-            __nv_bfloat16* dst = isq ? ea.q + (size_t)grow * nq + col
-                                     : ea.k + (size_t)grow * nk + (col - nq);
+            __nv_bfloat16* dst = isq ? ea.q + (size_t)grow * nq + qcol
+                                     : ea.k + (size_t)grow * nk + (col - nqc);
 #pragma unroll 1
             for (int i0 = 0; i0 < half; i0 += 32) {
                 uint32_t ra[32], rb[32];
@@ -203,7 +222,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
                 }
             }
         } else {
-            const int vcol = col - nq - nk;
+            const int vcol = col - nqc - nk;
 #pragma unroll 1
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];

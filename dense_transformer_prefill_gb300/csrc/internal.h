@@ -57,7 +57,11 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype,
                            int cols, float eps, cudaStream_t s, const int* row_idx = nullptr);
 cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
                                 const int32_t* pos, int T, int n_heads, int head_dim,
-                                int rope_dims, float freq_base, float eps, cudaStream_t s);
+                                int rope_dims, float freq_base, float eps, cudaStream_t s,
+                                int head_stride = 0);
+// attn[t, h*hd + e] *= sigmoid(gate[t * ldg + h*gstride + e]) (float32)
+cudaError_t launch_gate_mul_f32(float* attn, int lda, const float* gate, int ldg, int gstride,
+                                int T, int n_head, int head_dim, cudaStream_t s);
 cudaError_t launch_rope_table(float2* tab, int T, int rope_dims, float freq_base,
                               cudaStream_t s);
 cudaError_t launch_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
@@ -74,7 +78,8 @@ cudaError_t launch_gemm_simt(const float* x, int ldx, const float* W, void* y, i
 cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, const void* v,
                              int ldv, int v_t, void* out, int ldo, int dtype, int T,
                              int n_head, int n_head_kv, int head_dim, float scale,
-                             cudaStream_t s, const int* tok_pos = nullptr);
+                             cudaStream_t s, const int* tok_pos = nullptr,
+                             int q_head_stride = 0);
 // Per-sequence schedule for packed sequences: tile_start [n_seq+1] (prefix of
 // ceil(len/128)), vcol_start [n_seq] (prefix of len rounded up to 8),
 // last_row [n_seq] (cu[b+1]-1); then per-token tok_pos / tok_vcol [total].
@@ -112,6 +117,8 @@ struct GemmEpiArgs {
     __nv_bfloat16* v_rows = nullptr;    // optional token-major v [M, n_head_kv*hd]
     const int* tok_pos = nullptr;       // optional per-row RoPE position (default: the row)
     const int* tok_vcol = nullptr;      // optional per-row v^T column (default: the row)
+    int q_gated = 0;                    // q region holds [q | gate] per head
+    __nv_bfloat16* gate = nullptr;      // [M, n_head*hd] raw gate values (when q_gated)
     const float* q_norm = nullptr;
     const float* k_norm = nullptr;
     const float2* rope = nullptr;       // [M, rope_dims/2] (cos, sin)
@@ -135,6 +142,7 @@ cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                            int n_head, int n_head_kv, int head_dim, float scale, cudaStream_t s);
 // Several sequences packed along the token axis (see seq_meta in simt.cu).
 struct AttnVarlen {
+    const __nv_bfloat16* gate = nullptr;   // optional [T, n_head*hd]: out *= sigmoid(gate)
     int n_seq = 0;
     const int* cu_seqlens = nullptr;   // [n_seq + 1]
     const int* tile_start = nullptr;   // [n_seq + 1]

@@ -222,7 +222,7 @@ cudaError_t launch_rope_table(float2* tab, int T, int rope_dims, float freq_base
 template <typename Tx>
 __global__ void qk_norm_rope_kernel(Tx* __restrict__ x, int ld, const float* __restrict__ w,
                                     const int32_t* __restrict__ pos, int n_heads, int hd,
-                                    int rope_dims, double base, float eps) {
+                                    int rope_dims, double base, float eps, int head_stride) {
     extern __shared__ float sm[];
     const int t = blockIdx.x, half = rope_dims / 2;
     float2* cs = reinterpret_cast<float2*>(sm);                 // [half]
@@ -233,7 +233,7 @@ __global__ void qk_norm_rope_kernel(Tx* __restrict__ x, int ld, const float* __r
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     float* rb = rowbuf + warp * hd;
     for (int h = warp; h < n_heads; h += nw) {
-        Tx* row = x + (size_t)t * ld + (size_t)h * hd;
+        Tx* row = x + (size_t)t * ld + (size_t)h * head_stride;
         float ss = 0.f;
         for (int e = lane; e < hd; e += 32) {
             float v = ld_elt(row, e);
@@ -264,18 +264,20 @@ __global__ void qk_norm_rope_kernel(Tx* __restrict__ x, int ld, const float* __r
 
 cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
                                 const int32_t* pos, int T, int n_heads, int head_dim,
-                                int rope_dims, float freq_base, float eps, cudaStream_t s) {
+                                int rope_dims, float freq_base, float eps, cudaStream_t s,
+                                int head_stride) {
     LaunchScope ls(DTP_K_OTHER, s);
+    if (head_stride <= 0) head_stride = head_dim;
     int warps = n_heads < 8 ? n_heads : 8;
     size_t smem = (size_t)(rope_dims + warps * head_dim) * sizeof(float);
     if (dtype == DTP_BF16)
         qk_norm_rope_kernel<<<T, warps * 32, smem, s>>>((__nv_bfloat16*)x, ld, w_norm, pos,
                                                         n_heads, head_dim, rope_dims,
-                                                        (double)freq_base, eps);
+                                                        (double)freq_base, eps, head_stride);
     else
         qk_norm_rope_kernel<<<T, warps * 32, smem, s>>>((float*)x, ld, w_norm, pos, n_heads,
                                                         head_dim, rope_dims, (double)freq_base,
-                                                        eps);
+                                                        eps, head_stride);
     return cudaGetLastError();
 }
 
@@ -403,7 +405,7 @@ template <typename T, bool VT>
 __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __restrict__ k,
                                  int ldk, const T* __restrict__ v, int ldv, T* __restrict__ out,
                                  int ldo, int Tn, int n_head, int n_head_kv, int hd, float scale,
-                                 const int* __restrict__ tok_pos) {
+                                 const int* __restrict__ tok_pos, int q_head_stride) {
     extern __shared__ float sm[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -411,7 +413,8 @@ __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __re
     const int kvh = head / (n_head / n_head_kv);
     float* qs = sm + warp * hd;
     if (t >= Tn) return;
-    for (int e = lane; e < hd; e += 32) qs[e] = ld_elt(q, (size_t)t * ldq + (size_t)head * hd + e);
+    for (int e = lane; e < hd; e += 32)
+        qs[e] = ld_elt(q, (size_t)t * ldq + (size_t)head * q_head_stride + e);
     __syncwarp();
     constexpr int MAXD = 8;                 // hd <= 256
     float acc[MAXD];
@@ -462,8 +465,9 @@ __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __re
 cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, const void* v,
                              int ldv, int v_t, void* out, int ldo, int dtype, int T,
                              int n_head, int n_head_kv, int head_dim, float scale,
-                             cudaStream_t s, const int* tok_pos) {
+                             cudaStream_t s, const int* tok_pos, int q_head_stride) {
     LaunchScope ls(DTP_K_ATTN, s);
+    if (q_head_stride <= 0) q_head_stride = head_dim;
     const int warps = 4;
     dim3 grid((T + warps - 1) / warps, n_head);
     size_t smem = (size_t)warps * head_dim * sizeof(float);
@@ -472,20 +476,20 @@ cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, con
         if (v_t)
             attn_simt_kernel<B, true><<<grid, warps * 32, smem, s>>>(
                 (const B*)q, ldq, (const B*)k, ldk, (const B*)v, ldv, (B*)out, ldo, T, n_head,
-                n_head_kv, head_dim, scale, tok_pos);
+                n_head_kv, head_dim, scale, tok_pos, q_head_stride);
         else
             attn_simt_kernel<B, false><<<grid, warps * 32, smem, s>>>(
                 (const B*)q, ldq, (const B*)k, ldk, (const B*)v, ldv, (B*)out, ldo, T, n_head,
-                n_head_kv, head_dim, scale, tok_pos);
+                n_head_kv, head_dim, scale, tok_pos, q_head_stride);
     } else {
         if (v_t)
             attn_simt_kernel<float, true><<<grid, warps * 32, smem, s>>>(
                 (const float*)q, ldq, (const float*)k, ldk, (const float*)v, ldv, (float*)out,
-                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos);
+                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos, q_head_stride);
         else
             attn_simt_kernel<float, false><<<grid, warps * 32, smem, s>>>(
                 (const float*)q, ldq, (const float*)k, ldk, (const float*)v, ldv, (float*)out,
-                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos);
+                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos, q_head_stride);
     }
     return cudaGetLastError();
 }
@@ -657,6 +661,29 @@ cudaError_t launch_seq_meta(const int* cu_seqlens, int n_seq, int total, int* ti
     LaunchScope ls2(DTP_K_OTHER, s);
     tok_meta_kernel<<<(total + 255) / 256, 256, 0, s>>>(cu_seqlens, vcol_start, bad, n_seq, total,
                                                          vt_cols, tok_pos, tok_vcol);
+    return cudaGetLastError();
+}
+
+// gated attention (f32 path): attn *= sigmoid(gate), gate head blocks gstride apart
+__global__ void gate_mul_f32_kernel(float* __restrict__ attn, int lda, const float* __restrict__ gate,
+                                    int ldg, int gstride, int T, int n_head, int hd) {
+    const size_t n = (size_t)T * n_head * hd;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t t = i / ((size_t)n_head * hd);
+        const int r = (int)(i % ((size_t)n_head * hd)), h = r / hd, e = r % hd;
+        const float g = gate[t * ldg + (size_t)h * gstride + e];
+        attn[t * lda + r] = attn[t * lda + r] / (1.0f + expf(-g));
+    }
+}
+
+cudaError_t launch_gate_mul_f32(float* attn, int lda, const float* gate, int ldg, int gstride,
+                                int T, int n_head, int head_dim, cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    size_t n = (size_t)T * n_head * head_dim, blocks = (n + 255) / 256;
+    if (blocks > 65535 * 8) blocks = 65535 * 8;
+    gate_mul_f32_kernel<<<(unsigned)blocks, 256, 0, s>>>(attn, lda, gate, ldg, gstride, T, n_head,
+                                                         head_dim);
     return cudaGetLastError();
 }
 

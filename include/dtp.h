@@ -76,12 +76,18 @@ typedef struct dtp_config {
     float rope_freq_base; /* RoPE base; theta_i = base^(-2i/r)                      */
     float rms_eps;        /* epsilon inside every RMSNorm's square root             */
     int precision;        /* DTP_PREC_F32 or DTP_PREC_BF16                          */
+    int attn_gate;        /* 1: gated attention -- the Q projection also yields, per head,
+                             head_dim gate values after its head_dim q values, and the
+                             attention output is multiplied by sigmoid(gate) before the
+                             O projection (memra-engine spec.rs, `q_gate_split`); 0: none */
 } dtp_config;
 
 /* One layer's source weights: device float32, the pages' layouts. */
 typedef struct dtp_layer_src {
     const float* attn_norm; /* [n_embd]                       */
-    const float* wq;        /* [n_head*head_dim, n_embd]      */
+    const float* wq;        /* [n_head*head_dim, n_embd]; with attn_gate
+                               [n_head*2*head_dim, n_embd]: per head, head_dim q rows
+                               then head_dim gate rows                            */
     const float* wk;        /* [n_head_kv*head_dim, n_embd]   */
     const float* wv;        /* [n_head_kv*head_dim, n_embd]   */
     const float* q_norm;    /* [head_dim]                     */

@@ -15,6 +15,11 @@ sites, not their bodies):
   * GQA: query head i reads kv head i // (n_head / n_head_kv).
   * Causal: key s is visible to query t iff s <= t.
   * SwiGLU (`ffn_act`): act = silu(gate) * up, silu(x) = x / (1 + e^-x).
+  * Gated attention (the FusedQ gate of docs.rs memra-engine 0.101.0
+    src/spec.rs, `qwen35_tparallel_fa_layer`: `q_gate_split`, `sigmoid`,
+    `mul`): the Q projection yields, per head, head_dim q values followed by
+    head_dim gate values; the attention output is multiplied elementwise by
+    sigmoid(gate) before the O projection.
   * bf16-operand mode: matrices are rounded to bf16 once; every GEMM input
     activation (normed h, attention output, SwiGLU act, final normed x) and the
     q/k/v handed to attention are rounded to bf16 (nearest, ties to even); all
@@ -164,6 +169,10 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     # attention block
     hN = op(rms_norm(x, L["attn_norm"], eps))
     q = linear(hN, L["wq"])
+    gate = None
+    if getattr(cfg, "attn_gate", False):
+        qg = q.reshape(q.shape[0], h, 2, hd)
+        q, gate = qg[:, :, 0, :].reshape(-1, h * hd), op(qg[:, :, 1, :].reshape(-1, h * hd))
     k = linear(hN, L["wk"])
     v = linear(hN, L["wv"])
     q = qk_norm(q, L["q_norm"], hd, eps)
@@ -173,7 +182,10 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     v = op(v)
     if kv_out is not None:
         kv_out.append((k, v))
-    attn = op(sdpa_causal_gqa(q, k, v, h, g, hd, scale))
+    attn = sdpa_causal_gqa(q, k, v, h, g, hd, scale)
+    if gate is not None:
+        attn = attn / (1.0 + np.exp(-gate))          # attn * sigmoid(gate)
+    attn = op(attn)
     x1 = x + linear(attn, L["wo"])
     # ffn block (dense SwiGLU)
     z = op(rms_norm(x1, L["ffn_norm"], eps))

@@ -103,13 +103,15 @@ class ModelConfig:
     rope_freq_base: float = 1e6
     rms_eps: float = 1e-6
     precision: str = "bf16"          # "f32" (exact) or "bf16" (bf16 operands, f32 accumulate)
+    attn_gate: bool = False          # sigmoid output gate fused into the Q projection
 
     def replace(self, **kw) -> "ModelConfig":
         return dataclasses.replace(self, **kw)
 
     @property
     def n_qkv(self) -> int:
-        return (self.n_head + 2 * self.n_head_kv) * self.head_dim
+        """Rows of the fused QKV weight: q (and its gate, per head) + k + v."""
+        return (self.n_head * (2 if self.attn_gate else 1) + 2 * self.n_head_kv) * self.head_dim
 
     def gemm_flops(self, T: int | None = None) -> float:
         """2*T*sum(out*in) over every projection, the FFN and the lm_head."""
@@ -161,7 +163,8 @@ def layer_tid(layer: int, name: str) -> int:
 def layer_shapes(cfg: ModelConfig) -> dict:
     d, hd, h, g, F = cfg.n_embd, cfg.head_dim, cfg.n_head, cfg.n_head_kv, cfg.n_ff
     return {
-        "attn_norm": (d,), "wq": (h * hd, d), "wk": (g * hd, d), "wv": (g * hd, d),
+        "attn_norm": (d,), "wq": (h * hd * (2 if cfg.attn_gate else 1), d), "wk": (g * hd, d),
+        "wv": (g * hd, d),
         "q_norm": (hd,), "k_norm": (hd,), "wo": (d, h * hd), "ffn_norm": (d,),
         "w_gate": (F, d), "w_up": (F, d), "w_down": (d, F),
     }

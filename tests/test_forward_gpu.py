@@ -277,3 +277,13 @@ def test_varlen_bad_offsets_are_reported(dtp):
             dtp.check()
         assert e.value.code == -1
     dtp.check()
+
+
+@pytest.mark.parametrize("prec", ["f32", "bf16"])
+def test_gated_attention(dtp, prec):
+    """attn_gate: per head [q | gate] from the Q projection, attention output *
+    sigmoid(gate) before the O projection (spec.rs q_gate_split / sigmoid / mul)."""
+    cfg = synth.CONFIGS["small"].replace(precision=prec, n_layer=2, attn_gate=True)
+    _, gl, gh = run_gpu(dtp, cfg, T=200)
+    _, rl, rh = oracle_forward(cfg, T=200)
+    assert_parity(cfg.replace(T=200), gl, gh, rl, rh)

@@ -390,3 +390,45 @@ def test_planted_transposed_weight_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "linear",
                         lambda x, W: np.asarray(x) @ np.asarray(W).reshape(W.shape[1], W.shape[0]))
     assert _pins_fail(test_linear_exact_on_integers_and_orientation)
+
+
+# ---------------------------------------------------------------- gated attention
+def _gated_from(cfg, w, gate_rows):
+    """Gated weights: per head, that head's q rows then `gate_rows(head)`."""
+    hd, h = cfg.head_dim, cfg.n_head
+    w2 = dict(w)
+    w2["layers"] = []
+    for lw in w["layers"]:
+        blocks = []
+        for i in range(h):
+            blocks.append(lw["wq"][i * hd:(i + 1) * hd])
+            blocks.append(gate_rows(lw, i))
+        w2["layers"].append(dict(lw, wq=np.concatenate(blocks, axis=0)))
+    return w2
+
+
+def test_gated_attention_zero_gate_halves_attention():
+    # sigmoid(0) = 1/2: the gated model with zero gate rows is the ungated model
+    # with Wo halved -- this also pins the per-head [q | gate] row layout
+    w = synth.model_weights(TINY)
+    gcfg = TINY.replace(attn_gate=True)
+    wg = _gated_from(TINY, w, lambda lw, i: np.zeros((TINY.head_dim, TINY.n_embd)))
+    wh = dict(w)
+    wh["layers"] = [dict(lw, wo=0.5 * lw["wo"]) for lw in w["layers"]]
+    toks = synth.tokens(TINY)
+    np.testing.assert_allclose(oracle.forward(gcfg, wg, toks), oracle.forward(TINY, wh, toks),
+                               rtol=1e-12, atol=1e-14)
+
+
+def test_planted_gate_layout_swap_is_caught(monkeypatch):
+    # reading the q region as [all q heads | all gate heads] instead of per head
+    real = om.forward_layer
+
+    def wrong(cfg, lw, x, pos, bf16_operands=False, kv_out=None):
+        if getattr(cfg, "attn_gate", False):
+            h, hd = cfg.n_head, cfg.head_dim
+            wq = lw["wq"].reshape(2, h, hd, -1).transpose(1, 0, 2, 3).reshape(2 * h * hd, -1)
+            lw = dict(lw, wq=wq)
+        return real(cfg, lw, x, pos, bf16_operands, kv_out)
+    monkeypatch.setattr(om, "forward_layer", wrong)
+    assert _pins_fail(test_gated_attention_zero_gate_halves_attention)
