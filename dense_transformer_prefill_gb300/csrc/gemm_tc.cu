@@ -62,20 +62,49 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : (BN == 224 ? 5 : 6);
+    // The 224-wide tile keeps a fifth pipeline stage instead of the epilogue
+    // staging (the main loop is latency-bound: its depth matters more than store
+    // efficiency there) and stores directly from registers.
+    static constexpr bool TMA_OUT = BN != 224;
+    static constexpr int STAGES = BN == 128 ? 6 : (BN == 224 ? 5 : 4);
     // two accumulators; the second starts at a 256-column boundary when BN > 128
     static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;
     static constexpr int TMEM_COLS = 2 * ACC_STRIDE;
+    // epilogue staging: per epilogue warp two 32-row x 128-byte boxes (4 KB each)
+    static constexpr int EPI_BUF = 4096;
+    static constexpr int EPI_BYTES = TMA_OUT ? 4 * 2 * EPI_BUF : 0;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
 };
 
 struct Params {
     int M, N, K;
     int tiles_m, tiles_n, num_kb;
     int vec_ok;     // y row stride / base allow 16-byte vector stores
+    int tma_out;    // outputs go through shared-memory staging and TMA stores
     GemmEpiArgs ea;
 };
+
+// Per-epilogue-warp staging state: two 32-row x 128-byte boxes in the
+// 128-byte-swizzle layout TMA expects (16-byte chunk j of row r at
+// r*128 + ((j ^ (r & 7)) << 4)), their residual-load barriers, and a running
+// buffer counter.  Lane 0 issues every bulk copy.
+struct EpiStage {
+    uint8_t* buf[2];
+    uint64_t* rbar[2];
+    uint32_t rphase[2];
+    uint32_t pending[2];    // a residual load into buf[b] not yet waited for
+    uint32_t cnt;
+    int lane;
+    int row0;           // global row of this warp's lane 0
+};
+
+__device__ __forceinline__ void stage_put16(uint8_t* buf, int lane, int chunk, uint4 v) {
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((chunk ^ (lane & 7)) << 4)) = v;
+}
+__device__ __forceinline__ uint4 stage_get16(const uint8_t* buf, int lane, int chunk) {
+    return *reinterpret_cast<const uint4*>(buf + lane * 128 + ((chunk ^ (lane & 7)) << 4));
+}
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
@@ -273,24 +302,274 @@ __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, int 
     }
 }
 
+// ----------------------------------------------------------------------------- TMA-store epilogues
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+    uint4 u;
+    u.x = ptx::pack_bf16x2(v[0], v[1]);
+    u.y = ptx::pack_bf16x2(v[2], v[3]);
+    u.z = ptx::pack_bf16x2(v[4], v[5]);
+    u.w = ptx::pack_bf16x2(v[6], v[7]);
+    return u;
+}
+
+// Hand the staged box to TMA (lane 0) after every lane's writes are visible to it.
+__device__ __forceinline__ void stage_flush(EpiStage& st, int b, const CUtensorMap* map, int x) {
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (st.lane == 0) {
+        ptx::tma_store_2d(map, st.buf[b], x, st.row0);
+        ptx::bulk_commit();
+    }
+}
+
+// Before writing buffer b: the bulk store issued from it two flushes ago has
+// finished reading it.
+__device__ __forceinline__ void stage_claim(EpiStage& st) {
+    if (st.lane == 0) ptx::bulk_wait_read<1>();
+    __syncwarp();
+}
+
+// Residual chunk (f32 32x32 box) for the chunk at column x into buffer b.
+__device__ __forceinline__ void stage_prefetch(EpiStage& st, int b, const CUtensorMap* tmR, int x) {
+    if (st.lane == 0) {
+        ptx::bulk_wait_read<0>();
+        ptx::mbar_arrive_expect_tx(st.rbar[b], 32 * 128);
+        ptx::tma_load_2d(tmR, st.rbar[b], st.buf[b], x, st.row0);
+    }
+    st.pending[b] = 1;
+    __syncwarp();
+}
+
+// y = acc (+ residual): float32 chunks of 32 columns or bf16 chunks of 64.
+// BN must be a multiple of the chunk width (32 for float32, 64 for bf16 output).
+template <int BN>
+__device__ __forceinline__ bool epi_store_tma(const Params& p, EpiStage& st, uint32_t tbase, int n0,
+                                              const CUtensorMap* tmY, const CUtensorMap* tmR,
+                                              volatile int* abort_flag) {
+    const GemmEpiArgs& ea = p.ea;
+    const bool f32out = ea.y_dtype == DTP_F32;
+    const bool resid = ea.residual != nullptr;
+    const int CW = f32out ? 32 : 64;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += CW) {
+        const int col0 = n0 + c;
+        if (col0 >= p.N) break;
+        const int b = st.cnt & 1;
+        if (resid) {
+            // buf[b] already holds (or is receiving) this chunk's residual; the
+            // first chunk of a tile was prefetched before the accumulator wait
+            if (c + CW < BN && col0 + CW < p.N) stage_prefetch(st, b ^ 1, tmR, col0 + CW);
+        } else {
+            stage_claim(st);
+        }
+        float v[64];
+        uint32_t r[32];
+        __syncwarp();
+        ptx::tmem_ld32(tbase + c, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = f32(r[j]);
+        if (!f32out) {
+            __syncwarp();
+            ptx::tmem_ld32(tbase + c + 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[32 + j] = f32(r[j]);
+        }
+        if (resid) {
+            const bool ok = ptx::wait_bounded(st.rbar[b], st.rphase[b], abort_flag, &g_gemm_err,
+                                              ERRBIT_TIMEOUT);
+            if (!__all_sync(0xffffffffu, ok)) return false;
+            st.rphase[b] ^= 1;
+            st.pending[b] = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 u = stage_get16(st.buf[b], st.lane, j);
+                v[4 * j + 0] += __uint_as_float(u.x);
+                v[4 * j + 1] += __uint_as_float(u.y);
+                v[4 * j + 2] += __uint_as_float(u.z);
+                v[4 * j + 3] += __uint_as_float(u.w);
+            }
+        }
+        if (f32out) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                stage_put16(st.buf[b], st.lane, j,
+                            make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                       __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3])));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) stage_put16(st.buf[b], st.lane, j, pack8_bf16(v + 8 * j));
+        }
+        stage_flush(st, b, tmY, col0);
+        ++st.cnt;
+    }
+    return true;
+}
+
+// gate/up (interleaved 64-column blocks) -> act = silu(g) * u, bf16 boxes of 64 columns.
+template <int BN>
+__device__ __forceinline__ void epi_swiglu_tma(const Params& p, EpiStage& st, uint32_t tbase,
+                                               int n0, const CUtensorMap* tmY) {
+#pragma unroll 1
+    for (int b = 0; b < BN; b += 128) {
+        const int colblk = n0 + b;
+        if (colblk >= p.N) break;
+        const int bb = st.cnt & 1;
+        stage_claim(st);
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 32) {
+            uint32_t rg[32], ru[32];
+            __syncwarp();
+            ptx::tmem_ld32(tbase + b + c, rg);
+            ptx::tmem_ld32(tbase + b + 64 + c, ru);
+            float a[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] = silu_f(f32(rg[j])) * f32(ru[j]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) stage_put16(st.buf[bb], st.lane, c / 8 + j, pack8_bf16(a + 8 * j));
+        }
+        stage_flush(st, bb, tmY, colblk / 2);
+        ++st.cnt;
+    }
+}
+
+// QKV: q/k heads normalised and rotated, staged as 64-column bf16 boxes (one or
+// two per head); v heads (transposed) and gate blocks stored directly.
+template <int BN>
+__device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint32_t tbase,
+                                            int grow, int n0, const CUtensorMap* tmQ,
+                                            const CUtensorMap* tmK) {
+    const GemmEpiArgs& ea = p.ea;
+    const int hd = ea.head_dim, half = ea.rope_dims / 2;
+    const int nq = ea.n_head * hd, nk = ea.n_head_kv * hd;
+    const bool live = grow < p.M;
+    const int nqc = ea.q_gated ? 2 * nq : nq;
+#pragma unroll 1
+    for (int h0 = 0; h0 < BN; h0 += hd) {
+        const int col = n0 + h0;
+        if (col >= p.N) break;
+        const uint32_t th = tbase + h0;
+        const int blk = col / hd;
+        if (ea.q_gated && col < nqc && (blk & 1)) {
+#pragma unroll 1
+            for (int c = 0; c < hd; c += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + c, r);
+                if (live) {
+                    float y[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[j] = f32(r[j]);
+                    store_row32(ea.gate + (size_t)grow * nq + (blk >> 1) * hd + c, y);
+                }
+            }
+            continue;
+        }
+        if (col < nqc + nk) {
+            const bool isq = col < nqc;
+            const int ocol = isq ? (ea.q_gated ? (blk >> 1) * hd : col) : col - nqc;
+            const float* w = isq ? ea.q_norm : ea.k_norm;
+            float ss = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < hd; c += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + c, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ss = fmaf(f32(r[j]), f32(r[j]), ss);
+            }
+            const float rstd = 1.0f / sqrtf(ss / (float)hd + ea.eps);
+            // both staging buffers may be needed (head_dim 128): wait for all reads
+            if (st.lane == 0) ptx::bulk_wait_read<0>();
+            __syncwarp();
+            const int pos = ea.tok_pos ? ea.tok_pos[live ? grow : 0] : grow;
+#pragma unroll 1
+            for (int i0 = 0; i0 < half; i0 += 32) {
+                uint32_t ra[32], rb[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + i0, ra);
+                ptx::tmem_ld32(th + half + i0, rb);
+                const float2* cs = ea.rope + (size_t)(live ? pos : 0) * half + i0;
+                float ya[32], yb[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float a = f32(ra[j]) * rstd * w[i0 + j];
+                    const float bv = f32(rb[j]) * rstd * w[half + i0 + j];
+                    const float2 c2 = cs[j];
+                    ya[j] = a * c2.x - bv * c2.y;
+                    yb[j] = a * c2.y + bv * c2.x;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    stage_put16(st.buf[(i0 >> 6)], st.lane, ((i0 & 63) >> 3) + j, pack8_bf16(ya + 8 * j));
+                    const int cb = half + i0;
+                    stage_put16(st.buf[(cb >> 6)], st.lane, ((cb & 63) >> 3) + j, pack8_bf16(yb + 8 * j));
+                }
+            }
+#pragma unroll 1
+            for (int c = ea.rope_dims; c < hd; c += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + c, r);
+                float y[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) y[j] = f32(r[j]) * rstd * w[c + j];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    stage_put16(st.buf[(c >> 6)], st.lane, ((c & 63) >> 3) + j, pack8_bf16(y + 8 * j));
+            }
+            const CUtensorMap* map = isq ? tmQ : tmK;
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (st.lane == 0) {
+                for (int a = 0; a < hd / 64; ++a) ptx::tma_store_2d(map, st.buf[a], ocol + 64 * a, st.row0);
+                ptx::bulk_commit();
+            }
+        } else {
+            const int vcol = col - nqc - nk;
+#pragma unroll 1
+            for (int c = 0; c < hd; c += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                ptx::tmem_ld32(th + c, r);
+                if (live) {
+                    const int tcol = ea.tok_vcol ? ea.tok_vcol[grow] : grow;
+                    __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        dst[(size_t)j * ea.ldvt] = __float2bfloat16_rn(f32(r[j]));
+                    if (ea.v_rows) {
+                        float y[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) y[j] = f32(r[j]);
+                        store_row32(ea.v_rows + (size_t)grow * nk + vcol + c, y);
+                    }
+                }
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------------------- kernel
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const Params p) {
+                   const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmY2,
+                   const __grid_constant__ CUtensorMap tmR, const Params p) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint8_t* sEpi = smem + C::STAGES * C::STAGE_BYTES;          // 1024-byte aligned
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + C::EPI_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
     uint64_t* tfull = bars + 2 * C::STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* rbars = drain + 1;                                 // [4 warps][2]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(rbars + 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -304,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&tempty[b], 128);
         }
         ptx::mbar_init(drain, 1);
+        for (int i = 0; i < 8; ++i) ptx::mbar_init(&rbars[i], 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -314,6 +594,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1 && lane == 0) {
         ptx::tma_prefetch_desc(&tmA);
         ptx::tma_prefetch_desc(&tmB);
+        if (C::TMA_OUT && p.tma_out) {
+            ptx::tma_prefetch_desc(&tmY);
+            ptx::tma_prefetch_desc(&tmY2);
+            ptx::tma_prefetch_desc(&tmR);
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -406,25 +691,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- epilogue warps 2..5
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
+        EpiStage st;
+        st.buf[0] = sEpi + (warp - 2) * 2 * C::EPI_BUF;
+        st.buf[1] = st.buf[0] + C::EPI_BUF;
+        st.rbar[0] = &rbars[(warp - 2) * 2];
+        st.rbar[1] = &rbars[(warp - 2) * 2 + 1];
+        st.rphase[0] = st.rphase[1] = 0;
+        st.pending[0] = st.pending[1] = 0;
+        st.cnt = 0;
+        st.lane = lane;
+        const bool tma_out = C::TMA_OUT && p.tma_out;
+        const bool resid_tma = EPI == EPI_STORE && tma_out && p.ea.residual != nullptr;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int mb = tile % p.tiles_m, nb = tile / p.tiles_m;
+            const int grow = mb * BM + row, n0 = nb * BN;
+            st.row0 = mb * BM + quarter * 32;
+            // the first residual chunk of the tile loads while the main loop runs
+            if (resid_tma) stage_prefetch(st, st.cnt & 1, &tmR, n0);
             const bool ok = ptx::wait_bounded(&tfull[acc], acc_phase, abort_flag, &g_gemm_err,
                                               ERRBIT_TIMEOUT);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_STRIDE;
-            const int grow = mb * BM + row, n0 = nb * BN;
-            if (EPI == EPI_STORE) epi_store<BN>(p, tbase, grow, n0);
-            if (EPI == EPI_QKV) epi_qkv<BN>(p, tbase, grow, n0);
-            if (EPI == EPI_SWIGLU) epi_swiglu<BN>(p, tbase, grow, n0);
+            bool eok = true;
+            if (tma_out) {
+                if (EPI == EPI_STORE)
+                    eok = epi_store_tma<BN>(p, st, tbase, n0, &tmY, &tmR, abort_flag);
+                if (EPI == EPI_QKV) epi_qkv_tma<BN>(p, st, tbase, grow, n0, &tmY, &tmY2);
+                if (EPI == EPI_SWIGLU) epi_swiglu_tma<BN>(p, st, tbase, n0, &tmY);
+            } else {
+                if (EPI == EPI_STORE) epi_store<BN>(p, tbase, grow, n0);
+                if (EPI == EPI_QKV) epi_qkv<BN>(p, tbase, grow, n0);
+                if (EPI == EPI_SWIGLU) epi_swiglu<BN>(p, tbase, grow, n0);
+            }
             __syncwarp();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&tempty[acc]);
+            if (!eok) break;
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        // every staged box is written out, and every residual load that was
+        // issued but not consumed (only after an abort) has landed, before the
+        // CTA and its shared memory go away
+        if (lane == 0) {
+            ptx::bulk_wait<0>();
+            volatile int never = 0;
+            for (int b = 0; b < 2; ++b)
+                if (st.pending[b])
+                    ptx::wait_bounded(st.rbar[b], st.rphase[b], &never, &g_gemm_err, ERRBIT_TIMEOUT);
+        }
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -437,7 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN, int EPI>
-cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
+                        const CUtensorMap& ty2, const CUtensorMap& tr, const Params& p,
                         cudaStream_t s) {
     using C = Cfg<BN>;
     static std::once_flag once;
@@ -450,7 +770,7 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const Para
     if (attr_err != cudaSuccess) return attr_err;
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::SMEM_BYTES, s>>>(ta, tb, p);
+    gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::SMEM_BYTES, s>>>(ta, tb, ty, ty2, tr, p);
     return cudaGetLastError();
 }
 
@@ -458,27 +778,21 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const Para
 
 // Tile width: the fused QKV and SwiGLU epilogues need 256 (whole heads / whole
 // 128-column gate-up blocks).  A plain store picks the width whose persistent
-// schedule finishes first: waves(BN) * BN, waves = ceil(tiles / SMs).
-static int pick_bn(int M, int N, GemmEpi epi) {
+// schedule finishes first: waves(BN) * BN, waves = ceil(tiles / SMs); 224 only
+// with float32 output (its epilogue chunks are 32 columns; bf16 chunks are 64).
+static int pick_bn(int M, int N, GemmEpi epi, int y_dtype) {
     if (epi != EPI_STORE) return 256;
     if (N <= 128) return 128;
+    if (y_dtype != DTP_F32) return 256;
+    // 256 stores through TMA; 224 only when it saves at least 5% of the schedule
     const long long tm = (M + BM - 1) / BM, sms = num_sms();
-    int best = 256;
-    long long best_cost = -1;
-    for (int bn : {256, 224}) {
-        const long long tiles = tm * ((N + bn - 1) / bn);
-        const long long cost = (tiles + sms - 1) / sms * bn;
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = bn;
-        }
-    }
-    return best;
+    auto cost = [&](long long bn) { return (tm * ((N + bn - 1) / bn) + sms - 1) / sms * bn; };
+    return 20 * cost(224) < 19 * cost(256) ? 224 : 256;
 }
 
 cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,
                            GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind) {
-    const int BN = pick_bn(M, N, epi);
+    const int BN = pick_bn(M, N, epi, ea.y_dtype);
     CUtensorMap ta, tb;
     if (!make_tmap_2d(&ta, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, K, BM, BK))
         return cudaErrorInvalidValue;
@@ -493,20 +807,39 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M
     p.num_kb = (K + BK - 1) / BK;
     p.ea = ea;
     p.vec_ok = 1;
+    p.tma_out = 0;
+    // output (and residual) tensor maps: 32-row boxes of 128 bytes, 128-byte swizzle
+    CUtensorMap ty = ta, ty2 = ta, tr = ta;
+    auto al16 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
     if (epi == EPI_STORE) {
         const int eb = ea.y_dtype == DTP_F32 ? 4 : 2;
-        if ((ea.ldy * eb) % 16 != 0 || reinterpret_cast<uintptr_t>(ea.y) % 16 != 0 ||
-            (ea.residual && reinterpret_cast<uintptr_t>(ea.residual) % 16 != 0))
+        if ((ea.ldy * eb) % 16 != 0 || !al16(ea.y) || (ea.residual && !al16(ea.residual)))
             p.vec_ok = 0;
+        const CUtensorMapDataType dt =
+            ea.y_dtype == DTP_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        if (p.vec_ok && make_tmap_2d(&ty, ea.y, dt, eb, M, N, ea.ldy, 32, 128 / eb) &&
+            (!ea.residual || make_tmap_2d(&tr, ea.residual, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N,
+                                          ea.ldy, 32, 32)))
+            p.tma_out = 1;
+    } else if (epi == EPI_SWIGLU) {
+        p.tma_out = al16(ea.act) &&
+                    make_tmap_2d(&ty, ea.act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N / 2, N / 2, 32, 64);
+    } else if (epi == EPI_QKV) {
+        const int nq = ea.n_head * ea.head_dim, nk = ea.n_head_kv * ea.head_dim;
+        p.tma_out = al16(ea.q) && al16(ea.k) &&
+                    make_tmap_2d(&ty, ea.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, nq, nq, 32, 64) &&
+                    make_tmap_2d(&ty2, ea.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, nk, nk, 32, 64);
     }
+    if (BN == 224) p.tma_out = 0;
+    if (!p.tma_out) ty = ty2 = tr = ta;
     LaunchScope ls(kind, s);
     if (BN == 256) {
-        if (epi == EPI_QKV) return launch_impl<256, EPI_QKV>(ta, tb, p, s);
-        if (epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU>(ta, tb, p, s);
-        return launch_impl<256, EPI_STORE>(ta, tb, p, s);
+        if (epi == EPI_QKV) return launch_impl<256, EPI_QKV>(ta, tb, ty, ty2, tr, p, s);
+        if (epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU>(ta, tb, ty, ty2, tr, p, s);
+        return launch_impl<256, EPI_STORE>(ta, tb, ty, ty2, tr, p, s);
     }
-    if (BN == 224) return launch_impl<224, EPI_STORE>(ta, tb, p, s);
-    return launch_impl<128, EPI_STORE>(ta, tb, p, s);
+    if (BN == 224) return launch_impl<224, EPI_STORE>(ta, tb, ty, ty2, tr, p, s);
+    return launch_impl<128, EPI_STORE>(ta, tb, ty, ty2, tr, p, s);
 }
 
 }  // namespace dtp

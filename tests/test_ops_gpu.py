@@ -118,7 +118,8 @@ def test_linear_f32(dtp, M, N, K, resid):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (128, 256, 64), (130, 200, 72), (256, 768, 512),
-                                   (300, 1000, 136), (513, 2048, 1024), (64, 384, 4096)])
+                                   (300, 1000, 136), (513, 2048, 1024), (64, 384, 4096),
+                                   (77, 1001, 136)])   # odd row stride: direct-store epilogue
 @pytest.mark.parametrize("mode", ["f32", "bf16", "resid"])
 def test_linear_bf16_tensor_core(dtp, M, N, K, mode):
     x = bf16_round32(synth.normal(6, 600, (M, K)))
