@@ -17,10 +17,12 @@ from ._binding import (  # noqa: F401
     check,
     config_from,
     fwd_prefill,
+    fwd_prefill_chunk,
     fwd_prefill_ex,
     fwd_prefill_host,
     fwd_prefill_varlen,
     gate_up_swiglu,
+    kv_state_size,
     last_error,
     launch_count,
     linear,

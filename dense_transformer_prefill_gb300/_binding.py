@@ -63,6 +63,10 @@ _SIGS = {
     "dtp_fwd_prefill_varlen": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_void_p, c_int,
                                 c_int, ctypes.POINTER(FwdOutputs), c_void_p, c_size_t, c_void_p],
                                c_int),
+    "dtp_kv_state_size": ([ctypes.POINTER(Config), c_int], c_size_t),
+    "dtp_fwd_prefill_chunk": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int, c_int,
+                               c_void_p, c_size_t, c_int, ctypes.POINTER(FwdOutputs), c_void_p,
+                               c_size_t, c_void_p], c_int),
     "dtp_fwd_prefill_host": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int,
                               c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "dtp_check": ([c_void_p], c_int),
@@ -207,6 +211,26 @@ def fwd_prefill_varlen(c: Config, packed: torch.Tensor, tokens: torch.Tensor,
                                      cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, tokens.numel(),
                                      ctypes.byref(o), workspace.data_ptr(),
                                      workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kv_state_size(c: Config, max_T: int) -> int:
+    return lib().dtp_kv_state_size(ctypes.byref(c), max_T)
+
+
+def fwd_prefill_chunk(c: Config, packed: torch.Tensor, tokens: torch.Tensor, p0: int,
+                      kv_state: torch.Tensor, max_T: int, workspace: torch.Tensor, logits=None,
+                      last_only: bool = False, hidden=None, stream=None) -> None:
+    """Positions p0 .. p0+len(tokens)-1 of one sequence against `kv_state`
+    (dtp_kv_state_size(c, max_T) bytes), which holds positions 0 .. p0-1."""
+    assert tokens.dtype in (torch.int32, torch.uint32) and tokens.is_contiguous()
+    o = FwdOutputs(_ptr(logits), 1 if last_only else 0, _ptr(hidden), None, None)
+    _ok(lib().dtp_fwd_prefill_chunk(ctypes.byref(c), packed.data_ptr(),
+                                    packed.numel() * packed.element_size(), tokens.data_ptr(),
+                                    tokens.numel(), p0, kv_state.data_ptr(),
+                                    kv_state.numel() * kv_state.element_size(), max_T,
+                                    ctypes.byref(o), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(stream)))
 
 
 def fwd_prefill_host(c: Config, packed: torch.Tensor, tokens_host: torch.Tensor,

@@ -17,7 +17,9 @@
 //               unless it grows by more than 8 (then O is rescaled in TMEM),
 //               P = 2^(s - m) rounded to bf16 into 128-byte-swizzled shared
 //               memory, row sums in float32
-// Causality: key tiles 0..qt only; the diagonal tile masks key > query.
+// Causality: key tiles up to the one holding the tile's last query position;
+// tiles that reach past the first query position mask key > query.  Queries may
+// start at a position p0 > 0 (chunked prefill against earlier keys).
 // Query tiles are scheduled longest first.
 #include <math.h>
 #include <mutex>
@@ -75,6 +77,9 @@ struct AParams {
     const int* tile_start;   // [n_seq + 1] prefix of ceil(len / 128)
     const int* vcol_start;   // [n_seq] first v^T column of each sequence (multiple of 8)
     const __nv_bfloat16* gate;   // optional [T, n_head*hd]: out *= sigmoid(gate)
+    // one sequence (n_seq == 0): queries sit at positions p0 .. p0+T-1 and see
+    // keys 0 .. p0+T-1 (kv_len = p0 + T)
+    int p0, kv_len;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -86,10 +91,11 @@ __device__ __forceinline__ float ex2(float x) {
 // One pass over a 128-key score row of S in TMEM (64 columns per load):
 // mx <- max(mx, unmasked scores) and, when WRITE, P = 2^(s*sl2 - m_ref) rounded
 // to bf16 into the row's 128-byte-swizzled shared-memory slots, rs += sum(P).
-// DIAG masks keys past the query (col > row) on the diagonal tile.
+// DIAG masks keys past the query: key column col is hidden from this row when
+// col > row + dof (dof = first query position of the tile - first key position).
 template <bool DIAG, bool WRITE>
-__device__ __forceinline__ void tile_pass(uint32_t tS, uint8_t* Prow, int sw, int row, float sl2,
-                                          float m_ref, float& mx, float& rs) {
+__device__ __forceinline__ void tile_pass(uint32_t tS, uint8_t* Prow, int sw, int row, int dof,
+                                          float sl2, float m_ref, float& mx, float& rs) {
 #pragma unroll
     for (int c = 0; c < BKV; c += 64) {
         uint32_t r[64];
@@ -102,7 +108,7 @@ __device__ __forceinline__ void tile_pass(uint32_t tS, uint8_t* Prow, int sw, in
             for (int t = 0; t < 8; ++t) {
                 const int col = c + c8 * 8 + t;
                 const float sv = __uint_as_float(r[c8 * 8 + t]);
-                const bool masked = DIAG && col > row;
+                const bool masked = DIAG && col > row + dof;
                 mx = masked ? mx : fmaxf(mx, sv);
                 if (WRITE) {
                     e[t] = masked ? 0.f : ex2(fmaf(sv, sl2, -m_ref));
@@ -155,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rem = (int)blockIdx.x % items_per_qt;
     const int g = rem / pairs;
     const int h0 = g * G + 2 * (rem % pairs);
-    int qt = tile_idx, seq_start = 0, seq_len = p.T, vstart = 0;
+    int qt = tile_idx, seq_start = 0, seq_len = p.T, vstart = 0, qpos0 = p.p0, kv_len = p.kv_len;
     if (p.n_seq > 0) {
         if (tile_idx >= p.tile_start[p.n_seq]) return;      // beyond the schedule: whole CTA
         int lo = 0, hi = p.n_seq - 1;                        // last b with tile_start[b] <= tile_idx
@@ -168,8 +174,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         seq_start = p.cu_seqlens[lo];
         seq_len = p.cu_seqlens[lo + 1] - seq_start;
         vstart = p.vcol_start[lo];
+        qpos0 = 0;
+        kv_len = seq_len;
     }
-    const int n_kv = qt + 1;
+    qpos0 += qt * BQ;                       // position of the tile's first query
+    // key tiles up to the one holding the tile's last query position
+    const int kv_tiles = (kv_len + BKV - 1) / BKV, need_tiles = (qpos0 + BQ - 1) / BKV + 1;
+    const int n_kv = kv_tiles < need_tiles ? kv_tiles : need_tiles;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
@@ -339,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tc_fence_after();
             }
-            const bool diag = (j == qt);
+            const int dof = qpos0 - j * BKV;           // key col c hidden iff c > row + dof
+            const bool diag = dof < BKV - 1;
             const float sl2 = p.scale_log2;
             // Speculative single pass: P against the running max m while finding the
             // tile max.  If the tile raises a row's max by more than 2^8 (always on
@@ -347,11 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the warp redoes the pass.
             float mx = -INFINITY, rs = 0.f;
             if (j > 0) {
-                if (diag) tile_pass<true, true>(tS, Prow, sw, row, sl2, m, mx, rs);
-                else tile_pass<false, true>(tS, Prow, sw, row, sl2, m, mx, rs);
+                if (diag) tile_pass<true, true>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
+                else tile_pass<false, true>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
             } else {
-                if (diag) tile_pass<true, false>(tS, Prow, sw, row, sl2, m, mx, rs);
-                else tile_pass<false, false>(tS, Prow, sw, row, sl2, m, mx, rs);
+                if (diag) tile_pass<true, false>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
+                else tile_pass<false, false>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
             }
             const float m_tile = mx * sl2;
             const bool need = (j == 0) || (m_tile > m + kRescaleLog2);
@@ -376,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 rs = 0.f;
                 float unused = -INFINITY;
-                if (diag) tile_pass<true, true>(tS, Prow, sw, row, sl2, m, unused, rs);
-                else tile_pass<false, true>(tS, Prow, sw, row, sl2, m, unused, rs);
+                if (diag) tile_pass<true, true>(tS, Prow, sw, row, dof, sl2, m, unused, rs);
+                else tile_pass<false, true>(tS, Prow, sw, row, dof, sl2, m, unused, rs);
             }
             l += rs;
             ptx::fence_proxy_async_smem();
@@ -467,9 +479,12 @@ cudaError_t launch_attn_tc_varlen(const __nv_bfloat16* q, const __nv_bfloat16* k
     if (!attn_tc_supported(n_head, n_head_kv, head_dim)) return cudaErrorNotSupported;
     CUtensorMap tq, tk, tv;
     const int hd = head_dim;
+    // keys: T rows, or p0 + T rows of a KV state (the map ends there, so keys past
+    // the last query read zeros, never stale state)
+    const int kv_len = vl.n_seq > 0 ? T : vl.p0 + T;
     if (!make_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, (uint64_t)n_head * hd,
                       (uint64_t)n_head * hd, BQ, 64) ||
-        !make_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, (uint64_t)n_head_kv * hd,
+        !make_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_len, (uint64_t)n_head_kv * hd,
                       (uint64_t)n_head_kv * hd, BKV, 64) ||
         !make_tmap_2d(&tv, vt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)n_head_kv * hd,
                       (uint64_t)vt_cols, (uint64_t)ldvt, hd, 64))
@@ -487,6 +502,8 @@ cudaError_t launch_attn_tc_varlen(const __nv_bfloat16* q, const __nv_bfloat16* k
     p.tile_start = vl.tile_start;
     p.vcol_start = vl.vcol_start;
     p.gate = vl.gate;
+    p.p0 = vl.n_seq > 0 ? 0 : vl.p0;
+    p.kv_len = kv_len;
     LaunchScope ls(DTP_K_ATTN, s);
     if (hd == 128) return launch_hd<128>(tq, tk, tv, p, s);
     return launch_hd<64>(tq, tk, tv, p, s);

@@ -257,10 +257,35 @@ static VarlenCtx varlen_ctx(const Workspace& W, uint8_t* ws, int n_seq, const in
 
 static bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
+// KV state of a chunked prefill: per layer K (token-major), then V^T (bf16) or
+// V (f32), each 256-byte aligned.
+struct KvState {
+    uint8_t* base = nullptr;    // nullptr: an ordinary (unchunked) pass
+    int p0 = 0;
+    long long ldvt = 0;         // bf16: V^T row stride (max_T rounded up to 8)
+    size_t v_off = 0, layer_bytes = 0;
+    uint8_t* k(int l) const { return base + (size_t)l * layer_bytes; }
+    uint8_t* v(int l) const { return base + (size_t)l * layer_bytes + v_off; }
+};
+
+static KvState kv_state_layout(const dtp_config* c, int max_T) {
+    KvState S;
+    const size_t nk = (size_t)c->n_head_kv * c->head_dim;
+    if (c->precision == DTP_PREC_BF16) {
+        S.ldvt = (long long)align_up((size_t)max_T, 8);
+        S.v_off = align_up((size_t)max_T * nk * 2, 256);
+        S.layer_bytes = S.v_off + align_up(nk * (size_t)S.ldvt * 2, 256);
+    } else {
+        S.v_off = align_up((size_t)max_T * nk * 4, 256);
+        S.layer_bytes = 2 * S.v_off;
+    }
+    return S;
+}
+
 // ----------------------------------------------------------------------------- forward
 static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
                    const uint32_t* tokens, int T, const dtp_fwd_outputs& o, uint8_t* ws,
-                   const Workspace& W, const VarlenCtx& V, cudaStream_t s) {
+                   const Workspace& W, const VarlenCtx& V, const KvState& S, cudaStream_t s) {
     float* logits = o.logits;
     float* hidden = o.hidden;
     const int d = c->n_embd, hd = c->head_dim, h = c->n_head, g = c->n_head_kv, F = c->n_ff;
@@ -289,18 +314,30 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
                                         T, nqkv, d, nullptr, s, DTP_K_GEMM_QKV));
         DTP_CUDA_CHECK(launch_qk_norm_rope(qkv, DTP_F32, nqkv, (const float*)(lp + L.q_norm),
                                            V.tok_pos, T, h, hd, c->rope_dim_count,
-                                           c->rope_freq_base, c->rms_eps, s, qstride));
+                                           c->rope_freq_base, c->rms_eps, s, qstride, S.p0));
         DTP_CUDA_CHECK(launch_qk_norm_rope(qkv + nqc, DTP_F32, nqkv, (const float*)(lp + L.k_norm),
                                            V.tok_pos, T, g, hd, c->rope_dim_count,
-                                           c->rope_freq_base, c->rms_eps, s));
+                                           c->rope_freq_base, c->rms_eps, s, 0, S.p0));
         if (o.k_cache)
             DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc, nqkv,
                                                 (float*)o.k_cache + (size_t)l * T * nk, nk, T, nk, s));
         if (o.v_cache)
             DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc + nk, nqkv,
                                                 (float*)o.v_cache + (size_t)l * T * nk, nk, T, nk, s));
-        DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, qkv + nqc, nqkv, qkv + nqc + nk, nqkv, 0, attn,
-                                        nq, DTP_F32, T, h, g, hd, scale, s, V.tok_pos, qstride));
+        if (S.base) {           // chunked: append this chunk's keys and values to the state
+            float* ks = (float*)S.k(l);
+            float* vs = (float*)S.v(l);
+            DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc, nqkv, ks + (size_t)S.p0 * nk, nk, T,
+                                                nk, s));
+            DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc + nk, nqkv, vs + (size_t)S.p0 * nk, nk,
+                                                T, nk, s));
+            DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, ks, nk, vs, nk, 0, attn, nq, DTP_F32, T, h,
+                                            g, hd, scale, s, nullptr, qstride, S.p0));
+        } else {
+            DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, qkv + nqc, nqkv, qkv + nqc + nk, nqkv, 0,
+                                            attn, nq, DTP_F32, T, h, g, hd, scale, s, V.tok_pos,
+                                            qstride));
+        }
         if (c->attn_gate)
             DTP_CUDA_CHECK(launch_gate_mul_f32(attn, nq, qkv + hd, nqkv, 2 * hd, T, h, hd, s));
         DTP_CUDA_CHECK(launch_gemm_simt(attn, nq, (const float*)(lp + L.wo), x, DTP_F32, d, T, d,
@@ -336,7 +373,7 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
 
 static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
                     const uint32_t* tokens, int T, const dtp_fwd_outputs& o, uint8_t* ws,
-                    const Workspace& W, const VarlenCtx& V, cudaStream_t s) {
+                    const Workspace& W, const VarlenCtx& V, const KvState& S, cudaStream_t s) {
     float* logits = o.logits;
     float* hidden = o.hidden;
     typedef __nv_bfloat16 bf;
@@ -368,7 +405,14 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         vl.tile_start = V.tile_start;
         vl.vcol_start = V.vcol_start;
     }
-    DTP_CUDA_CHECK(launch_rope_table(rope, T, c->rope_dim_count, c->rope_freq_base, s));
+    long long ldvt = W.ldvt;
+    if (S.base) {               // chunked: keys 0 .. p0+T-1 of the state
+        vl.p0 = S.p0;
+        vt_cols = S.p0 + T;
+        ldvt = S.ldvt;
+    }
+    // row t of the table holds position p0 + t
+    DTP_CUDA_CHECK(launch_rope_table(rope, T, c->rope_dim_count, c->rope_freq_base, s, S.p0));
     DTP_CUDA_CHECK(launch_embed(tokens, T, c->n_vocab, d, P + L.tok_embd, DTP_BF16, x, s));
     for (int l = 0; l < c->n_layer; ++l) {
         const uint8_t* lp = P + (size_t)l * L.layer_bytes;
@@ -377,12 +421,18 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.attn_norm), hb, DTP_BF16, T, d,
                                       c->rms_eps, s));
         GemmEpiArgs e;
-        // with a KV cache the keys are written straight into it (attention reads them there)
+        // with a KV cache the keys are written straight into it (attention reads them
+        // there); a chunk writes its keys and values into the state at position p0
         bf* kl = o.k_cache ? (bf*)o.k_cache + (size_t)l * T * nk : k;
+        bf* vtl = vt;
+        if (S.base) {
+            kl = (bf*)S.k(l);
+            vtl = (bf*)S.v(l);
+        }
         e.q = q;
-        e.k = kl;
-        e.vt = vt;
-        e.ldvt = W.ldvt;
+        e.k = kl + (size_t)S.p0 * nk;
+        e.vt = vtl + S.p0;
+        e.ldvt = ldvt;
         e.v_rows = o.v_cache ? (bf*)o.v_cache + (size_t)l * T * nk : nullptr;
         e.tok_pos = V.tok_pos;
         e.tok_vcol = V.tok_vcol;
@@ -399,7 +449,7 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(lp + L.w_qkv), T, nqkv, d, EPI_QKV, e, s,
                                       DTP_K_GEMM_QKV));
         if (fa)
-            DTP_CUDA_CHECK(launch_attn_tc_varlen(q, kl, vt, W.ldvt, vt_cols, attn, T, h, g, hd,
+            DTP_CUDA_CHECK(launch_attn_tc_varlen(q, kl, vtl, ldvt, vt_cols, attn, T, h, g, hd,
                                                  scale, vl, s));
         else
             return fail(DTP_ERR_UNSUPPORTED,
@@ -531,7 +581,8 @@ size_t dtp_workspace_size_host(const dtp_config* cfg, int T) {
 static int fwd_checked(const dtp_config* cfg, const void* packed, size_t packed_bytes,
                        const uint32_t* tokens, int T, const dtp_fwd_outputs& out,
                        void* workspace, size_t ws_bytes, bool host_layout, dtp_stream_t stream,
-                       int n_seq = 0, const int* cu_seqlens = nullptr) {
+                       int n_seq = 0, const int* cu_seqlens = nullptr,
+                       const KvState& S = KvState()) {
     float* logits = out.logits;
     float* hidden = out.hidden;
     int rc = validate_config(cfg);
@@ -539,7 +590,8 @@ static int fwd_checked(const dtp_config* cfg, const void* packed, size_t packed_
     if (T <= 0) return fail(DTP_ERR_INVALID_ARG, "T must be >= 1 (got %d)", T);
     if (!packed || !tokens || !workspace)
         return fail(DTP_ERR_INVALID_ARG, "NULL packed, tokens or workspace");
-    if (!logits && !hidden && !out.k_cache && !out.v_cache)
+    // (a chunk may only extend its KV state)
+    if (!S.base && !logits && !hidden && !out.k_cache && !out.v_cache)
         return fail(DTP_ERR_INVALID_ARG, "no output requested");
     PackedLayout L = packed_layout(cfg);
     if (packed_bytes < L.total)
@@ -561,8 +613,9 @@ static int fwd_checked(const dtp_config* cfg, const void* packed, size_t packed_
     const VarlenCtx V = varlen_ctx(W, (uint8_t*)workspace, n_seq, cu_seqlens);
     if (cfg->precision == DTP_PREC_BF16)
         return fwd_bf16(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, V,
-                        s);
-    return fwd_f32(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, V, s);
+                        S, s);
+    return fwd_f32(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, V, S,
+                   s);
 }
 
 int dtp_fwd_prefill(const dtp_config* cfg, const void* packed, size_t packed_bytes,
@@ -598,6 +651,35 @@ int dtp_fwd_prefill_varlen(const dtp_config* cfg, const void* packed, size_t pac
     if (n_seq > (1 << 20)) return fail(DTP_ERR_UNSUPPORTED, "n_seq > 2^20");
     return fwd_checked(cfg, packed, packed_bytes, tokens, total, *out, workspace, ws_bytes, false,
                        stream, n_seq, cu_seqlens);
+}
+
+size_t dtp_kv_state_size(const dtp_config* cfg, int max_T) {
+    if (validate_config(cfg) != DTP_OK || max_T <= 0) return 0;
+    return kv_state_layout(cfg, max_T).layer_bytes * (size_t)cfg->n_layer;
+}
+
+int dtp_fwd_prefill_chunk(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                          const uint32_t* tokens, int C, int p0, void* kv_state,
+                          size_t state_bytes, int max_T, const dtp_fwd_outputs* out,
+                          void* workspace, size_t ws_bytes, dtp_stream_t stream) {
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (!out) return fail(DTP_ERR_INVALID_ARG, "NULL outputs");
+    if (!kv_state) return fail(DTP_ERR_INVALID_ARG, "NULL kv_state");
+    if (out->k_cache || out->v_cache)
+        return fail(DTP_ERR_INVALID_ARG, "chunked prefill: k_cache/v_cache must be NULL");
+    if (C <= 0 || p0 < 0 || max_T <= 0 || (long long)p0 + C > max_T)
+        return fail(DTP_ERR_INVALID_ARG, "chunk [%d, %d + %d) outside 0..max_T = %d", p0, p0, C,
+                    max_T);
+    if (!aligned(kv_state, 256)) return fail(DTP_ERR_INVALID_ARG, "kv_state must be 256-byte aligned");
+    KvState S = kv_state_layout(cfg, max_T);
+    const size_t need = S.layer_bytes * (size_t)cfg->n_layer;
+    if (state_bytes < need)
+        return fail(DTP_ERR_WORKSPACE, "kv_state %zu < %zu bytes", state_bytes, need);
+    S.base = (uint8_t*)kv_state;
+    S.p0 = p0;
+    return fwd_checked(cfg, packed, packed_bytes, tokens, C, *out, workspace, ws_bytes, false,
+                       stream, 0, nullptr, S);
 }
 
 int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packed_bytes,

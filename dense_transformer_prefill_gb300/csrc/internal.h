@@ -58,12 +58,12 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype,
 cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
                                 const int32_t* pos, int T, int n_heads, int head_dim,
                                 int rope_dims, float freq_base, float eps, cudaStream_t s,
-                                int head_stride = 0);
+                                int head_stride = 0, int pos0 = 0);
 // attn[t, h*hd + e] *= sigmoid(gate[t * ldg + h*gstride + e]) (float32)
 cudaError_t launch_gate_mul_f32(float* attn, int lda, const float* gate, int ldg, int gstride,
                                 int T, int n_head, int head_dim, cudaStream_t s);
 cudaError_t launch_rope_table(float2* tab, int T, int rope_dims, float freq_base,
-                              cudaStream_t s);
+                              cudaStream_t s, int pos0 = 0);
 cudaError_t launch_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
                           cudaStream_t s);
 cudaError_t launch_swiglu_interleaved64(const float* gu, float* act, int T, int F,
@@ -79,7 +79,7 @@ cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, con
                              int ldv, int v_t, void* out, int ldo, int dtype, int T,
                              int n_head, int n_head_kv, int head_dim, float scale,
                              cudaStream_t s, const int* tok_pos = nullptr,
-                             int q_head_stride = 0);
+                             int q_head_stride = 0, int q_pos0 = 0);
 // Per-sequence schedule for packed sequences: tile_start [n_seq+1] (prefix of
 // ceil(len/128)), vcol_start [n_seq] (prefix of len rounded up to 8),
 // last_row [n_seq] (cu[b+1]-1); then per-token tok_pos / tok_vcol [total].
@@ -143,6 +143,9 @@ cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
 // Several sequences packed along the token axis (see seq_meta in simt.cu).
 struct AttnVarlen {
     const __nv_bfloat16* gate = nullptr;   // optional [T, n_head*hd]: out *= sigmoid(gate)
+    // one sequence: the T queries sit at positions p0 .. p0+T-1 and k / v^T hold
+    // keys 0 .. p0+T-1 (chunked prefill against a KV state)
+    int p0 = 0;
     int n_seq = 0;
     const int* cu_seqlens = nullptr;   // [n_seq + 1]
     const int* tile_start = nullptr;   // [n_seq + 1]

@@ -201,18 +201,21 @@ __device__ __forceinline__ float2 rope_cs(double pos, int i, int rope_dims, doub
     return make_float2((float)cs, (float)sn);
 }
 
-__global__ void rope_table_kernel(float2* tab, int T, int half, int rope_dims, double base) {
+// row t of the table holds position pos0 + t
+__global__ void rope_table_kernel(float2* tab, int T, int half, int rope_dims, double base,
+                                  int pos0) {
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= T * half) return;
     const int t = idx / half, i = idx % half;
-    tab[idx] = rope_cs((double)t, i, rope_dims, base);
+    tab[idx] = rope_cs((double)(pos0 + t), i, rope_dims, base);
 }
 
 cudaError_t launch_rope_table(float2* tab, int T, int rope_dims, float freq_base,
-                              cudaStream_t s) {
+                              cudaStream_t s, int pos0) {
     LaunchScope ls(DTP_K_OTHER, s);
     const int half = rope_dims / 2, n = T * half;
-    rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(tab, T, half, rope_dims, (double)freq_base);
+    rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(tab, T, half, rope_dims, (double)freq_base,
+                                                      pos0);
     return cudaGetLastError();
 }
 
@@ -222,12 +225,13 @@ cudaError_t launch_rope_table(float2* tab, int T, int rope_dims, float freq_base
 template <typename Tx>
 __global__ void qk_norm_rope_kernel(Tx* __restrict__ x, int ld, const float* __restrict__ w,
                                     const int32_t* __restrict__ pos, int n_heads, int hd,
-                                    int rope_dims, double base, float eps, int head_stride) {
+                                    int rope_dims, double base, float eps, int head_stride,
+                                    int pos0) {
     extern __shared__ float sm[];
     const int t = blockIdx.x, half = rope_dims / 2;
     float2* cs = reinterpret_cast<float2*>(sm);                 // [half]
     float* rowbuf = sm + 2 * half;                              // [warps][hd]
-    const double p = pos ? (double)pos[t] : (double)t;
+    const double p = pos ? (double)pos[t] : (double)(pos0 + t);
     for (int i = threadIdx.x; i < half; i += blockDim.x) cs[i] = rope_cs(p, i, rope_dims, base);
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -265,7 +269,7 @@ __global__ void qk_norm_rope_kernel(Tx* __restrict__ x, int ld, const float* __r
 cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
                                 const int32_t* pos, int T, int n_heads, int head_dim,
                                 int rope_dims, float freq_base, float eps, cudaStream_t s,
-                                int head_stride) {
+                                int head_stride, int pos0) {
     LaunchScope ls(DTP_K_OTHER, s);
     if (head_stride <= 0) head_stride = head_dim;
     int warps = n_heads < 8 ? n_heads : 8;
@@ -273,11 +277,11 @@ cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
     if (dtype == DTP_BF16)
         qk_norm_rope_kernel<<<T, warps * 32, smem, s>>>((__nv_bfloat16*)x, ld, w_norm, pos,
                                                         n_heads, head_dim, rope_dims,
-                                                        (double)freq_base, eps, head_stride);
+                                                        (double)freq_base, eps, head_stride, pos0);
     else
         qk_norm_rope_kernel<<<T, warps * 32, smem, s>>>((float*)x, ld, w_norm, pos, n_heads,
                                                         head_dim, rope_dims, (double)freq_base,
-                                                        eps, head_stride);
+                                                        eps, head_stride, pos0);
     return cudaGetLastError();
 }
 
@@ -401,11 +405,14 @@ cudaError_t launch_gemm_simt(const float* x, int ldx, const float* W, void* y, i
 // forward.rs `e.sdpa_naive(q, k, v, attn, head_dim, n_head, n_head_kv, t, t,
 // scale, true)`: one warp per (query t, head i); keys in chunks of 32 (one
 // per lane), online softmax in float32 with expf.  kv head = i / (h / g).
+// Query row t sees keys k0 .. t + q_pos0: k0 = t - tok_pos[t] for packed
+// sequences, else 0; q_pos0 > 0 when the queries follow q_pos0 earlier keys
+// held in k / v (chunked prefill).
 template <typename T, bool VT>
 __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __restrict__ k,
                                  int ldk, const T* __restrict__ v, int ldv, T* __restrict__ out,
                                  int ldo, int Tn, int n_head, int n_head_kv, int hd, float scale,
-                                 const int* __restrict__ tok_pos, int q_head_stride) {
+                                 const int* __restrict__ tok_pos, int q_head_stride, int q_pos0) {
     extern __shared__ float sm[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -422,10 +429,11 @@ __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __re
     for (int j = 0; j < MAXD; ++j) acc[j] = 0.f;
     float m = -INFINITY, l = 0.f;
     const int k0 = tok_pos ? t - tok_pos[t] : 0;       // first key of this query's sequence
-    for (int s0 = k0; s0 <= t; s0 += 32) {
+    const int kl = tok_pos ? t : t + q_pos0;            // last key it sees
+    for (int s0 = k0; s0 <= kl; s0 += 32) {
         const int s = s0 + lane;
         float sc = -INFINITY;
-        if (s <= t) {
+        if (s <= kl) {
             const T* kr = k + (size_t)s * ldk + (size_t)kvh * hd;
             float dot = 0.f;
             for (int e = 0; e < hd; ++e) dot = fmaf(qs[e], ld_elt(kr, e), dot);
@@ -434,11 +442,11 @@ __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __re
         const float mc = warp_max(sc);
         const float mn = fmaxf(m, mc);
         const float alpha = expf(m - mn);     // m = -inf on the first chunk -> 0
-        const float p = (s <= t) ? expf(sc - mn) : 0.f;
+        const float p = (s <= kl) ? expf(sc - mn) : 0.f;
         l = l * alpha + warp_sum(p);
 #pragma unroll
         for (int j = 0; j < MAXD; ++j) acc[j] *= alpha;
-        const int nk = min(32, t - s0 + 1);
+        const int nk = min(32, kl - s0 + 1);
         for (int jj = 0; jj < nk; ++jj) {
             const float pj = __shfl_sync(0xffffffffu, p, jj);
             const int sk = s0 + jj;
@@ -465,7 +473,8 @@ __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __re
 cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, const void* v,
                              int ldv, int v_t, void* out, int ldo, int dtype, int T,
                              int n_head, int n_head_kv, int head_dim, float scale,
-                             cudaStream_t s, const int* tok_pos, int q_head_stride) {
+                             cudaStream_t s, const int* tok_pos, int q_head_stride,
+                             int q_pos0) {
     LaunchScope ls(DTP_K_ATTN, s);
     if (q_head_stride <= 0) q_head_stride = head_dim;
     const int warps = 4;
@@ -476,20 +485,20 @@ cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, con
         if (v_t)
             attn_simt_kernel<B, true><<<grid, warps * 32, smem, s>>>(
                 (const B*)q, ldq, (const B*)k, ldk, (const B*)v, ldv, (B*)out, ldo, T, n_head,
-                n_head_kv, head_dim, scale, tok_pos, q_head_stride);
+                n_head_kv, head_dim, scale, tok_pos, q_head_stride, q_pos0);
         else
             attn_simt_kernel<B, false><<<grid, warps * 32, smem, s>>>(
                 (const B*)q, ldq, (const B*)k, ldk, (const B*)v, ldv, (B*)out, ldo, T, n_head,
-                n_head_kv, head_dim, scale, tok_pos, q_head_stride);
+                n_head_kv, head_dim, scale, tok_pos, q_head_stride, q_pos0);
     } else {
         if (v_t)
             attn_simt_kernel<float, true><<<grid, warps * 32, smem, s>>>(
                 (const float*)q, ldq, (const float*)k, ldk, (const float*)v, ldv, (float*)out,
-                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos, q_head_stride);
+                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos, q_head_stride, q_pos0);
         else
             attn_simt_kernel<float, false><<<grid, warps * 32, smem, s>>>(
                 (const float*)q, ldq, (const float*)k, ldk, (const float*)v, ldv, (float*)out,
-                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos, q_head_stride);
+                ldo, T, n_head, n_head_kv, head_dim, scale, tok_pos, q_head_stride, q_pos0);
     }
     return cudaGetLastError();
 }

@@ -184,6 +184,36 @@ int dtp_fwd_prefill_varlen(const dtp_config* cfg, const void* packed, size_t pac
                            const dtp_fwd_outputs* out, void* workspace, size_t ws_bytes,
                            dtp_stream_t stream);
 
+/* Chunked prefill of one sequence against a growing KV state.  The forward.rs
+ * `Model::forward` pass is causal, so positions p0 .. p0+C-1 depend on the
+ * earlier positions only through every layer's keys and values (after QK-norm
+ * and RoPE).  A call processes the C tokens at those positions, reading the
+ * keys and values of positions 0 .. p0-1 from `kv_state` (left there by the
+ * earlier calls) and writing its own; the chunks' logits, concatenated, equal
+ * the logits of one dtp_fwd_prefill over the whole sequence.
+ *
+ * KV state (device, caller-owned, 256-byte aligned, dtp_kv_state_size bytes
+ * for up to max_T positions; nk = n_head_kv*head_dim): per layer l, at byte
+ * offset l * S with S the per-layer stride below,
+ *   DTP_PREC_BF16: K  bf16 [max_T, nk] token-major, then (256-byte aligned)
+ *                  V^T bf16 [nk, ldvt], ldvt = max_T rounded up to 8
+ *   DTP_PREC_F32:  K  f32 [max_T, nk], then (256-byte aligned) V f32 [max_T, nk]
+ * Positions >= p0 + C are neither read nor written.  Calls on one state run
+ * in position order (the stream orders them).
+ *   tokens     device uint32 [C]
+ *   p0, C      p0 >= 0, C >= 1, p0 + C <= max_T
+ *   out        logits ([C, n_vocab], or the last position's with last_only) and
+ *              hidden ([n_layer + 1, C, n_embd]); k_cache / v_cache must be NULL
+ *              (the state holds them)
+ *   workspace  >= dtp_workspace_size(cfg, C) bytes
+ * Errors: DTP_ERR_INVALID_ARG for a range or pointer problem, DTP_ERR_WORKSPACE
+ * for a short state or workspace; nothing is enqueued then. */
+size_t dtp_kv_state_size(const dtp_config* cfg, int max_T);
+int dtp_fwd_prefill_chunk(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                          const uint32_t* tokens, int C, int p0, void* kv_state,
+                          size_t state_bytes, int max_T, const dtp_fwd_outputs* out,
+                          void* workspace, size_t ws_bytes, dtp_stream_t stream);
+
 /* Bytes of device workspace dtp_fwd_prefill_host needs (the forward workspace
  * plus device staging for the tokens and logits). */
 size_t dtp_workspace_size_host(const dtp_config* cfg, int T);

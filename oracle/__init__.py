@@ -22,6 +22,7 @@ invariants, brute force on tiny inputs, library routines in float64).
 from .model import (  # noqa: F401
     argmax,
     forward,
+    forward_chunk,
     forward_layer,
     linear,
     prime_gate_verdict,

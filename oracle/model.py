@@ -20,6 +20,10 @@ sites, not their bodies):
     `mul`): the Q projection yields, per head, head_dim q values followed by
     head_dim gate values; the attention output is multiplied elementwise by
     sigmoid(gate) before the O projection.
+  * Chunked prefill (the pages' "growing KV" reading of the causal pass): a
+    chunk at positions p0 .. p0+C-1 attends to the keys/values of positions
+    0 .. p0-1 kept from earlier chunks, then to its own; its logits are the
+    full pass's rows p0 .. p0+C-1.
   * bf16-operand mode: matrices are rounded to bf16 once; every GEMM input
     activation (normed h, attention output, SwiGLU act, final normed x) and the
     q/k/v handed to attention are rounded to bf16 (nearest, ties to even); all
@@ -96,14 +100,18 @@ def rope_neox(x, pos, n_heads: int, head_dim: int, n_dims: int, freq_base: float
 
 
 def sdpa_causal_gqa(q, k, v, n_head: int, n_head_kv: int, head_dim: int, scale: float,
-                    rows=None) -> np.ndarray:
+                    rows=None, p0: int = 0) -> np.ndarray:
     """forward.rs, Model::forward, `e.sdpa_naive(q, k, v, attn, head_dim,
     n_head, n_head_kv, t, t, scale, true)` with scale = 1/sqrt(head_dim):
     out[t, head i] = sum_{s <= t} softmax_s(q[t,i] . k[s,j] * scale) v[s,j],
     j = i // (n_head / n_head_kv).  q [T, n_head*hd], k/v [T, n_head_kv*hd].
 
-    `rows` (optional) restricts the output to those query positions; each row
-    is computed from the keys 0..row only, exactly as in the full result."""
+    `rows` (optional) restricts the output to those query rows; each row
+    is computed from the keys 0..row only, exactly as in the full result.
+
+    p0 > 0: the query rows sit at positions p0, p0+1, ... and k/v hold the keys
+    of positions 0 .. p0+T-1 (the earlier positions first), so query row r
+    sees keys 0 .. p0+r: one chunk of a chunked prefill."""
     q = np.asarray(q, dtype=F64)
     k = np.asarray(k, dtype=F64)
     v = np.asarray(v, dtype=F64)
@@ -111,9 +119,10 @@ def sdpa_causal_gqa(q, k, v, n_head: int, n_head_kv: int, head_dim: int, scale: 
     rows = np.arange(T) if rows is None else np.asarray(rows)
     group = n_head // n_head_kv
     out = np.zeros((len(rows), n_head * head_dim), dtype=F64)
-    n_keys = int(rows.max()) + 1 if len(rows) else 0
+    qpos = rows + p0                                     # position of each query row
+    n_keys = int(qpos.max()) + 1 if len(rows) else 0
     key_idx = np.arange(n_keys)
-    hidden = key_idx[None, :] > rows[:, None]           # key s not visible to query t
+    hidden = key_idx[None, :] > qpos[:, None]           # key s not visible to query t
     for i in range(n_head):
         j = i // group
         qi = q[rows, i * head_dim:(i + 1) * head_dim]
@@ -157,10 +166,15 @@ def _mats(w: dict, bf16: bool) -> dict:
     return out
 
 
-def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=None) -> np.ndarray:
+def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=None,
+                  kv_prefix=None) -> np.ndarray:
     """One decoder layer, forward.rs `Model::forward` loop body, on the residual
     stream x [T, n_embd]; returns the new x.  If `kv_out` is a list, the layer's
-    attention inputs (k after QK-norm and RoPE, and v) are appended to it."""
+    attention inputs (k after QK-norm and RoPE, and v) are appended to it.
+
+    `kv_prefix` = (k, v) of the p0 positions before x (which then sits at
+    positions pos = p0 .. p0+T-1): attention runs over those keys followed by
+    x's own, the only way earlier positions reach later ones."""
     op = round_bf16 if bf16_operands else (lambda a: a)
     L = _mats(lw, bf16_operands)
     d, h, g, hd = cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim
@@ -182,7 +196,12 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     v = op(v)
     if kv_out is not None:
         kv_out.append((k, v))
-    attn = sdpa_causal_gqa(q, k, v, h, g, hd, scale)
+    p0 = 0
+    if kv_prefix is not None:
+        p0 = kv_prefix[0].shape[0]
+        k = np.concatenate([np.asarray(kv_prefix[0], dtype=F64), k])
+        v = np.concatenate([np.asarray(kv_prefix[1], dtype=F64), v])
+    attn = sdpa_causal_gqa(q, k, v, h, g, hd, scale, p0=p0)
     if gate is not None:
         attn = attn / (1.0 + np.exp(-gate))          # attn * sigmoid(gate)
     attn = op(attn)
@@ -227,6 +246,39 @@ def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidd
     if return_hidden:
         return logits, np.stack(hidden)
     return logits
+
+
+def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: bool = False):
+    """Chunked prefill: logits [C, n_vocab] for the next C tokens of a sequence
+    whose first p0 positions went through earlier calls.  forward.rs
+    `Model::forward` is causal, so those positions reach these only through
+    each layer's keys and values: kv_state holds, per layer, the (k, v) of
+    positions 0..p0-1 (empty list on the first chunk) and is extended in place
+    with this chunk's.  The chunks' logits, concatenated, are forward(tokens)'s."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    C = tokens.shape[0]
+    op = round_bf16 if bf16_operands else (lambda a: a)
+    first = len(kv_state) == 0
+    p0 = 0 if first else kv_state[0][0].shape[0]
+    x = np.asarray(weights["tok_embd"], dtype=F64)[tokens]
+    if bf16_operands:
+        x = round_bf16(x)
+    pos = p0 + np.arange(C)
+    for l in range(cfg.n_layer):
+        new = []
+        prefix = None if first else kv_state[l]
+        x = forward_layer(cfg, weights["layers"][l], x, pos, bf16_operands, new, prefix)
+        k, v = new[0]
+        if first:
+            kv_state.append((k, v))
+        else:
+            kv_state[l] = (np.concatenate([kv_state[l][0], k]),
+                           np.concatenate([kv_state[l][1], v]))
+    hn = op(rms_norm(x, np.asarray(weights["output_norm"], dtype=F64), cfg.rms_eps))
+    W_out = np.asarray(weights["output"], dtype=F64)
+    if bf16_operands:
+        W_out = round_bf16(W_out)
+    return linear(hn, W_out)
 
 
 # --------------------------------------------------------------------------------------

@@ -87,3 +87,36 @@ def test_host_side_rejections(dtp):
                                     ctypes.byref(outs), fake, 1 << 40, None) == -1
     assert L.dtp_fwd_prefill_varlen(ctypes.byref(c), fake, 1 << 40, fake, fake, 0, 256,
                                     ctypes.byref(outs), fake, 1 << 40, None) == -1
+
+
+def test_chunk_state_size_and_rejections(dtp):
+    """dtp_kv_state_size follows the documented layout; dtp_fwd_prefill_chunk
+    rejects bad ranges and buffers before enqueueing anything."""
+    L = dtp.lib()
+    up = lambda x, a: (x + a - 1) // a * a
+    for prec in ("bf16", "f32"):
+        cfg = synth.CONFIGS["small"].replace(precision=prec)
+        c = dtp.config_from(cfg)
+        nk = cfg.n_head_kv * cfg.head_dim
+        for max_T in (1, 100, 256, 4099):
+            if prec == "bf16":
+                per = up(max_T * nk * 2, 256) + up(nk * up(max_T, 8) * 2, 256)
+            else:
+                per = 2 * up(max_T * nk * 4, 256)
+            assert dtp.kv_state_size(c, max_T) == cfg.n_layer * per
+        assert dtp.kv_state_size(c, 0) == 0
+    c = _cfg(dtp)
+    fake = ctypes.c_void_p(0x10000)   # never dereferenced
+    big = 1 << 40
+    outs = dtp._binding.FwdOutputs(0x10000, 0, None, None, None)
+    call = lambda C, p0, max_T, sb=big, o=outs, st=fake: L.dtp_fwd_prefill_chunk(
+        ctypes.byref(c), fake, big, fake, C, p0, st, sb, max_T, ctypes.byref(o), fake, big, None)
+    assert call(0, 0, 64) == -1                      # empty chunk
+    assert call(16, -1, 64) == -1                    # negative start
+    assert call(16, 50, 64) == -1                    # runs past max_T
+    assert "max_T" in dtp.last_error()
+    assert call(16, 0, 64, st=None) == -1
+    assert call(16, 0, 64, st=ctypes.c_void_p(0x10010)) == -1      # not 256-byte aligned
+    assert call(16, 0, 64, sb=dtp.kv_state_size(c, 64) - 1) == -4   # short state
+    kv = dtp._binding.FwdOutputs(0x10000, 0, None, 0x10000, None)
+    assert call(16, 0, 64, o=kv) == -1               # the state is the cache

@@ -287,3 +287,104 @@ def test_gated_attention(dtp, prec):
     _, gl, gh = run_gpu(dtp, cfg, T=200)
     _, rl, rh = oracle_forward(cfg, T=200)
     assert_parity(cfg.replace(T=200), gl, gh, rl, rh)
+
+
+def _run_chunks(dtp, m, cfg, toks, plan, max_T, state=None, last_only=False):
+    """dtp_fwd_prefill_chunk over consecutive chunks of `toks`; the KV state
+    starts filled with NaN bytes, so reading a position no chunk has written
+    yet (or one past the current chunk) poisons the result."""
+    L = cfg.n_layer
+    if state is None:
+        state = torch.full((dtp.kv_state_size(m.c, max_T),), 0xFF, dtype=torch.uint8, device=dev)
+    logits, hidden, p0 = [], [], 0
+    for C in plan:
+        t = torch.as_tensor(toks[p0:p0 + C].astype(np.int32), device=dev)
+        lg = torch.empty((1 if last_only else C, cfg.n_vocab), dtype=torch.float32, device=dev)
+        hd = torch.empty((L + 1, C, cfg.n_embd), dtype=torch.float32, device=dev)
+        dtp.fwd_prefill_chunk(m.c, m.packed, t, p0, state, max_T, m.workspace(C), logits=lg,
+                              last_only=last_only, hidden=hd)
+        logits.append(lg)
+        hidden.append(hd)
+        p0 += C
+    torch.cuda.synchronize()
+    dtp.check()
+    return (torch.cat(logits).cpu().numpy(), torch.cat(hidden, dim=1).cpu().numpy(), state)
+
+
+CHUNK_PLANS = [(256, 256, 88), (100, 300, 200), (1, 598, 1), (600,)]
+
+
+@pytest.mark.parametrize("prec", ["f32", "bf16"])
+@pytest.mark.parametrize("plan", CHUNK_PLANS)
+def test_chunked_prefill(dtp, prec, plan):
+    """dtp_fwd_prefill_chunk: positions p0..p0+C-1 against the KV state of the
+    earlier chunks.  The concatenated logits and hidden states meet the oracle's
+    whole-pass bars, and equal this library's own whole pass exactly (every row
+    is computed by the same arithmetic whatever rows share its tiles)."""
+    T = 600
+    cfg = synth.CONFIGS["small"].replace(precision=prec, n_layer=2, T=T)
+    m = load_model(dtp, cfg)
+    toks = synth.tokens(cfg, 0, T)
+    gl, gh, _ = _run_chunks(dtp, m, cfg, toks, plan, max_T=T + 13)
+    assert np.isfinite(gl).all()
+    _, full_l, full_h = run_gpu(dtp, cfg, T=T, model=m)
+    np.testing.assert_array_equal(gl, full_l)
+    np.testing.assert_array_equal(gh, full_h)
+    if plan == CHUNK_PLANS[0]:
+        _, rl, rh = oracle_forward(cfg, T=T)
+        assert_parity(cfg, gl, gh, rl, rh)
+
+
+@pytest.mark.parametrize("prec", ["f32", "bf16"])
+def test_chunked_prefill_state_is_the_kv_cache(dtp, prec):
+    """After the chunks, the state holds every layer's K (and V, transposed in
+    bf16) exactly as dtp_fwd_prefill_ex's KV outputs of the whole pass."""
+    T, max_T = 300, 307
+    cfg = synth.CONFIGS["small"].replace(precision=prec, n_layer=2, T=T)
+    m = load_model(dtp, cfg)
+    toks = synth.tokens(cfg, 0, T)
+    state = torch.zeros((dtp.kv_state_size(m.c, max_T),), dtype=torch.uint8, device=dev)
+    # the first chunks extend the state only (no outputs), the last gives logits
+    t = lambda a, b: torch.as_tensor(toks[a:b].astype(np.int32), device=dev)
+    dtp.fwd_prefill_chunk(m.c, m.packed, t(0, 130), 0, state, max_T, m.workspace(130))
+    dtp.fwd_prefill_chunk(m.c, m.packed, t(130, 170), 130, state, max_T, m.workspace(40))
+    last = torch.empty((1, cfg.n_vocab), dtype=torch.float32, device=dev)
+    dtp.fwd_prefill_chunk(m.c, m.packed, t(170, T), 170, state, max_T, m.workspace(T - 170),
+                          logits=last, last_only=True)
+    L, nk = cfg.n_layer, cfg.n_head_kv * cfg.head_dim
+    cdt = torch.float32 if prec == "f32" else torch.bfloat16
+    kc = torch.empty((L, T, nk), dtype=cdt, device=dev)
+    vc = torch.empty((L, T, nk), dtype=cdt, device=dev)
+    full = torch.empty((T, cfg.n_vocab), dtype=torch.float32, device=dev)
+    dtp.fwd_prefill_ex(m.c, m.packed, t(0, T), m.workspace(T), logits=full, k_cache=kc, v_cache=vc)
+    torch.cuda.synchronize()
+    dtp.check()
+    assert torch.equal(last[0], full[-1])
+    eb = 4 if prec == "f32" else 2
+    up = lambda x, a: (x + a - 1) // a * a
+    k_bytes = up(max_T * nk * eb, 256)
+    per = dtp.kv_state_size(m.c, max_T) // L
+    for l in range(L):
+        lay = state[l * per:(l + 1) * per]
+        ks = lay[:max_T * nk * eb].view(cdt).view(max_T, nk)
+        assert torch.equal(ks[:T], kc[l])
+        if prec == "f32":
+            vs = lay[k_bytes:k_bytes + max_T * nk * 4].view(cdt).view(max_T, nk)
+            assert torch.equal(vs[:T], vc[l])
+        else:
+            ldvt = up(max_T, 8)
+            vt = lay[k_bytes:k_bytes + nk * ldvt * 2].view(cdt).view(nk, ldvt)
+            assert torch.equal(vt[:, :T].t(), vc[l])
+
+
+def test_chunked_prefill_head_dim_128_gated(dtp):
+    """The head_dim-128 attention kernel and the gated Q projection under chunking."""
+    T = 333
+    cfg = synth.CONFIGS["qwen3-0.6b-shape"].replace(n_layer=2, T=T, n_vocab=4096, attn_gate=True)
+    m = load_model(dtp, cfg)
+    toks = synth.tokens(cfg, 0, T)
+    gl, gh, _ = _run_chunks(dtp, m, cfg, toks, (129, 127, 77), max_T=T)
+    _, full_l, full_h = run_gpu(dtp, cfg, T=T, model=m)
+    np.testing.assert_array_equal(gl, full_l)
+    _, rl, rh = oracle_forward(cfg, T=T)
+    assert_parity(cfg, gl, gh, rl, rh)

@@ -432,3 +432,56 @@ def test_planted_gate_layout_swap_is_caught(monkeypatch):
         return real(cfg, lw, x, pos, bf16_operands, kv_out)
     monkeypatch.setattr(om, "forward_layer", wrong)
     assert _pins_fail(test_gated_attention_zero_gate_halves_attention)
+
+
+# ---------------------------------------------------------------- chunked prefill
+def _chunked(cfg, w, toks, sizes, bf16=False):
+    state, outs, p = [], [], 0
+    for c in sizes:
+        outs.append(oracle.forward_chunk(cfg, w, toks[p:p + c], state, bf16_operands=bf16))
+        p += c
+    return np.concatenate(outs), state
+
+
+@pytest.mark.parametrize("sizes", [(16,), (5, 7, 4), (1, 1, 14), (15, 1)])
+def test_forward_chunk_concatenates_to_the_full_pass(tiny_weights, sizes):
+    """Causality: the chunks' logits are the whole pass's rows, and the state
+    ends up holding every layer's (k, v) of the whole pass."""
+    toks = synth.tokens(TINY)
+    kv = []
+    full = oracle.forward(TINY, tiny_weights, toks, kv_out=kv)
+    got, state = _chunked(TINY, tiny_weights, toks, sizes)
+    np.testing.assert_allclose(got, full, rtol=1e-11, atol=1e-13)
+    assert len(state) == TINY.n_layer
+    for (k, v), (k2, v2) in zip(state, kv):
+        np.testing.assert_allclose(k, k2, rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(v, v2, rtol=1e-11, atol=1e-13)
+
+
+def test_forward_chunk_bf16_mode_concatenates(tiny_weights):
+    toks = synth.tokens(TINY)
+    full = oracle.forward(TINY, tiny_weights, toks, bf16_operands=True)
+    got, _ = _chunked(TINY, tiny_weights, toks, (6, 10), bf16=True)
+    # same values rounded the same way; only BLAS summation order may differ
+    assert np.linalg.norm(got - full) / np.linalg.norm(full) < 1e-2
+
+
+def test_sdpa_offset_equals_row_subset():
+    a = synth.attention_inputs(24, 4, 2, 8, seed=3)
+    q, k, v = a["q"], a["k"], a["v"]
+    full = oracle.sdpa_causal_gqa(q, k, v, 4, 2, 8, 0.3)
+    for p0 in (0, 1, 9, 23):
+        np.testing.assert_allclose(oracle.sdpa_causal_gqa(q[p0:], k, v, 4, 2, 8, 0.3, p0=p0),
+                                   full[p0:], rtol=1e-12, atol=1e-14)
+
+
+def test_planted_chunk_positions_restart_is_caught(monkeypatch, tiny_weights):
+    """A chunk that restarts RoPE positions at 0 (or masks from its own first
+    row) fails the concatenation pin."""
+    real = om.forward_layer
+
+    def wrong(cfg, lw, x, pos, bf16=False, kv_out=None, kv_prefix=None):
+        return real(cfg, lw, x, np.arange(len(pos)), bf16, kv_out, kv_prefix)
+    monkeypatch.setattr(om, "forward_layer", wrong)
+    assert _pins_fail(lambda: test_forward_chunk_concatenates_to_the_full_pass(tiny_weights,
+                                                                              (5, 7, 4)))
