@@ -9,8 +9,10 @@ from .build import build  # noqa: F401
 from ._binding import (  # noqa: F401
     DTP_BF16,
     DTP_F32,
+    DTP_TF32,
     DTP_PREC_BF16,
     DTP_PREC_F32,
+    DTP_PREC_TF32,
     KERNEL_KINDS,
     DtpError,
     Model,

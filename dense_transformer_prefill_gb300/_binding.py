@@ -11,8 +11,8 @@ import torch
 
 from .build import LIB, build  # noqa: F401
 
-DTP_F32, DTP_BF16 = 0, 1
-DTP_PREC_F32, DTP_PREC_BF16 = 0, 2
+DTP_F32, DTP_BF16, DTP_TF32 = 0, 1, 2
+DTP_PREC_F32, DTP_PREC_TF32, DTP_PREC_BF16 = 0, 1, 2
 KERNEL_KINDS = {"embed": 0, "rmsnorm": 1, "gemm_qkv": 2, "attn": 3, "gemm_o": 4,
                 "gemm_gateup": 5, "gemm_down": 6, "gemm_lmhead": 7, "other": 8}
 
@@ -136,11 +136,11 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def config_from(cfg) -> Config:
     """Config from an object/dict with the dtp_config field names; precision may be
-    "f32"/"bf16" or the DTP_PREC_* code."""
+    "f32"/"tf32"/"bf16" or the DTP_PREC_* code."""
     get = (lambda k: cfg[k]) if isinstance(cfg, dict) else (lambda k: getattr(cfg, k))
     prec = get("precision")
     if isinstance(prec, str):
-        prec = {"f32": DTP_PREC_F32, "bf16": DTP_PREC_BF16}[prec]
+        prec = {"f32": DTP_PREC_F32, "tf32": DTP_PREC_TF32, "bf16": DTP_PREC_BF16}[prec]
     try:
         gate = int(bool(get("attn_gate")))
     except (KeyError, AttributeError):
@@ -247,9 +247,12 @@ def check(stream=None) -> None:
     _ok(lib().dtp_check(_stream(stream)))
 
 
-def rms_norm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, eps: float, stream=None) -> None:
+def rms_norm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, eps: float, tf32: bool = False,
+             stream=None) -> None:
+    """tf32=True: float32 y rounded to tf32 (a tensor-core GEMM operand)."""
     rows, cols = x.shape
-    _ok(lib().dtp_rms_norm(x.data_ptr(), w.data_ptr(), y.data_ptr(), _dtype_code(y), rows, cols,
+    dt = DTP_TF32 if tf32 else _dtype_code(y)
+    _ok(lib().dtp_rms_norm(x.data_ptr(), w.data_ptr(), y.data_ptr(), dt, rows, cols,
                            eps, _stream(stream)))
 
 
@@ -277,10 +280,13 @@ def swiglu(gate, up, out, stream=None) -> None:
                          gate.numel(), _stream(stream)))
 
 
-def linear(x, W, y, residual=None, stream=None) -> None:
+def linear(x, W, y, residual=None, tf32: bool = False, stream=None) -> None:
+    """y = x W^T (+ residual).  tf32=True: float32 x and W holding tf32 values
+    go to the kind::tf32 tensor-core GEMM."""
     M, K = x.shape
     N = W.shape[0]
-    _ok(lib().dtp_linear(x.data_ptr(), W.data_ptr(), y.data_ptr(), _dtype_code(x), _dtype_code(y),
+    dt = DTP_TF32 if tf32 else _dtype_code(x)
+    _ok(lib().dtp_linear(x.data_ptr(), W.data_ptr(), y.data_ptr(), dt, _dtype_code(y),
                          M, N, K, _ptr(residual), _stream(stream)))
 
 

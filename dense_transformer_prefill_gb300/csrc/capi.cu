@@ -124,12 +124,15 @@ static int validate_config(const dtp_config* c) {
         return fail(DTP_ERR_INVALID_ARG, "rope_dim_count must be even and in [2, head_dim]");
     if (!(c->rms_eps >= 0.f) || !(c->rope_freq_base > 0.f))
         return fail(DTP_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_freq_base > 0");
-    if (c->precision != DTP_PREC_F32 && c->precision != DTP_PREC_BF16)
+    if (c->precision != DTP_PREC_F32 && c->precision != DTP_PREC_TF32 &&
+        c->precision != DTP_PREC_BF16)
         return fail(DTP_ERR_INVALID_ARG, "unknown precision %d", c->precision);
     if (c->attn_gate != 0 && c->attn_gate != 1)
         return fail(DTP_ERR_INVALID_ARG, "attn_gate must be 0 or 1");
     if (c->n_embd % 8 || c->n_ff % 64)
         return fail(DTP_ERR_UNSUPPORTED, "n_embd must be a multiple of 8 and n_ff of 64");
+    if (c->precision == DTP_PREC_TF32 && (c->n_head * c->head_dim) % 4)
+        return fail(DTP_ERR_UNSUPPORTED, "tf32 path: n_head*head_dim must be a multiple of 4");
     if (c->precision == DTP_PREC_BF16) {
         if (c->head_dim != 64 && c->head_dim != 128)
             return fail(DTP_ERR_UNSUPPORTED, "bf16 path: head_dim must be 64 or 128");
@@ -300,6 +303,20 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
     float* gu = (float*)(ws + W.gu);
     float* act = (float*)(ws + W.act);
     const float scale = 1.0f / sqrtf((float)hd);
+    // DTP_PREC_TF32: the GEMMs run on tcgen05 (kind::tf32) and each GEMM input is
+    // rounded to tf32 by the kernel that writes it; otherwise the SIMT GEMM
+    const bool tc = c->precision == DTP_PREC_TF32;
+    const int opd = tc ? DTP_TF32 : DTP_F32;
+    auto gemm = [&](const float* a, const float* w, float* y, int M, int N, int K,
+                    const float* res, int kind) -> cudaError_t {
+        if (!tc) return launch_gemm_simt(a, K, w, y, DTP_F32, N, M, N, K, res, s, kind);
+        GemmEpiArgs e;
+        e.y = y;
+        e.y_dtype = DTP_F32;
+        e.ldy = N;
+        e.residual = res;
+        return launch_gemm_tc_tf32(a, w, M, N, K, e, s, kind);
+    };
     if (V.n_seq)
         DTP_CUDA_CHECK(launch_seq_meta(V.cu, V.n_seq, T, V.tile_start, V.vcol_start, V.last_row,
                                        V.tok_pos, V.tok_vcol, T, s));
@@ -308,10 +325,10 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
         const uint8_t* lp = P + (size_t)l * L.layer_bytes;
         if (hidden)
             DTP_CUDA_CHECK(launch_copy_f32(x, hidden + (size_t)l * T * d, (size_t)T * d, s));
-        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.attn_norm), hb, DTP_F32, T, d,
+        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.attn_norm), hb, opd, T, d,
                                       c->rms_eps, s));
-        DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(lp + L.w_qkv), qkv, DTP_F32, nqkv,
-                                        T, nqkv, d, nullptr, s, DTP_K_GEMM_QKV));
+        DTP_CUDA_CHECK(gemm(hb, (const float*)(lp + L.w_qkv), qkv, T, nqkv, d, nullptr,
+                            DTP_K_GEMM_QKV));
         DTP_CUDA_CHECK(launch_qk_norm_rope(qkv, DTP_F32, nqkv, (const float*)(lp + L.q_norm),
                                            V.tok_pos, T, h, hd, c->rope_dim_count,
                                            c->rope_freq_base, c->rms_eps, s, qstride, S.p0));
@@ -340,34 +357,32 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
         }
         if (c->attn_gate)
             DTP_CUDA_CHECK(launch_gate_mul_f32(attn, nq, qkv + hd, nqkv, 2 * hd, T, h, hd, s));
-        DTP_CUDA_CHECK(launch_gemm_simt(attn, nq, (const float*)(lp + L.wo), x, DTP_F32, d, T, d,
-                                        nq, x, s, DTP_K_GEMM_O));
-        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.ffn_norm), hb, DTP_F32, T, d,
+        if (tc) DTP_CUDA_CHECK(launch_round_tf32(attn, (size_t)T * nq, s));
+        DTP_CUDA_CHECK(gemm(attn, (const float*)(lp + L.wo), x, T, d, nq, x, DTP_K_GEMM_O));
+        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.ffn_norm), hb, opd, T, d,
                                       c->rms_eps, s));
-        DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(lp + L.w_gu), gu, DTP_F32, 2 * F, T,
-                                        2 * F, d, nullptr, s, DTP_K_GEMM_GATEUP));
-        DTP_CUDA_CHECK(launch_swiglu_interleaved64(gu, act, T, F, s));
-        DTP_CUDA_CHECK(launch_gemm_simt(act, F, (const float*)(lp + L.w_down), x, DTP_F32, d, T, d,
-                                        F, x, s, DTP_K_GEMM_DOWN));
+        DTP_CUDA_CHECK(gemm(hb, (const float*)(lp + L.w_gu), gu, T, 2 * F, d, nullptr,
+                            DTP_K_GEMM_GATEUP));
+        DTP_CUDA_CHECK(launch_swiglu_interleaved64(gu, act, T, F, s, opd));
+        DTP_CUDA_CHECK(gemm(act, (const float*)(lp + L.w_down), x, T, d, F, x, DTP_K_GEMM_DOWN));
     }
     if (hidden)
         DTP_CUDA_CHECK(
             launch_copy_f32(x, hidden + (size_t)c->n_layer * T * d, (size_t)T * d, s));
     if (!logits) return DTP_OK;
     if (o.last_only && V.n_seq) {            // the last position of every sequence
-        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(P + L.output_norm), hb, DTP_F32, V.n_seq,
+        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(P + L.output_norm), hb, opd, V.n_seq,
                                       d, c->rms_eps, s, V.last_row));
-        DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(P + L.output), logits, DTP_F32,
-                                        c->n_vocab, V.n_seq, c->n_vocab, d, nullptr, s,
-                                        DTP_K_GEMM_LMHEAD));
+        DTP_CUDA_CHECK(gemm(hb, (const float*)(P + L.output), logits, V.n_seq, c->n_vocab, d,
+                            nullptr, DTP_K_GEMM_LMHEAD));
         return DTP_OK;
     }
     const int rows = o.last_only ? 1 : T;
     const float* xf = x + (size_t)(T - rows) * d;
-    DTP_CUDA_CHECK(launch_rmsnorm(xf, (const float*)(P + L.output_norm), hb, DTP_F32, rows, d,
+    DTP_CUDA_CHECK(launch_rmsnorm(xf, (const float*)(P + L.output_norm), hb, opd, rows, d,
                                   c->rms_eps, s));
-    DTP_CUDA_CHECK(launch_gemm_simt(hb, d, (const float*)(P + L.output), logits, DTP_F32,
-                                    c->n_vocab, rows, c->n_vocab, d, nullptr, s, DTP_K_GEMM_LMHEAD));
+    DTP_CUDA_CHECK(gemm(hb, (const float*)(P + L.output), logits, rows, c->n_vocab, d, nullptr,
+                        DTP_K_GEMM_LMHEAD));
     return DTP_OK;
 }
 
@@ -529,7 +544,10 @@ int dtp_pack_layer(const dtp_config* cfg, int layer, const dtp_layer_src* src, v
     if (!aligned(packed, 256)) return fail(DTP_ERR_INVALID_ARG, "packed must be 256-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     uint8_t* lp = (uint8_t*)packed + (size_t)layer * L.layer_bytes;
-    const int bf = cfg->precision == DTP_PREC_BF16;
+    // matrix storage type: bf16, float32, or float32 rounded to tf32
+    const int bf = cfg->precision == DTP_PREC_BF16   ? DTP_BF16
+                   : cfg->precision == DTP_PREC_TF32 ? DTP_TF32
+                                                     : DTP_F32;
     const int d = cfg->n_embd, hd = cfg->head_dim, nq = cfg->n_head * hd,
               nk = cfg->n_head_kv * hd, F = cfg->n_ff;
     const int nqc = nq * (1 + cfg->attn_gate);      // q rows (with the per-head gate rows)
@@ -561,9 +579,10 @@ int dtp_pack_globals(const dtp_config* cfg, const float* tok_embd, const float* 
     if (!aligned(packed, 256)) return fail(DTP_ERR_INVALID_ARG, "packed must be 256-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     uint8_t* P = (uint8_t*)packed;
-    const int bf = cfg->precision == DTP_PREC_BF16;
+    const int bf = cfg->precision == DTP_PREC_BF16 ? DTP_BF16 : DTP_F32;
+    const int mat = cfg->precision == DTP_PREC_TF32 ? DTP_TF32 : bf;    // tok_embd is no GEMM operand
     DTP_CUDA_CHECK(launch_pack_matrix(tok_embd, cfg->n_vocab, cfg->n_embd, P + L.tok_embd, bf, 0, s));
-    DTP_CUDA_CHECK(launch_pack_matrix(output, cfg->n_vocab, cfg->n_embd, P + L.output, bf, 0, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(output, cfg->n_vocab, cfg->n_embd, P + L.output, mat, 0, s));
     DTP_CUDA_CHECK(launch_pack_matrix(output_norm, 1, cfg->n_embd, P + L.output_norm, 0, 0, s));
     return DTP_OK;
 }
@@ -732,7 +751,8 @@ int dtp_rms_norm(const float* x, const float* w, void* y, int y_dtype, int rows,
                  float eps, dtp_stream_t stream) {
     if (!x || !w || !y) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
     if (rows <= 0 || cols <= 0) return fail(DTP_ERR_INVALID_ARG, "rows and cols must be >= 1");
-    if (y_dtype != DTP_F32 && y_dtype != DTP_BF16) return fail(DTP_ERR_INVALID_ARG, "bad y_dtype");
+    if (y_dtype != DTP_F32 && y_dtype != DTP_BF16 && y_dtype != DTP_TF32)
+        return fail(DTP_ERR_INVALID_ARG, "bad y_dtype");
     if (!(eps >= 0.f)) return fail(DTP_ERR_INVALID_ARG, "eps must be >= 0");
     if ((cols % 4 == 0) && (!aligned(x, 16) || !aligned(w, 16)))
         return fail(DTP_ERR_INVALID_ARG, "x and w must be 16-byte aligned");
@@ -809,11 +829,26 @@ int dtp_linear(const void* x, const void* W, void* y, int dtype, int y_dtype, in
                const float* residual, dtp_stream_t stream) {
     if (!x || !W || !y) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
     if (M <= 0 || N <= 0 || K <= 0) return fail(DTP_ERR_INVALID_ARG, "M, N, K must be >= 1");
-    if ((dtype != DTP_F32 && dtype != DTP_BF16) || (y_dtype != DTP_F32 && y_dtype != DTP_BF16))
+    if ((dtype != DTP_F32 && dtype != DTP_BF16 && dtype != DTP_TF32) ||
+        (y_dtype != DTP_F32 && y_dtype != DTP_BF16))
         return fail(DTP_ERR_INVALID_ARG, "bad dtype");
     if (residual && y_dtype != DTP_F32)
         return fail(DTP_ERR_INVALID_ARG, "a residual needs a float32 output");
     cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == DTP_TF32) {
+        if (y_dtype != DTP_F32) return fail(DTP_ERR_INVALID_ARG, "tf32 linear: y must be float32");
+        if (K % 4) return fail(DTP_ERR_UNSUPPORTED, "tf32 linear: K must be a multiple of 4");
+        if (!aligned(x, 16) || !aligned(W, 16))
+            return fail(DTP_ERR_INVALID_ARG, "tf32 linear: x and W must be 16-byte aligned");
+        GemmEpiArgs e;
+        e.y = y;
+        e.y_dtype = DTP_F32;
+        e.ldy = N;
+        e.residual = residual;
+        DTP_CUDA_CHECK(launch_gemm_tc_tf32((const float*)x, (const float*)W, M, N, K, e, s,
+                                           DTP_K_OTHER));
+        return DTP_OK;
+    }
     if (dtype == DTP_F32) {
         DTP_CUDA_CHECK(launch_gemm_simt((const float*)x, K, (const float*)W, y, y_dtype, N, M, N, K,
                                         residual, s, DTP_K_OTHER));

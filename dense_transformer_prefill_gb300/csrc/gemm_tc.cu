@@ -6,9 +6,11 @@
 //   EPI_QKV     per-head QK-RMSNorm + NeoX RoPE on q and k, v stored transposed
 //   EPI_SWIGLU  silu(gate) * up on the interleaved gate/up product (`ffn_act`)
 //
-// D[M, N] = A[M, K] B[N, K]^T with A = activations, B = weights, both bf16 and
+// D[M, N] = A[M, K] B[N, K]^T with A = activations, B = weights, both bf16 (or
+// both float32 holding tf32 values: kind::tf32, EPI_STORE only) and
 // K-contiguous.  One persistent CTA per SM walks 128 x BN output tiles:
-//   warp 0      TMA producer: 128x64 A and BNx64 B boxes (128-byte swizzle) into
+//   warp 0      TMA producer: 128x64 A and BNx64 B boxes (128-byte swizzle; 32
+//               elements of K per 128-byte row for tf32) into
 //               a STAGES-deep shared-memory ring (mbarrier full/empty pairs)
 //   warp 1      one thread issues tcgen05.mma (M=128, N=BN, K=16) into a TMEM
 //               accumulator; two accumulators (2*BN columns) so the epilogue of
@@ -550,7 +552,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
 }
 
 // ----------------------------------------------------------------------------- kernel
-template <int BN, int EPI>
+template <int BN, int EPI, bool TF = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmY2,
@@ -619,8 +621,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            ERRBIT_TIMEOUT))
                         goto producer_done;
                     ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    ptx::tma_load_2d(&tmA, &full[stage], sA + stage * C::A_BYTES, kb * BK, mb * BM);
-                    ptx::tma_load_2d(&tmB, &full[stage], sB + stage * C::B_BYTES, kb * BK, nb * BN);
+                    // a stage holds 128 bytes of K per row: 64 bf16 or 32 tf32
+                    const int k0 = kb * (TF ? BK / 2 : BK);
+                    ptx::tma_load_2d(&tmA, &full[stage], sA + stage * C::A_BYTES, k0, mb * BM);
+                    ptx::tma_load_2d(&tmB, &full[stage], sB + stage * C::B_BYTES, k0, nb * BN);
                     ++issued;
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -646,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+            const uint32_t idesc = TF ? ptx::idesc_tf32_f32(BM, BN) : ptx::idesc_bf16_f32(BM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -667,10 +671,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const uint64_t adesc = ptx::sdesc_sw128(ptx::smem_u32(sA + stage * C::A_BYTES));
                     const uint64_t bdesc = ptx::sdesc_sw128(ptx::smem_u32(sB + stage * C::B_BYTES));
+                    // four MMAs per stage, each 32 bytes further along K (+2 in
+                    // the descriptor's 16-byte address units)
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        ptx::umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                                          (kb > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if constexpr (TF)
+                            ptx::umma_tf32_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                              (kb > 0 || kk > 0) ? 1u : 0u);
+                        else
+                            ptx::umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                              (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
                     ptx::umma_commit(&empty[stage]);
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -755,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool TF = false>
 cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                         const CUtensorMap& ty2, const CUtensorMap& tr, const Params& p,
                         cudaStream_t s) {
@@ -763,14 +774,14 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, TF>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::SMEM_BYTES, s>>>(ta, tb, ty, ty2, tr, p);
+    gemm_tc_kernel<BN, EPI, TF><<<grid, kThreads, C::SMEM_BYTES, s>>>(ta, tb, ty, ty2, tr, p);
     return cudaGetLastError();
 }
 
@@ -790,21 +801,25 @@ static int pick_bn(int M, int N, GemmEpi epi, int y_dtype) {
     return 20 * cost(224) < 19 * cost(256) ? 224 : 256;
 }
 
-cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,
-                           GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind) {
-    const int BN = pick_bn(M, N, epi, ea.y_dtype);
+static cudaError_t launch_gemm(const void* x, const void* W, bool tf32, int M, int N, int K,
+                               GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind) {
+    int BN = pick_bn(M, N, epi, ea.y_dtype);
+    if (tf32 && BN == 224) BN = 256;         // tf32 instantiates the 256 and 128 tiles only
+    // operand boxes: 128 bytes of K per row (64 bf16 or 32 float32)
+    const int bke = tf32 ? BK / 2 : BK;
+    const CUtensorMapDataType odt =
+        tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int oeb = tf32 ? 4 : 2;
     CUtensorMap ta, tb;
-    if (!make_tmap_2d(&ta, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, K, BM, BK))
-        return cudaErrorInvalidValue;
-    if (!make_tmap_2d(&tb, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, K, BN, BK))
-        return cudaErrorInvalidValue;
+    if (!make_tmap_2d(&ta, x, odt, oeb, M, K, K, BM, bke)) return cudaErrorInvalidValue;
+    if (!make_tmap_2d(&tb, W, odt, oeb, N, K, K, BN, bke)) return cudaErrorInvalidValue;
     Params p;
     p.M = M;
     p.N = N;
     p.K = K;
     p.tiles_m = (M + BM - 1) / BM;
     p.tiles_n = (N + BN - 1) / BN;
-    p.num_kb = (K + BK - 1) / BK;
+    p.num_kb = (K + bke - 1) / bke;
     p.ea = ea;
     p.vec_ok = 1;
     p.tma_out = 0;
@@ -833,6 +848,11 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M
     if (BN == 224) p.tma_out = 0;
     if (!p.tma_out) ty = ty2 = tr = ta;
     LaunchScope ls(kind, s);
+    if (tf32) {
+        if (epi != EPI_STORE) return cudaErrorNotSupported;
+        if (BN == 256) return launch_impl<256, EPI_STORE, true>(ta, tb, ty, ty2, tr, p, s);
+        return launch_impl<128, EPI_STORE, true>(ta, tb, ty, ty2, tr, p, s);
+    }
     if (BN == 256) {
         if (epi == EPI_QKV) return launch_impl<256, EPI_QKV>(ta, tb, ty, ty2, tr, p, s);
         if (epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU>(ta, tb, ty, ty2, tr, p, s);
@@ -840,6 +860,16 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M
     }
     if (BN == 224) return launch_impl<224, EPI_STORE>(ta, tb, ty, ty2, tr, p, s);
     return launch_impl<128, EPI_STORE>(ta, tb, ty, ty2, tr, p, s);
+}
+
+cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,
+                           GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind) {
+    return launch_gemm(x, W, false, M, N, K, epi, ea, s, kind);
+}
+
+cudaError_t launch_gemm_tc_tf32(const float* x, const float* W, int M, int N, int K,
+                                const GemmEpiArgs& ea, cudaStream_t s, int kind) {
+    return launch_gemm(x, W, true, M, N, K, EPI_STORE, ea, s, kind);
 }
 
 }  // namespace dtp

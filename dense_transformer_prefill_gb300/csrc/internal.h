@@ -67,7 +67,8 @@ cudaError_t launch_rope_table(float2* tab, int T, int rope_dims, float freq_base
 cudaError_t launch_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
                           cudaStream_t s);
 cudaError_t launch_swiglu_interleaved64(const float* gu, float* act, int T, int F,
-                                        cudaStream_t s);
+                                        cudaStream_t s, int act_dtype = DTP_F32);
+cudaError_t launch_round_tf32(float* x, size_t n, cudaStream_t s);
 cudaError_t launch_gemm_simt(const float* x, int ldx, const float* W, void* y, int y_dtype,
                              int ldy, int M, int N, int K, const float* residual,
                              cudaStream_t s, int kind);
@@ -89,7 +90,8 @@ cudaError_t launch_seq_meta(const int* cu_seqlens, int n_seq, int total, int* ti
                             long long vt_cols, cudaStream_t s);
 cudaError_t launch_transpose_v(const __nv_bfloat16* v, __nv_bfloat16* vt, int T, int width,
                                int ldt, cudaStream_t s);
-cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_bf16,
+// to_dtype: DTP_F32, DTP_BF16 or DTP_TF32 (float32 rounded to tf32)
+cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_dtype,
                                int mode, cudaStream_t s);
 cudaError_t launch_copy_f32(const float* src, float* dst, size_t n, cudaStream_t s);
 // dst[r, 0:cols] = src[r, 0:cols] for r < rows (float32, row strides lds / ldd)
@@ -131,6 +133,10 @@ struct GemmEpiArgs {
 // y-side work of one GEMM: x [M, K] bf16 (row stride K), W [N, K] bf16.
 cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,
                            GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind);
+// The same GEMM on float32 operands holding tf32 values (tcgen05 kind::tf32),
+// EPI_STORE epilogue (float32 y, optional residual); K a multiple of 4.
+cudaError_t launch_gemm_tc_tf32(const float* x, const float* W, int M, int N, int K,
+                                const GemmEpiArgs& ea, cudaStream_t s, int kind);
 
 cudaError_t launch_selftest_wait(cudaStream_t s);
 

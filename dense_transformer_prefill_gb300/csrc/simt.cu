@@ -28,6 +28,21 @@ __device__ __forceinline__ void st_elt(__nv_bfloat16* p, size_t i, float v) {
     p[i] = __float2bfloat16_rn(v);
 }
 
+// Round a float32 to TensorFloat-32 (keep 10 fraction bits), nearest with ties
+// to even: add half of the 13 dropped bits' range, minus one unless the kept
+// last bit is odd, then clear them.  Finite inputs only.
+__device__ __forceinline__ float round_tf32(float x) {
+    uint32_t u = __float_as_uint(x);
+    u += 0xFFFu + ((u >> 13) & 1u);
+    return __uint_as_float(u & ~0x1FFFu);
+}
+// float32 storage of tf32 values (DTP_TF32): stores round, loads are plain.
+struct tf32_t {
+    float v;
+};
+__device__ __forceinline__ float ld_elt(const tf32_t* p, size_t i) { return p[i].v; }
+__device__ __forceinline__ void st_elt(tf32_t* p, size_t i, float v) { p[i].v = round_tf32(v); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -179,6 +194,8 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype,
         if (y_dtype == DTP_BF16)
             rmsnorm_reg_kernel<<<rows, threads, 0, s>>>(x, w, (__nv_bfloat16*)y, cols, eps,
                                                         row_idx);
+        else if (y_dtype == DTP_TF32)
+            rmsnorm_reg_kernel<<<rows, threads, 0, s>>>(x, w, (tf32_t*)y, cols, eps, row_idx);
         else
             rmsnorm_reg_kernel<<<rows, threads, 0, s>>>(x, w, (float*)y, cols, eps, row_idx);
         return cudaGetLastError();
@@ -186,6 +203,8 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype,
     int threads = cols >= 1024 ? 256 : (cols >= 256 ? 128 : 32);
     if (y_dtype == DTP_BF16)
         rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (__nv_bfloat16*)y, cols, eps, row_idx);
+    else if (y_dtype == DTP_TF32)
+        rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (tf32_t*)y, cols, eps, row_idx);
     else
         rmsnorm_kernel<<<rows, threads, 0, s>>>(x, w, (float*)y, cols, eps, row_idx);
     return cudaGetLastError();
@@ -313,8 +332,10 @@ cudaError_t launch_swiglu(const void* gate, const void* up, void* out, int dtype
 }
 
 // gu [T, 2F] holds gate/up interleaved in 64-column blocks (block b: gate
-// columns 64b..64b+63 then up columns 64b..64b+63); act [T, F].
-__global__ void swiglu_interleaved64_kernel(const float* __restrict__ gu, float* __restrict__ act,
+// columns 64b..64b+63 then up columns 64b..64b+63); act [T, F] (float32, or
+// float32 rounded to tf32 when To is tf32_t).
+template <typename To>
+__global__ void swiglu_interleaved64_kernel(const float* __restrict__ gu, To* __restrict__ act,
                                             int T, int F) {
     const size_t n = (size_t)T * F;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
@@ -322,16 +343,34 @@ __global__ void swiglu_interleaved64_kernel(const float* __restrict__ gu, float*
         const size_t t = i / F;
         const int f = (int)(i % F);
         const size_t base = t * 2 * F + (size_t)(f / 64) * 128 + (f % 64);
-        act[i] = silu_f(gu[base]) * gu[base + 64];
+        st_elt(act, i, silu_f(gu[base]) * gu[base + 64]);
     }
 }
 
 cudaError_t launch_swiglu_interleaved64(const float* gu, float* act, int T, int F,
-                                        cudaStream_t s) {
+                                        cudaStream_t s, int act_dtype) {
     LaunchScope ls(DTP_K_OTHER, s);
     size_t n = (size_t)T * F, blocks = (n + 255) / 256;
     if (blocks > 65535 * 8) blocks = 65535 * 8;
-    swiglu_interleaved64_kernel<<<(unsigned)blocks, 256, 0, s>>>(gu, act, T, F);
+    if (act_dtype == DTP_TF32)
+        swiglu_interleaved64_kernel<<<(unsigned)blocks, 256, 0, s>>>(gu, (tf32_t*)act, T, F);
+    else
+        swiglu_interleaved64_kernel<<<(unsigned)blocks, 256, 0, s>>>(gu, act, T, F);
+    return cudaGetLastError();
+}
+
+// x[i] = round_tf32(x[i]) in place (float32 storage).
+__global__ void round_tf32_kernel(float* __restrict__ x, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        x[i] = round_tf32(x[i]);
+}
+
+cudaError_t launch_round_tf32(float* x, size_t n, cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    size_t blocks = (n + 255) / 256;
+    if (blocks > 65535 * 8) blocks = 65535 * 8;
+    round_tf32_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, n);
     return cudaGetLastError();
 }
 
@@ -545,14 +584,16 @@ __global__ void pack_matrix_kernel(const float* __restrict__ src, int rows, int 
     }
 }
 
-cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_bf16,
+cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_dtype,
                                int mode, cudaStream_t s) {
     LaunchScope ls(DTP_K_OTHER, s);
     size_t n = (size_t)rows * cols, blocks = (n + 255) / 256;
     if (blocks > 65535 * 16) blocks = 65535 * 16;
-    if (to_bf16)
+    if (to_dtype == DTP_BF16)
         pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (__nv_bfloat16*)dst,
                                                             mode);
+    else if (to_dtype == DTP_TF32)
+        pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (tf32_t*)dst, mode);
     else
         pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (float*)dst, mode);
     return cudaGetLastError();

@@ -55,14 +55,20 @@ enum {
     DTP_ERR_DEVICE_TIMEOUT = -6  /* a kernel's bounded wait gave up (reported by dtp_check)   */
 };
 
-/* Element type of an activation buffer. */
-enum { DTP_F32 = 0, DTP_BF16 = 1 };
+/* Element type of an activation buffer.  DTP_TF32 is float32 storage whose
+ * values are TensorFloat-32 (10-bit fraction; producers round to nearest,
+ * ties to even): the operand type of the kind::tf32 tensor-core GEMM. */
+enum { DTP_F32 = 0, DTP_BF16 = 1, DTP_TF32 = 2 };
 
 /* Arithmetic of the forward pass.
  *   DTP_PREC_F32:  float32 everywhere (SIMT kernels; the pages' "all f32" stage).
+ *   DTP_PREC_TF32: every GEMM on tcgen05 tensor cores with tf32 operands (the
+ *                  weights and each GEMM input rounded to tf32) and float32
+ *                  accumulation; residual stream, norms, QK-norm/RoPE, attention
+ *                  (float32 SIMT kernel), SwiGLU and logits in float32.
  *   DTP_PREC_BF16: bf16 GEMM/attention operands, float32 accumulation, float32
  *                  residual stream, norms, softmax and logits (tcgen05 tensor cores). */
-enum { DTP_PREC_F32 = 0, DTP_PREC_BF16 = 2 };
+enum { DTP_PREC_F32 = 0, DTP_PREC_TF32 = 1, DTP_PREC_BF16 = 2 };
 
 typedef struct dtp_config {
     int n_layer;          /* decoder layers                                         */
@@ -75,7 +81,7 @@ typedef struct dtp_config {
     int n_vocab;          /* vocabulary V                                           */
     float rope_freq_base; /* RoPE base; theta_i = base^(-2i/r)                      */
     float rms_eps;        /* epsilon inside every RMSNorm's square root             */
-    int precision;        /* DTP_PREC_F32 or DTP_PREC_BF16                          */
+    int precision;        /* DTP_PREC_F32, DTP_PREC_TF32 or DTP_PREC_BF16           */
     int attn_gate;        /* 1: gated attention -- the Q projection also yields, per head,
                              head_dim gate values after its head_dim q values, and the
                              attention output is multiplied by sigmoid(gate) before the
@@ -107,7 +113,9 @@ typedef struct dtp_layer_src {
  * matrix, Wgate and Wup interleaved in blocks of 64 rows into one [2F, d] matrix,
  * Wo, Wdown, and the four norm vectors; then tok_embd [V, d], output_norm [d]
  * and the lm_head [V, d].  Matrices are stored as bf16 (round to nearest even)
- * under DTP_PREC_BF16 and float32 under DTP_PREC_F32; norm vectors are float32.
+ * under DTP_PREC_BF16, float32 under DTP_PREC_F32, and float32 rounded to tf32
+ * (nearest even) under DTP_PREC_TF32, except tok_embd, which stays float32;
+ * norm vectors are float32.
  * ------------------------------------------------------------------------------------ */
 
 /* Bytes of the packed buffer for `cfg` (0 if cfg is invalid). */
@@ -154,7 +162,7 @@ typedef struct dtp_fwd_outputs {
     float* hidden;   /* device float32 [n_layer + 1, T, n_embd], as in dtp_fwd_prefill      */
     void* k_cache;   /* device [n_layer, T, n_head_kv*head_dim]: every layer's keys after
                         QK-norm and RoPE (what attention consumed), token-major; bf16 under
-                        DTP_PREC_BF16, float32 under DTP_PREC_F32 -- a decode KV cache     */
+                        DTP_PREC_BF16, float32 otherwise -- a decode KV cache              */
     void* v_cache;   /* device [n_layer, T, n_head_kv*head_dim]: every layer's values, same
                         dtype and layout as k_cache                                         */
 } dtp_fwd_outputs;
@@ -197,7 +205,8 @@ int dtp_fwd_prefill_varlen(const dtp_config* cfg, const void* packed, size_t pac
  * offset l * S with S the per-layer stride below,
  *   DTP_PREC_BF16: K  bf16 [max_T, nk] token-major, then (256-byte aligned)
  *                  V^T bf16 [nk, ldvt], ldvt = max_T rounded up to 8
- *   DTP_PREC_F32:  K  f32 [max_T, nk], then (256-byte aligned) V f32 [max_T, nk]
+ *   DTP_PREC_F32 / DTP_PREC_TF32:
+ *                  K  f32 [max_T, nk], then (256-byte aligned) V f32 [max_T, nk]
  * Positions >= p0 + C are neither read nor written.  Calls on one state run
  * in position order (the stream orders them).
  *   tokens     device uint32 [C]
@@ -244,8 +253,8 @@ const char* dtp_last_error(void);
 /* rms_norm (forward.rs: `e.rms_norm(x, w, out, ncols, nrows, eps)`):
  * y[r, c] = x[r, c] / sqrt(mean_c(x[r, :]^2) + eps) * w[c].
  * x device float32 [rows, cols]; w device float32 [cols]; y device [rows, cols]
- * of y_dtype (DTP_F32 or DTP_BF16, bf16 rounded to nearest even).  y may alias
- * x when y_dtype is DTP_F32. */
+ * of y_dtype (DTP_F32, DTP_BF16 or DTP_TF32; bf16 / tf32 rounded to nearest
+ * even).  y may alias x when y_dtype is DTP_F32 or DTP_TF32. */
 int dtp_rms_norm(const float* x, const float* w, void* y, int y_dtype, int rows, int cols,
                  float eps, dtp_stream_t stream);
 
@@ -311,7 +320,9 @@ int dtp_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
 /* Linear (forward.rs `e.matmul(&w, &x, t)`): y[M, N] = x[M, K] W[N, K]^T
  * (+ residual[M, N]).
  * x, W device, both of dtype: DTP_F32 -> float32 SIMT kernel; DTP_BF16 ->
- * tcgen05 tensor cores with float32 accumulation (K % 8 == 0).
+ * tcgen05 tensor cores with float32 accumulation (K % 8 == 0); DTP_TF32 ->
+ * tcgen05 kind::tf32 with float32 accumulation (K % 4 == 0, y_dtype DTP_F32;
+ * x and W hold tf32 values -- float32 with the low 13 fraction bits zero).
  * y device of y_dtype (DTP_F32 or DTP_BF16).  residual: device float32
  * [M, N] or NULL; when given, y_dtype must be DTP_F32 and y = residual + x W^T;
  * residual may alias y (in-place residual add). */

@@ -31,6 +31,7 @@ from .model import (  # noqa: F401
     rope_angles,
     rope_neox,
     round_bf16,
+    round_tf32,
     sdpa_causal_gqa,
     silu,
     swiglu,

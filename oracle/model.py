@@ -28,6 +28,9 @@ sites, not their bodies):
     activation (normed h, attention output, SwiGLU act, final normed x) and the
     q/k/v handed to attention are rounded to bf16 (nearest, ties to even); all
     sums and the residual stream stay in float64.
+  * tf32-operand mode: the same GEMM operands rounded to TensorFloat-32 (10-bit
+    fraction, nearest, ties to even) instead; q/k/v and the gate stay unrounded
+    (that mode's attention reads float32).
 """
 from __future__ import annotations
 
@@ -48,6 +51,29 @@ def round_bf16(x) -> np.ndarray:
     x = np.asarray(x, dtype=F64)
     m, e = np.frexp(x)
     return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def round_tf32(x) -> np.ndarray:
+    """Round to the nearest TensorFloat-32 value (11 significant bits: the f32
+    exponent with a 10-bit fraction), ties to even; same construction as
+    round_bf16 with 2^11 in place of 2^8."""
+    x = np.asarray(x, dtype=F64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 2048.0), e - 11)
+
+
+def _rounders(bf16_operands: bool, tf32_operands: bool):
+    """(GEMM-operand rounding, attention-operand rounding) of a mode.  bf16 mode
+    rounds both (the tensor-core attention reads bf16 q/k/v); tf32 mode rounds
+    the GEMM operands only (its attention runs on float32 q/k/v)."""
+    ident = lambda a: a
+    if bf16_operands and tf32_operands:
+        raise ValueError("bf16_operands and tf32_operands are exclusive")
+    if bf16_operands:
+        return round_bf16, round_bf16
+    if tf32_operands:
+        return round_tf32, ident
+    return ident, ident
 
 
 # --------------------------------------------------------------------------------------
@@ -158,16 +184,17 @@ def linear(x, W) -> np.ndarray:
 # --------------------------------------------------------------------------------------
 # Whole forward
 # --------------------------------------------------------------------------------------
-def _mats(w: dict, bf16: bool) -> dict:
+def _mats(w: dict, rnd) -> dict:
+    """Layer tensors in float64, every matrix passed through `rnd`."""
     out = {}
     for name, a in w.items():
         a = np.asarray(a, dtype=F64)
-        out[name] = round_bf16(a) if (bf16 and a.ndim == 2) else a
+        out[name] = rnd(a) if a.ndim == 2 else a
     return out
 
 
 def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=None,
-                  kv_prefix=None) -> np.ndarray:
+                  kv_prefix=None, tf32_operands: bool = False) -> np.ndarray:
     """One decoder layer, forward.rs `Model::forward` loop body, on the residual
     stream x [T, n_embd]; returns the new x.  If `kv_out` is a list, the layer's
     attention inputs (k after QK-norm and RoPE, and v) are appended to it.
@@ -175,8 +202,8 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     `kv_prefix` = (k, v) of the p0 positions before x (which then sits at
     positions pos = p0 .. p0+T-1): attention runs over those keys followed by
     x's own, the only way earlier positions reach later ones."""
-    op = round_bf16 if bf16_operands else (lambda a: a)
-    L = _mats(lw, bf16_operands)
+    op, opa = _rounders(bf16_operands, tf32_operands)
+    L = _mats(lw, op)
     d, h, g, hd = cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim
     eps = cfg.rms_eps
     scale = 1.0 / np.sqrt(F64(hd))
@@ -186,14 +213,14 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     gate = None
     if getattr(cfg, "attn_gate", False):
         qg = q.reshape(q.shape[0], h, 2, hd)
-        q, gate = qg[:, :, 0, :].reshape(-1, h * hd), op(qg[:, :, 1, :].reshape(-1, h * hd))
+        q, gate = qg[:, :, 0, :].reshape(-1, h * hd), opa(qg[:, :, 1, :].reshape(-1, h * hd))
     k = linear(hN, L["wk"])
     v = linear(hN, L["wv"])
     q = qk_norm(q, L["q_norm"], hd, eps)
     k = qk_norm(k, L["k_norm"], hd, eps)
-    q = op(rope_neox(q, pos, h, hd, cfg.rope_dim_count, cfg.rope_freq_base))
-    k = op(rope_neox(k, pos, g, hd, cfg.rope_dim_count, cfg.rope_freq_base))
-    v = op(v)
+    q = opa(rope_neox(q, pos, h, hd, cfg.rope_dim_count, cfg.rope_freq_base))
+    k = opa(rope_neox(k, pos, g, hd, cfg.rope_dim_count, cfg.rope_freq_base))
+    v = opa(v)
     if kv_out is not None:
         kv_out.append((k, v))
     p0 = 0
@@ -213,7 +240,7 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
 
 
 def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidden: bool = False,
-            layer_source=None, kv_out=None):
+            layer_source=None, kv_out=None, tf32_operands: bool = False):
     """forward.rs `Model::forward`: logits [T, n_vocab] for `tokens`, positions 0..T-1.
 
     weights: {"tok_embd" [V,d], "layers": [dict per layer], "output_norm" [d],
@@ -224,7 +251,7 @@ def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidd
     stream entering output_norm."""
     tokens = np.asarray(tokens, dtype=np.int64)
     T = tokens.shape[0]
-    op = round_bf16 if bf16_operands else (lambda a: a)
+    op, _ = _rounders(bf16_operands, tf32_operands)
     emb = np.asarray(weights["tok_embd"], dtype=F64)
     if bf16_operands:
         emb = round_bf16(emb[tokens])
@@ -235,20 +262,18 @@ def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidd
     hidden = [x.copy()] if return_hidden else None
     for l in range(cfg.n_layer):
         lw = layer_source(l) if layer_source is not None else weights["layers"][l]
-        x = forward_layer(cfg, lw, x, pos, bf16_operands, kv_out)
+        x = forward_layer(cfg, lw, x, pos, bf16_operands, kv_out, tf32_operands=tf32_operands)
         if return_hidden:
             hidden.append(x.copy())
     hn = op(rms_norm(x, np.asarray(weights["output_norm"], dtype=F64), cfg.rms_eps))
-    W_out = np.asarray(weights["output"], dtype=F64)
-    if bf16_operands:
-        W_out = round_bf16(W_out)
-    logits = linear(hn, W_out)
+    logits = linear(hn, op(np.asarray(weights["output"], dtype=F64)))
     if return_hidden:
         return logits, np.stack(hidden)
     return logits
 
 
-def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: bool = False):
+def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: bool = False,
+                  tf32_operands: bool = False):
     """Chunked prefill: logits [C, n_vocab] for the next C tokens of a sequence
     whose first p0 positions went through earlier calls.  forward.rs
     `Model::forward` is causal, so those positions reach these only through
@@ -257,7 +282,7 @@ def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: boo
     with this chunk's.  The chunks' logits, concatenated, are forward(tokens)'s."""
     tokens = np.asarray(tokens, dtype=np.int64)
     C = tokens.shape[0]
-    op = round_bf16 if bf16_operands else (lambda a: a)
+    op, _ = _rounders(bf16_operands, tf32_operands)
     first = len(kv_state) == 0
     p0 = 0 if first else kv_state[0][0].shape[0]
     x = np.asarray(weights["tok_embd"], dtype=F64)[tokens]
@@ -267,7 +292,8 @@ def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: boo
     for l in range(cfg.n_layer):
         new = []
         prefix = None if first else kv_state[l]
-        x = forward_layer(cfg, weights["layers"][l], x, pos, bf16_operands, new, prefix)
+        x = forward_layer(cfg, weights["layers"][l], x, pos, bf16_operands, new, prefix,
+                          tf32_operands)
         k, v = new[0]
         if first:
             kv_state.append((k, v))
@@ -275,10 +301,7 @@ def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: boo
             kv_state[l] = (np.concatenate([kv_state[l][0], k]),
                            np.concatenate([kv_state[l][1], v]))
     hn = op(rms_norm(x, np.asarray(weights["output_norm"], dtype=F64), cfg.rms_eps))
-    W_out = np.asarray(weights["output"], dtype=F64)
-    if bf16_operands:
-        W_out = round_bf16(W_out)
-    return linear(hn, W_out)
+    return linear(hn, op(np.asarray(weights["output"], dtype=F64)))
 
 
 # --------------------------------------------------------------------------------------

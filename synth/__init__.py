@@ -102,7 +102,8 @@ class ModelConfig:
     T: int
     rope_freq_base: float = 1e6
     rms_eps: float = 1e-6
-    precision: str = "bf16"          # "f32" (exact) or "bf16" (bf16 operands, f32 accumulate)
+    precision: str = "bf16"          # "f32" (exact), "tf32" or "bf16" (tf32 / bf16 GEMM
+                                     # operands, f32 accumulate)
     attn_gate: bool = False          # sigmoid output gate fused into the Q projection
 
     def replace(self, **kw) -> "ModelConfig":

@@ -47,6 +47,21 @@ def assert_parity(cfg, gl, gh, rl, rh):
         assert max(layer_err) <= 1e-5, metrics
         assert metrics["logit_rel_l2"] <= 1e-5, metrics
         return metrics
+    if cfg.precision == "tf32":
+        # Against the oracle's tf32-operand mode: the same operands are rounded
+        # on both sides, so differences are float32-level, amplified only where
+        # that moves a value across a tf32 rounding boundary (one tf32 ulp,
+        # u = 2^-11); bounded like the bf16 case with the tf32 u and no factor 2.
+        u = 2.0 ** -11
+        assert layer_err[0] == 0.0, metrics
+        for l in range(1, cfg.n_layer + 1):
+            assert layer_err[l] <= u * np.sqrt(l), (l, metrics)
+        assert metrics["logit_rel_l2"] <= u * np.sqrt(cfg.n_layer + 1), metrics
+        agree, structured = argmax_agreement_near_tie(gl, rl, 2 * metrics["logit_max_abs"])
+        metrics.update(argmax_agreement=agree, structured_flips=structured)
+        assert structured == 0 and agree >= 0.995, metrics
+        print(f"\nparity {cfg.name} T={cfg.T}: {metrics}")
+        return metrics
     u = 2.0 ** -8
     assert layer_err[0] == 0.0, metrics                    # same bf16 embedding rows
     for l in range(1, cfg.n_layer + 1):
@@ -213,7 +228,7 @@ def test_forward_last_and_kv_cache(dtp, prec):
     assert torch.equal(kc2, kc)
 
 
-@pytest.mark.parametrize("prec", ["f32", "bf16"])
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
 def test_varlen_packed_sequences(dtp, prec):
     """dtp_fwd_prefill_varlen: sequences packed along the token axis, each at
     positions 0..len-1 attending only to itself, equal the oracle run on every
@@ -232,7 +247,7 @@ def test_varlen_packed_sequences(dtp, prec):
     hidden = torch.empty((L + 1, total, cfg.n_embd), dtype=torch.float32, device=dev)
     dtp.fwd_prefill_varlen(m.c, m.packed, tt, ct, ws, logits=logits, hidden=hidden)
     last = torch.empty((len(lens), cfg.n_vocab), dtype=torch.float32, device=dev)
-    cdt = torch.float32 if prec == "f32" else torch.bfloat16
+    cdt = torch.bfloat16 if prec == "bf16" else torch.float32
     kc = torch.empty((L, total, nk), dtype=cdt, device=dev)
     dtp.fwd_prefill_varlen(m.c, m.packed, tt, ct, ws, logits=last, last_only=True, k_cache=kc)
     torch.cuda.synchronize()
@@ -245,11 +260,11 @@ def test_varlen_packed_sequences(dtp, prec):
         a = cu[b]
         kv = []
         rl, rh = oracle.forward(cfg, w, toks[a:a + n], bf16_operands=(prec == "bf16"),
-                                return_hidden=True, kv_out=kv)
+                                tf32_operands=(prec == "tf32"), return_hidden=True, kv_out=kv)
         assert_parity(cfg.replace(T=n), gl[a:a + n], gh[:, a:a + n], rl, rh)
         np.testing.assert_allclose(glast[b], gl[a + n - 1], rtol=0, atol=1e-6)
         k0 = kc[0, a:a + n].float().cpu().numpy()
-        assert rel_l2(k0, kv[0][0]) <= (1e-5 if prec == "f32" else 2.0 ** -8)
+        assert rel_l2(k0, kv[0][0]) <= {"f32": 1e-5, "tf32": 2.0 ** -11, "bf16": 2.0 ** -8}[prec]
 
 
 def test_varlen_single_sequence_matches_plain_forward(dtp):
@@ -314,7 +329,7 @@ def _run_chunks(dtp, m, cfg, toks, plan, max_T, state=None, last_only=False):
 CHUNK_PLANS = [(256, 256, 88), (100, 300, 200), (1, 598, 1), (600,)]
 
 
-@pytest.mark.parametrize("prec", ["f32", "bf16"])
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
 @pytest.mark.parametrize("plan", CHUNK_PLANS)
 def test_chunked_prefill(dtp, prec, plan):
     """dtp_fwd_prefill_chunk: positions p0..p0+C-1 against the KV state of the
@@ -335,7 +350,7 @@ def test_chunked_prefill(dtp, prec, plan):
         assert_parity(cfg, gl, gh, rl, rh)
 
 
-@pytest.mark.parametrize("prec", ["f32", "bf16"])
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
 def test_chunked_prefill_state_is_the_kv_cache(dtp, prec):
     """After the chunks, the state holds every layer's K (and V, transposed in
     bf16) exactly as dtp_fwd_prefill_ex's KV outputs of the whole pass."""
@@ -352,7 +367,7 @@ def test_chunked_prefill_state_is_the_kv_cache(dtp, prec):
     dtp.fwd_prefill_chunk(m.c, m.packed, t(170, T), 170, state, max_T, m.workspace(T - 170),
                           logits=last, last_only=True)
     L, nk = cfg.n_layer, cfg.n_head_kv * cfg.head_dim
-    cdt = torch.float32 if prec == "f32" else torch.bfloat16
+    cdt = torch.bfloat16 if prec == "bf16" else torch.float32
     kc = torch.empty((L, T, nk), dtype=cdt, device=dev)
     vc = torch.empty((L, T, nk), dtype=cdt, device=dev)
     full = torch.empty((T, cfg.n_vocab), dtype=torch.float32, device=dev)
@@ -360,7 +375,7 @@ def test_chunked_prefill_state_is_the_kv_cache(dtp, prec):
     torch.cuda.synchronize()
     dtp.check()
     assert torch.equal(last[0], full[-1])
-    eb = 4 if prec == "f32" else 2
+    eb = 2 if prec == "bf16" else 4
     up = lambda x, a: (x + a - 1) // a * a
     k_bytes = up(max_T * nk * eb, 256)
     per = dtp.kv_state_size(m.c, max_T) // L
@@ -368,7 +383,7 @@ def test_chunked_prefill_state_is_the_kv_cache(dtp, prec):
         lay = state[l * per:(l + 1) * per]
         ks = lay[:max_T * nk * eb].view(cdt).view(max_T, nk)
         assert torch.equal(ks[:T], kc[l])
-        if prec == "f32":
+        if prec != "bf16":
             vs = lay[k_bytes:k_bytes + max_T * nk * 4].view(cdt).view(max_T, nk)
             assert torch.equal(vs[:T], vc[l])
         else:

@@ -424,12 +424,12 @@ def test_planted_gate_layout_swap_is_caught(monkeypatch):
     # reading the q region as [all q heads | all gate heads] instead of per head
     real = om.forward_layer
 
-    def wrong(cfg, lw, x, pos, bf16_operands=False, kv_out=None):
+    def wrong(cfg, lw, x, pos, bf16_operands=False, kv_out=None, *args, **kw):
         if getattr(cfg, "attn_gate", False):
             h, hd = cfg.n_head, cfg.head_dim
             wq = lw["wq"].reshape(2, h, hd, -1).transpose(1, 0, 2, 3).reshape(2 * h * hd, -1)
             lw = dict(lw, wq=wq)
-        return real(cfg, lw, x, pos, bf16_operands, kv_out)
+        return real(cfg, lw, x, pos, bf16_operands, kv_out, *args, **kw)
     monkeypatch.setattr(om, "forward_layer", wrong)
     assert _pins_fail(test_gated_attention_zero_gate_halves_attention)
 
@@ -480,8 +480,46 @@ def test_planted_chunk_positions_restart_is_caught(monkeypatch, tiny_weights):
     row) fails the concatenation pin."""
     real = om.forward_layer
 
-    def wrong(cfg, lw, x, pos, bf16=False, kv_out=None, kv_prefix=None):
-        return real(cfg, lw, x, np.arange(len(pos)), bf16, kv_out, kv_prefix)
+    def wrong(cfg, lw, x, pos, *args, **kw):
+        return real(cfg, lw, x, np.arange(len(pos)), *args, **kw)
     monkeypatch.setattr(om, "forward_layer", wrong)
     assert _pins_fail(lambda: test_forward_chunk_concatenates_to_the_full_pass(tiny_weights,
                                                                               (5, 7, 4)))
+
+
+# ---------------------------------------------------------------- tf32 rounding
+def test_round_tf32_hand_fixture():
+    """11 significant bits, nearest, ties to even (hand-worked values)."""
+    u = 2.0 ** -10                                   # one tf32 ulp at 1.0
+    cases = [(1.0, 1.0), (1.0 + u, 1.0 + u), (1.0 + u / 2, 1.0),        # tie -> even (1.0)
+             (1.0 + 3 * u / 2, 1.0 + 2 * u),                            # tie -> even (1+2u)
+             (1.0 + 0.49 * u, 1.0), (1.0 + 0.51 * u, 1.0 + u),
+             (-3.0 - u, -3.0), (2.0 ** 20 * (1 + u / 2), 2.0 ** 20), (0.0, 0.0)]
+    for x, want in cases:
+        assert oracle.round_tf32(x) == want, (x, want)
+
+
+def test_round_tf32_matches_bit_rounding_on_f32_values():
+    """On float32 inputs, round_tf32 equals nearest-even rounding of the bit
+    pattern (add 0xFFF plus the kept lsb, clear the 13 dropped bits), and it is
+    idempotent and keeps at most 11 significant bits."""
+    x = (synth.normal(9, 900, (20000,)) * np.exp(synth.normal(9, 901, (20000,)) * 4)).astype(np.float32)
+    x[:4] = [1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, -(1.0 + 2.0 ** -11), 1.5]   # exact ties
+    u = x.view(np.uint32).astype(np.uint64)
+    want = ((u + 0xFFF + ((u >> 13) & 1)) & ~np.uint64(0x1FFF)).astype(np.uint32).view(np.float32)
+    got = oracle.round_tf32(x)
+    np.testing.assert_array_equal(got, want.astype(np.float64))
+    np.testing.assert_array_equal(oracle.round_tf32(got), got)
+    m, _ = np.frexp(got)
+    np.testing.assert_array_equal(m * 2048, np.rint(m * 2048))
+
+
+def test_forward_tf32_mode_between_exact_and_bf16(tiny_weights):
+    toks = synth.tokens(TINY)
+    a = oracle.forward(TINY, tiny_weights, toks)
+    t = oracle.forward(TINY, tiny_weights, toks, tf32_operands=True)
+    b = oracle.forward(TINY, tiny_weights, toks, bf16_operands=True)
+    rt = np.linalg.norm(a - t) / np.linalg.norm(a)
+    rb = np.linalg.norm(a - b) / np.linalg.norm(a)
+    # 3 more significant bits: the error shrinks about 8x
+    assert 1e-6 < rt < rb / 3
