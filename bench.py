@@ -140,7 +140,9 @@ class OracleSample:
 
     def __init__(self, cfg, s_layer: int = 1024, s_head: int = 512, v_slice: int = 8192):
         self.cfg = cfg
-        self.bf16 = cfg.precision == "bf16"
+        self.mode = {"bf16_operands": cfg.precision == "bf16",
+                     "tf32_operands": cfg.precision == "tf32",
+                     "fp8_operands": cfg.precision == "e4m3"}
         self.sl = min(cfg.T, s_layer)
         self.sh = min(cfg.T, s_head)
         self.vs = min(cfg.n_vocab, v_slice)
@@ -155,19 +157,18 @@ class OracleSample:
 
         cfg, T = self.cfg, self.cfg.T
         t0 = time.perf_counter()
-        oracle.forward_layer(cfg, self.lw, self.x, np.arange(self.sl), bf16_operands=self.bf16)
+        oracle.forward_layer(cfg, self.lw, self.x, np.arange(self.sl), **self.mode)
         t_layer = time.perf_counter() - t0
         t0 = time.perf_counter()
-        if self.bf16:
-            oracle.linear(oracle.round_bf16(self.hn), oracle.round_bf16(self.W))
-        else:
-            oracle.linear(self.hn, self.W)
+        rnd = {"bf16": oracle.round_bf16, "tf32": oracle.round_tf32,
+               "e4m3": oracle.fake_quant_rows_e4m3}.get(cfg.precision, lambda a: a)
+        oracle.linear(rnd(self.hn), rnd(self.W))
         t_head = time.perf_counter() - t0
         total = (cfg.n_layer * t_layer * T / self.sl
                  + t_head * (T / self.sh) * (cfg.n_vocab / self.vs))
         cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
         return {"value": T / total, "unit": UNIT, "cores": cores, "kind": "oracle",
-                "sample": (f"float64 numpy oracle ({'bf16-operand mode' if self.bf16 else 'exact'},"
+                "sample": (f"float64 numpy oracle ({cfg.precision} operand mode,"
                            f" BLAS on all {cores} host cores) on {cfg.name}: 1 decoder layer over "
                            f"the first {self.sl} tokens ({t_layer:.2f} s) + lm_head over "
                            f"{self.sh} rows x {self.vs} vocab rows ({t_head:.2f} s), scaled to "
@@ -218,6 +219,8 @@ def main():
     ap.add_argument("--no-attn-sweep", action="store_true")
     ap.add_argument("--n-layer", type=int, default=None,
                     help="override the layer count (profiling captures of a small case)")
+    ap.add_argument("--precision", default=None, choices=["bf16", "tf32", "e4m3", "f32"],
+                    help="arithmetic (default: the workload's, bf16 for the model shapes)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -228,6 +231,8 @@ def main():
     cfg = synth.CONFIGS[args.workload]
     if args.n_layer is not None:
         cfg = cfg.replace(n_layer=args.n_layer)
+    if args.precision is not None:
+        cfg = cfg.replace(precision=args.precision)
     config = {"workload": cfg.name, "T": cfg.T, "n_layer": cfg.n_layer, "n_embd": cfg.n_embd,
               "n_head": cfg.n_head, "n_head_kv": cfg.n_head_kv, "head_dim": cfg.head_dim,
               "n_ff": cfg.n_ff, "n_vocab": cfg.n_vocab, "sequences_per_gpu": 1,
@@ -365,23 +370,32 @@ def main():
     gu_n, gu_ms = kstats["gemm_gateup"]
     gu_flops = 2.0 * T * (2 * F) * d
     achieved = gu_flops / (gu_ms / gu_n / 1000.0) / 1e12 if gu_n else None
-    peak = peaks["bf16_tflops_sustained"] if cfg.precision == "bf16" else None
+    # GEMM peak of the operand type: the measured bf16 figure, times the nominal
+    # dense ratio for tf32 (1.1 / 2.25) and e4m3 (4.5 / 2.25); attention runs bf16
+    # tensor cores in bf16 and e4m3 modes
+    bf16_peak = peaks["bf16_tflops_sustained"]
+    peak = {"bf16": bf16_peak, "tf32": bf16_peak * 1.1 / 2.25,
+            "e4m3": bf16_peak * 2.0}.get(cfg.precision)
+    attn_peak = bf16_peak if cfg.precision in ("bf16", "e4m3") else None
     is8b = cfg.name == "qwen3-8b-shape" and cfg.T == 4096
-    roofline = {"kernel": "gemm_tc_kernel<256, EPI_SWIGLU> (gate/up projection + SwiGLU)",
+    roofline = {"kernel": "gemm_tc_kernel (gate/up projection, %s operands)" % cfg.precision,
                 "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if (achieved and peak) else None,
                 "traffic": profiled_traffic("gemm_tc_gateup_qwen3-8b-shape.md",
                                             ["gemm_tc.cu", "ptx.cuh", "internal.h"]) if is8b else None,
                 "algorithmic_bytes_per_launch": 2.0 * (T * d + 2 * F * d + T * F),
                 "flops_per_launch": gu_flops,
-                "peak_source": f"bf16_tflops_sustained of {peaks['source']} peaks",
+                "peak_source": f"bf16_tflops_sustained of {peaks['source']} peaks"
+                               + ("" if cfg.precision == "bf16" else
+                                  f" x the nominal {cfg.precision}/bf16 dense ratio"),
                 "avg_launch_ms": gu_ms / gu_n if gu_n else None}
     at_n, at_ms = kstats["attn"]
     at_flops = cfg.attn_flops() / cfg.n_layer
     at_ach = at_flops / (at_ms / at_n / 1000.0) / 1e12 if at_n else None
     roofline_attn = {"kernel": "attn_tc_kernel<%d> (causal GQA flash attention, one layer)"
-                     % cfg.head_dim, "bound": "tensor", "achieved": at_ach, "peak": peak,
-                     "unit": "TFLOP/s", "frac": (at_ach / peak) if (at_ach and peak) else None,
+                     % cfg.head_dim, "bound": "tensor", "achieved": at_ach, "peak": attn_peak,
+                     "unit": "TFLOP/s",
+                     "frac": (at_ach / attn_peak) if (at_ach and attn_peak) else None,
                      "traffic": profiled_traffic("attn_tc_qwen3-8b-shape.md",
                                                  ["attn_tc.cu", "ptx.cuh", "internal.h"]) if is8b else None,
                      "flops_per_launch": at_flops,
@@ -401,7 +415,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if cfg.precision == "bf16" else "f32",
+        "dtype": cfg.precision,
         "data": "synthetic (seeded random-init weights of the architecture, uniform token ids)",
         "config": config, "roofline": roofline, "roofline_attn": roofline_attn,
         "tflops": {"step": step_flops / (ms_per_step / 1000.0) / 1e12,
@@ -409,8 +423,8 @@ def main():
                    "attn": attn_flops / (attn_ms / 1000.0) / 1e12 if attn_ms else None,
                    "gemm_frac_of_peak": (gemm_flops / (gemm_ms / 1000.0) / 1e12 / peak)
                    if (gemm_ms and peak) else None,
-                   "attn_frac_of_peak": (attn_flops / (attn_ms / 1000.0) / 1e12 / peak)
-                   if (attn_ms and peak) else None},
+                   "attn_frac_of_peak": (attn_flops / (attn_ms / 1000.0) / 1e12 / attn_peak)
+                   if (attn_ms and attn_peak) else None},
         "kernels": per_kernel,
         "instrumented_ms_per_step": instrumented_ms_per_step,
         "clocks": clk.summary(),

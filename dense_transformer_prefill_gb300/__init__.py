@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     DTP_F32,
     DTP_TF32,
     DTP_PREC_BF16,
+    DTP_PREC_E4M3,
     DTP_PREC_F32,
     DTP_PREC_TF32,
     KERNEL_KINDS,
@@ -28,13 +29,16 @@ from ._binding import (  # noqa: F401
     last_error,
     launch_count,
     linear,
+    linear_e4m3,
     lib,
     pack_globals,
     pack_layer,
     packed_size,
     qk_norm_rope_neox,
+    quantize_rows_e4m3,
     qkv_norm_rope,
     rms_norm,
+    rms_norm_e4m3,
     sdpa_causal_gqa,
     sdpa_workspace_size,
     selftest_wait_timeout,

@@ -12,7 +12,7 @@ import torch
 from .build import LIB, build  # noqa: F401
 
 DTP_F32, DTP_BF16, DTP_TF32 = 0, 1, 2
-DTP_PREC_F32, DTP_PREC_TF32, DTP_PREC_BF16 = 0, 1, 2
+DTP_PREC_F32, DTP_PREC_TF32, DTP_PREC_BF16, DTP_PREC_E4M3 = 0, 1, 2, 3
 KERNEL_KINDS = {"embed": 0, "rmsnorm": 1, "gemm_qkv": 2, "attn": 3, "gemm_o": 4,
                 "gemm_gateup": 5, "gemm_down": 6, "gemm_lmhead": 7, "other": 8}
 
@@ -63,6 +63,11 @@ _SIGS = {
     "dtp_fwd_prefill_varlen": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_void_p, c_int,
                                 c_int, ctypes.POINTER(FwdOutputs), c_void_p, c_size_t, c_void_p],
                                c_int),
+    "dtp_quantize_rows_e4m3": ([c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p], c_int),
+    "dtp_rms_norm_e4m3": ([c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_float, c_void_p],
+                          c_int),
+    "dtp_linear_e4m3": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                         c_void_p, c_void_p], c_int),
     "dtp_kv_state_size": ([ctypes.POINTER(Config), c_int], c_size_t),
     "dtp_fwd_prefill_chunk": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int, c_int,
                                c_void_p, c_size_t, c_int, ctypes.POINTER(FwdOutputs), c_void_p,
@@ -136,11 +141,12 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def config_from(cfg) -> Config:
     """Config from an object/dict with the dtp_config field names; precision may be
-    "f32"/"tf32"/"bf16" or the DTP_PREC_* code."""
+    "f32"/"tf32"/"bf16"/"e4m3" or the DTP_PREC_* code."""
     get = (lambda k: cfg[k]) if isinstance(cfg, dict) else (lambda k: getattr(cfg, k))
     prec = get("precision")
     if isinstance(prec, str):
-        prec = {"f32": DTP_PREC_F32, "tf32": DTP_PREC_TF32, "bf16": DTP_PREC_BF16}[prec]
+        prec = {"f32": DTP_PREC_F32, "tf32": DTP_PREC_TF32, "bf16": DTP_PREC_BF16,
+                "e4m3": DTP_PREC_E4M3}[prec]
     try:
         gate = int(bool(get("attn_gate")))
     except (KeyError, AttributeError):
@@ -288,6 +294,28 @@ def linear(x, W, y, residual=None, tf32: bool = False, stream=None) -> None:
     dt = DTP_TF32 if tf32 else _dtype_code(x)
     _ok(lib().dtp_linear(x.data_ptr(), W.data_ptr(), y.data_ptr(), dt, _dtype_code(y),
                          M, N, K, _ptr(residual), _stream(stream)))
+
+
+def quantize_rows_e4m3(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None) -> None:
+    """Per-row e4m3 codes (uint8 [rows, cols]) and float32 scales [rows] of x."""
+    rows, cols = x.shape
+    _ok(lib().dtp_quantize_rows_e4m3(x.data_ptr(), _dtype_code(x), rows, cols, q.data_ptr(),
+                                     scale.data_ptr(), _stream(stream)))
+
+
+def rms_norm_e4m3(x: torch.Tensor, w: torch.Tensor, q: torch.Tensor, scale: torch.Tensor,
+                  eps: float, stream=None) -> None:
+    rows, cols = x.shape
+    _ok(lib().dtp_rms_norm_e4m3(x.data_ptr(), w.data_ptr(), q.data_ptr(), scale.data_ptr(), rows,
+                                cols, eps, _stream(stream)))
+
+
+def linear_e4m3(xq, x_scale, wq, w_scale, y, residual=None, stream=None) -> None:
+    """y = x_scale[m] w_scale[n] (xq wq^T)[m, n] (+ residual) on e4m3 codes."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _ok(lib().dtp_linear_e4m3(xq.data_ptr(), x_scale.data_ptr(), wq.data_ptr(), w_scale.data_ptr(),
+                              y.data_ptr(), M, N, K, _ptr(residual), _stream(stream)))
 
 
 def qkv_norm_rope(h, w_qkv, q_norm, k_norm, q, k, vt, n_head: int, n_head_kv: int,

@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(OUT_DIR, "libdtp.so")
-SOURCES = ["capi.cu", "simt.cu", "gemm_tc.cu", "attn_tc.cu", "noalloc.cu"]
+SOURCES = ["capi.cu", "simt.cu", "gemm_tc.cu", "attn_tc.cu", "noalloc.cu", "quant.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

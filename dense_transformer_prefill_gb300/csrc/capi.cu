@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -125,7 +126,7 @@ static int validate_config(const dtp_config* c) {
     if (!(c->rms_eps >= 0.f) || !(c->rope_freq_base > 0.f))
         return fail(DTP_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_freq_base > 0");
     if (c->precision != DTP_PREC_F32 && c->precision != DTP_PREC_TF32 &&
-        c->precision != DTP_PREC_BF16)
+        c->precision != DTP_PREC_BF16 && c->precision != DTP_PREC_E4M3)
         return fail(DTP_ERR_INVALID_ARG, "unknown precision %d", c->precision);
     if (c->attn_gate != 0 && c->attn_gate != 1)
         return fail(DTP_ERR_INVALID_ARG, "attn_gate must be 0 or 1");
@@ -133,7 +134,11 @@ static int validate_config(const dtp_config* c) {
         return fail(DTP_ERR_UNSUPPORTED, "n_embd must be a multiple of 8 and n_ff of 64");
     if (c->precision == DTP_PREC_TF32 && (c->n_head * c->head_dim) % 4)
         return fail(DTP_ERR_UNSUPPORTED, "tf32 path: n_head*head_dim must be a multiple of 4");
-    if (c->precision == DTP_PREC_BF16) {
+    if (c->precision == DTP_PREC_E4M3 &&
+        ((c->n_head * c->head_dim) % 16 || c->n_embd % 16 || c->n_embd > 16384))
+        return fail(DTP_ERR_UNSUPPORTED,
+                    "e4m3 path: n_embd and n_head*head_dim must be multiples of 16, n_embd <= 16384");
+    if (c->precision == DTP_PREC_BF16 || c->precision == DTP_PREC_E4M3) {
         if (c->head_dim != 64 && c->head_dim != 128)
             return fail(DTP_ERR_UNSUPPORTED, "bf16 path: head_dim must be 64 or 128");
         if ((c->rope_dim_count / 2) % 32 || (c->head_dim - c->rope_dim_count) % 32)
@@ -145,16 +150,20 @@ static int validate_config(const dtp_config* c) {
 }
 
 struct PackedLayout {
-    size_t elt = 4;
+    size_t elt = 4;         // bytes per matrix element (1 for e4m3)
+    size_t emb_elt = 4;     // bytes per tok_embd element
     size_t attn_norm, w_qkv, q_norm, k_norm, wo, ffn_norm, w_gu, w_down;   // within a layer
+    size_t w_qkv_s = 0, wo_s = 0, w_gu_s = 0, w_down_s = 0;               // e4m3 row scales
     size_t layer_bytes;
-    size_t tok_embd, output_norm, output;                                 // absolute
+    size_t tok_embd, output_norm, output, output_s = 0;                   // absolute
     size_t total;
 };
 
 static PackedLayout packed_layout(const dtp_config* c) {
     PackedLayout L;
-    L.elt = c->precision == DTP_PREC_BF16 ? 2 : 4;
+    const bool e4 = c->precision == DTP_PREC_E4M3;
+    L.elt = c->precision == DTP_PREC_BF16 ? 2 : (e4 ? 1 : 4);
+    L.emb_elt = (c->precision == DTP_PREC_BF16 || e4) ? 2 : 4;
     const size_t d = c->n_embd, hd = c->head_dim, nq = (size_t)c->n_head * hd,
                  nqkv = (size_t)(c->n_head * (1 + c->attn_gate) + 2 * c->n_head_kv) * hd,
                  F = c->n_ff;
@@ -168,14 +177,21 @@ static PackedLayout packed_layout(const dtp_config* c) {
     L.wo = take(d * nq * L.elt);
     L.w_gu = take(2 * F * d * L.elt);
     L.w_down = take(d * F * L.elt);
+    if (e4) {       // one float32 scale per weight row (output channel)
+        L.w_qkv_s = take(nqkv * 4);
+        L.wo_s = take(d * 4);
+        L.w_gu_s = take(2 * F * 4);
+        L.w_down_s = take(d * 4);
+    }
     L.attn_norm = take(d * 4);
     L.q_norm = take(hd * 4);
     L.k_norm = take(hd * 4);
     L.ffn_norm = take(d * 4);
     L.layer_bytes = o;
     o = L.layer_bytes * c->n_layer;
-    L.tok_embd = take((size_t)c->n_vocab * d * L.elt);
+    L.tok_embd = take((size_t)c->n_vocab * d * L.emb_elt);
     L.output = take((size_t)c->n_vocab * d * L.elt);
+    if (e4) L.output_s = take((size_t)c->n_vocab * 4);
     L.output_norm = take(d * 4);
     L.total = o;
     return L;
@@ -185,6 +201,7 @@ struct Workspace {
     size_t x, h, qkv, attn, gu, act;            // f32 path
     size_t q, k, vt, rope, gate;                 // bf16 path
     long long ldvt;
+    size_t q8, s8;                               // e4m3 GEMM operand + row scales
     size_t tokens, logits;                       // _host staging
     size_t tile_start, vcol_start, last_row, tok_pos, tok_vcol;   // packed sequences
     size_t total;
@@ -196,7 +213,8 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_s
     Workspace W = {};
     const size_t d = c->n_embd, hd = c->head_dim, nq = (size_t)c->n_head * hd,
                  nk = (size_t)c->n_head_kv * hd, F = c->n_ff;
-    const bool bf = c->precision == DTP_PREC_BF16;
+    const bool e4 = c->precision == DTP_PREC_E4M3;
+    const bool bf = c->precision == DTP_PREC_BF16 || e4;    // e4m3 runs the bf16 path
     const size_t e = bf ? 2 : 4;
     size_t o = 256;     // first 256 bytes reserved
     auto take = [&](size_t bytes) {
@@ -215,6 +233,10 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_s
         W.vt = take(nk * (size_t)W.ldvt * 2);
         W.rope = take((size_t)T * (c->rope_dim_count / 2) * sizeof(float2));
         if (c->attn_gate) W.gate = take((size_t)T * nq * 2);
+        if (e4) {       // one operand buffer, reused by each GEMM in turn
+            W.q8 = take((size_t)T * std::max(std::max(d, nq), F));
+            W.s8 = take(align_up((size_t)T, 128) * 4);
+        }
     } else {
         W.qkv = take((size_t)T * (nq * (1 + c->attn_gate) + 2 * nk) * 4);
         W.gu = take((size_t)T * 2 * F * 4);
@@ -274,7 +296,7 @@ struct KvState {
 static KvState kv_state_layout(const dtp_config* c, int max_T) {
     KvState S;
     const size_t nk = (size_t)c->n_head_kv * c->head_dim;
-    if (c->precision == DTP_PREC_BF16) {
+    if (c->precision == DTP_PREC_BF16 || c->precision == DTP_PREC_E4M3) {
         S.ldvt = (long long)align_up((size_t)max_T, 8);
         S.v_off = align_up((size_t)max_T * nk * 2, 256);
         S.layer_bytes = S.v_off + align_up(nk * (size_t)S.ldvt * 2, 256);
@@ -405,6 +427,25 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
     float2* rope = (float2*)(ws + W.rope);
     const float scale = 1.0f / sqrtf((float)hd);
     const bool fa = attn_tc_supported(h, g, hd);
+    // DTP_PREC_E4M3: every GEMM input is quantised per row to e4m3 (q8, scales s8)
+    // and every weight is e4m3 with per-row scales; attention stays bf16
+    const bool e4 = c->precision == DTP_PREC_E4M3;
+    uint8_t* q8 = e4 ? ws + W.q8 : nullptr;
+    float* s8 = e4 ? (float*)(ws + W.s8) : nullptr;
+    // the GEMM A operand: bf16 `a`, or its e4m3 codes in q8 (b_scale: the weight's
+    // row scales)
+    auto gemm = [&](const bf* a, const uint8_t* w, const float* w_scale, int M, int N, int K,
+                    GemmEpi epi, GemmEpiArgs e, int kind) -> cudaError_t {
+        if (!e4) return launch_gemm_tc(a, (const bf*)w, M, N, K, epi, e, s, kind);
+        e.a_scale = s8;
+        e.b_scale = w_scale;
+        return launch_gemm_tc_e4m3(q8, w, M, N, K, epi, e, s, kind);
+    };
+    // RMSNorm straight to the next GEMM's operand (bf16 h, or e4m3 codes + scales)
+    auto norm = [&](const float* xin, const float* w, int rows, const int* row_idx) {
+        if (e4) return launch_rmsnorm_e4m3(xin, w, q8, s8, rows, d, c->rms_eps, s, row_idx);
+        return launch_rmsnorm(xin, w, hb, DTP_BF16, rows, d, c->rms_eps, s, row_idx);
+    };
     // packed sequences: v^T blocks start on 8-column boundaries; the padding
     // columns between them are read by attention (with P = 0), so they are zeroed
     long long vt_cols = T;
@@ -433,8 +474,7 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         const uint8_t* lp = P + (size_t)l * L.layer_bytes;
         if (hidden)
             DTP_CUDA_CHECK(launch_copy_f32(x, hidden + (size_t)l * T * d, (size_t)T * d, s));
-        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.attn_norm), hb, DTP_BF16, T, d,
-                                      c->rms_eps, s));
+        DTP_CUDA_CHECK(norm(x, (const float*)(lp + L.attn_norm), T, nullptr));
         GemmEpiArgs e;
         // with a KV cache the keys are written straight into it (attention reads them
         // there); a chunk writes its keys and values into the state at position p0
@@ -461,8 +501,8 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         e.head_dim = hd;
         e.rope_dims = c->rope_dim_count;
         e.eps = c->rms_eps;
-        DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(lp + L.w_qkv), T, nqkv, d, EPI_QKV, e, s,
-                                      DTP_K_GEMM_QKV));
+        DTP_CUDA_CHECK(gemm(hb, lp + L.w_qkv, (const float*)(lp + L.w_qkv_s), T, nqkv, d, EPI_QKV,
+                            e, DTP_K_GEMM_QKV));
         if (fa)
             DTP_CUDA_CHECK(launch_attn_tc_varlen(q, kl, vtl, ldvt, vt_cols, attn, T, h, g, hd,
                                                  scale, vl, s));
@@ -474,16 +514,17 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         eo.y_dtype = DTP_F32;
         eo.ldy = d;
         eo.residual = x;
-        DTP_CUDA_CHECK(launch_gemm_tc(attn, (const bf*)(lp + L.wo), T, d, nq, EPI_STORE, eo, s,
-                                      DTP_K_GEMM_O));
-        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(lp + L.ffn_norm), hb, DTP_BF16, T, d,
-                                      c->rms_eps, s));
+        if (e4) DTP_CUDA_CHECK(launch_quant_rows_e4m3(attn, nq, T, nq, q8, s8, s));
+        DTP_CUDA_CHECK(gemm(attn, lp + L.wo, (const float*)(lp + L.wo_s), T, d, nq, EPI_STORE, eo,
+                            DTP_K_GEMM_O));
+        DTP_CUDA_CHECK(norm(x, (const float*)(lp + L.ffn_norm), T, nullptr));
         GemmEpiArgs eg;
         eg.act = act;
-        DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(lp + L.w_gu), T, 2 * F, d, EPI_SWIGLU, eg, s,
-                                      DTP_K_GEMM_GATEUP));
-        DTP_CUDA_CHECK(launch_gemm_tc(act, (const bf*)(lp + L.w_down), T, d, F, EPI_STORE, eo, s,
-                                      DTP_K_GEMM_DOWN));
+        DTP_CUDA_CHECK(gemm(hb, lp + L.w_gu, (const float*)(lp + L.w_gu_s), T, 2 * F, d, EPI_SWIGLU,
+                            eg, DTP_K_GEMM_GATEUP));
+        if (e4) DTP_CUDA_CHECK(launch_quant_rows_e4m3(act, F, T, F, q8, s8, s));
+        DTP_CUDA_CHECK(gemm(act, lp + L.w_down, (const float*)(lp + L.w_down_s), T, d, F, EPI_STORE,
+                            eo, DTP_K_GEMM_DOWN));
     }
     if (hidden)
         DTP_CUDA_CHECK(
@@ -493,19 +534,17 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
     int rows = o.last_only ? 1 : T;
     if (o.last_only && V.n_seq) {
         rows = V.n_seq;
-        DTP_CUDA_CHECK(launch_rmsnorm(x, (const float*)(P + L.output_norm), hb, DTP_BF16, rows, d,
-                                      c->rms_eps, s, V.last_row));
+        DTP_CUDA_CHECK(norm(x, (const float*)(P + L.output_norm), rows, V.last_row));
     } else {
-        DTP_CUDA_CHECK(launch_rmsnorm(x + (size_t)(T - rows) * d,
-                                      (const float*)(P + L.output_norm), hb, DTP_BF16, rows, d,
-                                      c->rms_eps, s));
+        DTP_CUDA_CHECK(norm(x + (size_t)(T - rows) * d, (const float*)(P + L.output_norm), rows,
+                            nullptr));
     }
     GemmEpiArgs el;
     el.y = logits;
     el.y_dtype = DTP_F32;
     el.ldy = c->n_vocab;
-    DTP_CUDA_CHECK(launch_gemm_tc(hb, (const bf*)(P + L.output), rows, c->n_vocab, d, EPI_STORE, el,
-                                  s, DTP_K_GEMM_LMHEAD));
+    DTP_CUDA_CHECK(gemm(hb, P + L.output, (const float*)(P + L.output_s), rows, c->n_vocab, d,
+                        EPI_STORE, el, DTP_K_GEMM_LMHEAD));
     return DTP_OK;
 }
 
@@ -551,6 +590,22 @@ int dtp_pack_layer(const dtp_config* cfg, int layer, const dtp_layer_src* src, v
     const int d = cfg->n_embd, hd = cfg->head_dim, nq = cfg->n_head * hd,
               nk = cfg->n_head_kv * hd, F = cfg->n_ff;
     const int nqc = nq * (1 + cfg->attn_gate);      // q rows (with the per-head gate rows)
+    if (cfg->precision == DTP_PREC_E4M3) {
+        // e4m3 codes with one float32 scale per row; same row order as below
+        uint8_t* qkv = lp + L.w_qkv;
+        float* qkv_s = (float*)(lp + L.w_qkv_s);
+        DTP_CUDA_CHECK(launch_pack_e4m3(src->wq, nqc, d, qkv, qkv_s, 0, s));
+        DTP_CUDA_CHECK(launch_pack_e4m3(src->wk, nk, d, qkv + (size_t)nqc * d, qkv_s + nqc, 0, s));
+        DTP_CUDA_CHECK(launch_pack_e4m3(src->wv, nk, d, qkv + (size_t)(nqc + nk) * d,
+                                        qkv_s + nqc + nk, 0, s));
+        DTP_CUDA_CHECK(launch_pack_e4m3(src->wo, d, nq, lp + L.wo, (float*)(lp + L.wo_s), 0, s));
+        DTP_CUDA_CHECK(launch_pack_e4m3(src->w_gate, F, d, lp + L.w_gu, (float*)(lp + L.w_gu_s),
+                                        1, s));
+        DTP_CUDA_CHECK(launch_pack_e4m3(src->w_up, F, d, lp + L.w_gu, (float*)(lp + L.w_gu_s), 2,
+                                        s));
+        DTP_CUDA_CHECK(launch_pack_e4m3(src->w_down, d, F, lp + L.w_down,
+                                        (float*)(lp + L.w_down_s), 0, s));
+    } else {
     DTP_CUDA_CHECK(launch_pack_matrix(src->wq, nqc, d, lp + L.w_qkv, bf, 0, s));
     DTP_CUDA_CHECK(launch_pack_matrix(src->wk, nk, d, lp + L.w_qkv + (size_t)nqc * d * L.elt, bf, 0, s));
     DTP_CUDA_CHECK(launch_pack_matrix(src->wv, nk, d, lp + L.w_qkv + (size_t)(nqc + nk) * d * L.elt,
@@ -559,6 +614,7 @@ int dtp_pack_layer(const dtp_config* cfg, int layer, const dtp_layer_src* src, v
     DTP_CUDA_CHECK(launch_pack_matrix(src->w_gate, F, d, lp + L.w_gu, bf, 1, s));
     DTP_CUDA_CHECK(launch_pack_matrix(src->w_up, F, d, lp + L.w_gu, bf, 2, s));
     DTP_CUDA_CHECK(launch_pack_matrix(src->w_down, d, F, lp + L.w_down, bf, 0, s));
+    }
     DTP_CUDA_CHECK(launch_pack_matrix(src->attn_norm, 1, d, lp + L.attn_norm, 0, 0, s));
     DTP_CUDA_CHECK(launch_pack_matrix(src->q_norm, 1, hd, lp + L.q_norm, 0, 0, s));
     DTP_CUDA_CHECK(launch_pack_matrix(src->k_norm, 1, hd, lp + L.k_norm, 0, 0, s));
@@ -579,10 +635,15 @@ int dtp_pack_globals(const dtp_config* cfg, const float* tok_embd, const float* 
     if (!aligned(packed, 256)) return fail(DTP_ERR_INVALID_ARG, "packed must be 256-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     uint8_t* P = (uint8_t*)packed;
-    const int bf = cfg->precision == DTP_PREC_BF16 ? DTP_BF16 : DTP_F32;
+    const bool e4 = cfg->precision == DTP_PREC_E4M3;
+    const int bf = (cfg->precision == DTP_PREC_BF16 || e4) ? DTP_BF16 : DTP_F32;
     const int mat = cfg->precision == DTP_PREC_TF32 ? DTP_TF32 : bf;    // tok_embd is no GEMM operand
     DTP_CUDA_CHECK(launch_pack_matrix(tok_embd, cfg->n_vocab, cfg->n_embd, P + L.tok_embd, bf, 0, s));
-    DTP_CUDA_CHECK(launch_pack_matrix(output, cfg->n_vocab, cfg->n_embd, P + L.output, mat, 0, s));
+    if (e4)
+        DTP_CUDA_CHECK(launch_pack_e4m3(output, cfg->n_vocab, cfg->n_embd, P + L.output,
+                                        (float*)(P + L.output_s), 0, s));
+    else
+        DTP_CUDA_CHECK(launch_pack_matrix(output, cfg->n_vocab, cfg->n_embd, P + L.output, mat, 0, s));
     DTP_CUDA_CHECK(launch_pack_matrix(output_norm, 1, cfg->n_embd, P + L.output_norm, 0, 0, s));
     return DTP_OK;
 }
@@ -618,19 +679,19 @@ static int fwd_checked(const dtp_config* cfg, const void* packed, size_t packed_
     Workspace W = workspace_layout(cfg, T, host_layout, n_seq);
     if (ws_bytes < W.total)
         return fail(DTP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, W.total);
-    if (cfg->precision == DTP_PREC_BF16 && !attn_tc_supported(cfg->n_head, cfg->n_head_kv,
-                                                              cfg->head_dim))
+    const bool tc_path = cfg->precision == DTP_PREC_BF16 || cfg->precision == DTP_PREC_E4M3;
+    if (tc_path && !attn_tc_supported(cfg->n_head, cfg->n_head_kv, cfg->head_dim))
         return fail(DTP_ERR_UNSUPPORTED, "bf16 path: n_head / n_head_kv must be even");
     if (!aligned(workspace, 256) || !aligned(packed, 256) || (logits && !aligned(logits, 16)) ||
         (hidden && !aligned(hidden, 16)) || (out.k_cache && !aligned(out.k_cache, 16)) ||
         (out.v_cache && !aligned(out.v_cache, 16)))
         return fail(DTP_ERR_INVALID_ARG,
                     "workspace/packed must be 256-byte aligned, outputs 16-byte aligned");
-    if (cfg->precision == DTP_PREC_BF16 && (cfg->n_vocab % 4))
+    if (tc_path && (cfg->n_vocab % 4))
         return fail(DTP_ERR_UNSUPPORTED, "bf16 path: n_vocab must be a multiple of 4");
     cudaStream_t s = (cudaStream_t)stream;
     const VarlenCtx V = varlen_ctx(W, (uint8_t*)workspace, n_seq, cu_seqlens);
-    if (cfg->precision == DTP_PREC_BF16)
+    if (tc_path)
         return fwd_bf16(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, V,
                         S, s);
     return fwd_f32(cfg, (const uint8_t*)packed, L, tokens, T, out, (uint8_t*)workspace, W, V, S,
@@ -864,6 +925,54 @@ int dtp_linear(const void* x, const void* W, void* y, int dtype, int y_dtype, in
     e.residual = residual;
     DTP_CUDA_CHECK(launch_gemm_tc((const __nv_bfloat16*)x, (const __nv_bfloat16*)W, M, N, K,
                                   EPI_STORE, e, s, DTP_K_OTHER));
+    return DTP_OK;
+}
+
+int dtp_quantize_rows_e4m3(const void* x, int dtype, int rows, int cols, uint8_t* q, float* scale,
+                           dtp_stream_t stream) {
+    if (!x || !q || !scale) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    if (rows <= 0 || cols <= 0) return fail(DTP_ERR_INVALID_ARG, "rows and cols must be >= 1");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == DTP_F32) {      // the weight-packing kernel quantises float32 rows
+        DTP_CUDA_CHECK(launch_pack_e4m3((const float*)x, rows, cols, q, scale, 0, s));
+        return DTP_OK;
+    }
+    if (dtype != DTP_BF16) return fail(DTP_ERR_INVALID_ARG, "bad dtype");
+    if (cols % 8 || !aligned(x, 16) || !aligned(q, 8))
+        return fail(DTP_ERR_UNSUPPORTED, "bf16 rows: cols %% 8 == 0, x 16- and q 8-byte aligned");
+    DTP_CUDA_CHECK(launch_quant_rows_e4m3((const __nv_bfloat16*)x, cols, rows, cols, q, scale, s));
+    return DTP_OK;
+}
+
+int dtp_rms_norm_e4m3(const float* x, const float* w, uint8_t* q, float* scale, int rows, int cols,
+                      float eps, dtp_stream_t stream) {
+    if (!x || !w || !q || !scale) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    if (rows <= 0 || cols <= 0) return fail(DTP_ERR_INVALID_ARG, "rows and cols must be >= 1");
+    if (!(eps >= 0.f)) return fail(DTP_ERR_INVALID_ARG, "eps must be >= 0");
+    if (cols % 4 || cols > 16384 || !aligned(x, 16) || !aligned(w, 16) || !aligned(q, 4))
+        return fail(DTP_ERR_UNSUPPORTED,
+                    "cols %% 4 == 0 and <= 16384, x/w 16-byte and q 4-byte aligned");
+    DTP_CUDA_CHECK(launch_rmsnorm_e4m3(x, w, q, scale, rows, cols, eps, (cudaStream_t)stream));
+    return DTP_OK;
+}
+
+int dtp_linear_e4m3(const uint8_t* xq, const float* x_scale, const uint8_t* wq,
+                    const float* w_scale, float* y, int M, int N, int K, const float* residual,
+                    dtp_stream_t stream) {
+    if (!xq || !x_scale || !wq || !w_scale || !y) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
+    if (M <= 0 || N <= 0 || K <= 0) return fail(DTP_ERR_INVALID_ARG, "M, N, K must be >= 1");
+    if (K % 16) return fail(DTP_ERR_UNSUPPORTED, "e4m3 linear: K must be a multiple of 16");
+    if (!aligned(xq, 16) || !aligned(wq, 16))
+        return fail(DTP_ERR_INVALID_ARG, "e4m3 linear: xq and wq must be 16-byte aligned");
+    GemmEpiArgs e;
+    e.y = y;
+    e.y_dtype = DTP_F32;
+    e.ldy = N;
+    e.residual = residual;
+    e.a_scale = x_scale;
+    e.b_scale = w_scale;
+    DTP_CUDA_CHECK(launch_gemm_tc_e4m3(xq, wq, M, N, K, EPI_STORE, e, (cudaStream_t)stream,
+                                       DTP_K_OTHER));
     return DTP_OK;
 }
 

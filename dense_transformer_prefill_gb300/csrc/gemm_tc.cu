@@ -6,11 +6,15 @@
 //   EPI_QKV     per-head QK-RMSNorm + NeoX RoPE on q and k, v stored transposed
 //   EPI_SWIGLU  silu(gate) * up on the interleaved gate/up product (`ffn_act`)
 //
-// D[M, N] = A[M, K] B[N, K]^T with A = activations, B = weights, both bf16 (or
-// both float32 holding tf32 values: kind::tf32, EPI_STORE only) and
-// K-contiguous.  One persistent CTA per SM walks 128 x BN output tiles:
-//   warp 0      TMA producer: 128x64 A and BNx64 B boxes (128-byte swizzle; 32
-//               elements of K per 128-byte row for tf32) into
+// D[M, N] = A[M, K] B[N, K]^T with A = activations, B = weights, both
+// K-contiguous and of one operand kind:
+//   OP_BF16  bf16 (kind::f16)
+//   OP_TF32  float32 holding tf32 values (kind::tf32; EPI_STORE only)
+//   OP_E4M3  e4m3 with a float32 scale per A row and per B row (kind::f8f6f4):
+//            the epilogue reads s_a[m] * s_b[n] * acc[m, n]
+// A stage holds 128 bytes of K per row (64 bf16, 32 tf32, 128 e4m3).  One
+// persistent CTA per SM walks 128 x BN output tiles:
+//   warp 0      TMA producer: 128-row A and BN-row B boxes (128-byte swizzle) into
 //               a STAGES-deep shared-memory ring (mbarrier full/empty pairs)
 //   warp 1      one thread issues tcgen05.mma (M=128, N=BN, K=16) into a TMEM
 //               accumulator; two accumulators (2*BN columns) so the epilogue of
@@ -110,6 +114,24 @@ __device__ __forceinline__ uint4 stage_get16(const uint8_t* buf, int lane, int c
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
+// Accumulator columns taddr .. taddr+31 of this thread's row (TMEM address
+// taddr = tbase + column offset in the tile), scaled by s_a[row] * s_b[col]
+// when the operands carry scales (SC: OP_E4M3).  Whole warp.
+template <bool SC>
+__device__ __forceinline__ void acc_ld32(const Params& p, uint32_t tbase, uint32_t taddr, int grow,
+                                         int n0, uint32_t (&r)[32]) {
+    ptx::tmem_ld32(taddr, r);
+    if constexpr (SC) {
+        const int col = n0 + (int)(taddr - tbase);
+        const float sa = grow < p.M ? p.ea.a_scale[grow] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float sb = col + j < p.N ? p.ea.b_scale[col + j] : 0.f;
+            r[j] = __float_as_uint(f32(r[j]) * (sa * sb));
+        }
+    }
+}
+
 // Store 32 consecutive floats (as float or bf16) to dst (16-byte aligned when vec).
 __device__ __forceinline__ void store_row32(float* dst, const float (&v)[32]) {
 #pragma unroll
@@ -131,14 +153,14 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // ----------------------------------------------------------------------------- epilogues
-template <int BN>
+template <int BN, bool SC>
 __device__ __forceinline__ void epi_store(const Params& p, uint32_t tbase, int grow, int n0) {
     const GemmEpiArgs& ea = p.ea;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
         __syncwarp();
-        ptx::tmem_ld32(tbase + c, r);
+        acc_ld32<SC>(p, tbase, tbase + c, grow, n0, r);
         const int col0 = n0 + c;
         if (col0 >= p.N) break;                     // warp-uniform
         if (grow >= p.M) continue;                  // the next tcgen05.ld reconverges below
@@ -173,7 +195,7 @@ __device__ __forceinline__ void epi_store(const Params& p, uint32_t tbase, int g
 
 // q/k heads: RMSNorm over head_dim with q_norm/k_norm, then NeoX RoPE from the
 // cos/sin table; v heads: stored transposed (key index contiguous).
-template <int BN>
+template <int BN, bool SC>
 __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int grow, int n0) {
     const GemmEpiArgs& ea = p.ea;
     const int hd = ea.head_dim, half = ea.rope_dims / 2;
@@ -192,7 +214,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + c, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
                 if (live) {
                     float y[32];
 #pragma unroll
@@ -211,7 +233,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + c, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ss = fmaf(f32(r[j]), f32(r[j]), ss);
             }
@@ -222,8 +244,8 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int i0 = 0; i0 < half; i0 += 32) {
                 uint32_t ra[32], rb[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + i0, ra);
-                ptx::tmem_ld32(th + half + i0, rb);
+                acc_ld32<SC>(p, tbase, th + i0, grow, n0, ra);
+                acc_ld32<SC>(p, tbase, th + half + i0, grow, n0, rb);
                 if (live) {
                     const int pos = ea.tok_pos ? ea.tok_pos[grow] : grow;
                     const float2* cs = ea.rope + (size_t)pos * half + i0;
@@ -244,7 +266,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int c = ea.rope_dims; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + c, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
                 if (live) {
                     float y[32];
 #pragma unroll
@@ -258,7 +280,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + c, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
                 if (live) {
                     const int tcol = ea.tok_vcol ? ea.tok_vcol[grow] : grow;
                     __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
@@ -279,7 +301,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
 
 // gate/up interleaved in 64-column blocks: block b of the product holds gate
 // columns 64b..64b+63 then up columns 64b..64b+63; act[:, 64b + j] = silu(g) * u.
-template <int BN>
+template <int BN, bool SC>
 __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, int grow, int n0) {
     const GemmEpiArgs& ea = p.ea;
     const int F = p.N / 2;
@@ -292,8 +314,8 @@ __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, int 
         for (int c = 0; c < 64; c += 32) {
             uint32_t rg[32], ru[32];
             __syncwarp();
-            ptx::tmem_ld32(tbase + b + c, rg);
-            ptx::tmem_ld32(tbase + b + 64 + c, ru);
+            acc_ld32<SC>(p, tbase, tbase + b + c, grow, n0, rg);
+            acc_ld32<SC>(p, tbase, tbase + b + 64 + c, grow, n0, ru);
             if (grow < p.M) {
                 float a[32];
 #pragma unroll
@@ -344,7 +366,7 @@ __device__ __forceinline__ void stage_prefetch(EpiStage& st, int b, const CUtens
 
 // y = acc (+ residual): float32 chunks of 32 columns or bf16 chunks of 64.
 // BN must be a multiple of the chunk width (32 for float32, 64 for bf16 output).
-template <int BN>
+template <int BN, bool SC>
 __device__ __forceinline__ bool epi_store_tma(const Params& p, EpiStage& st, uint32_t tbase, int n0,
                                               const CUtensorMap* tmY, const CUtensorMap* tmR,
                                               volatile int* abort_flag) {
@@ -352,6 +374,7 @@ __device__ __forceinline__ bool epi_store_tma(const Params& p, EpiStage& st, uin
     const bool f32out = ea.y_dtype == DTP_F32;
     const bool resid = ea.residual != nullptr;
     const int CW = f32out ? 32 : 64;
+    const int grow = st.row0 + st.lane;
 #pragma unroll 1
     for (int c = 0; c < BN; c += CW) {
         const int col0 = n0 + c;
@@ -367,12 +390,12 @@ __device__ __forceinline__ bool epi_store_tma(const Params& p, EpiStage& st, uin
         float v[64];
         uint32_t r[32];
         __syncwarp();
-        ptx::tmem_ld32(tbase + c, r);
+        acc_ld32<SC>(p, tbase, tbase + c, grow, n0, r);
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = f32(r[j]);
         if (!f32out) {
             __syncwarp();
-            ptx::tmem_ld32(tbase + c + 32, r);
+            acc_ld32<SC>(p, tbase, tbase + c + 32, grow, n0, r);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[32 + j] = f32(r[j]);
         }
@@ -408,9 +431,10 @@ __device__ __forceinline__ bool epi_store_tma(const Params& p, EpiStage& st, uin
 }
 
 // gate/up (interleaved 64-column blocks) -> act = silu(g) * u, bf16 boxes of 64 columns.
-template <int BN>
+template <int BN, bool SC>
 __device__ __forceinline__ void epi_swiglu_tma(const Params& p, EpiStage& st, uint32_t tbase,
                                                int n0, const CUtensorMap* tmY) {
+    const int grow = st.row0 + st.lane;
 #pragma unroll 1
     for (int b = 0; b < BN; b += 128) {
         const int colblk = n0 + b;
@@ -421,8 +445,8 @@ __device__ __forceinline__ void epi_swiglu_tma(const Params& p, EpiStage& st, ui
         for (int c = 0; c < 64; c += 32) {
             uint32_t rg[32], ru[32];
             __syncwarp();
-            ptx::tmem_ld32(tbase + b + c, rg);
-            ptx::tmem_ld32(tbase + b + 64 + c, ru);
+            acc_ld32<SC>(p, tbase, tbase + b + c, grow, n0, rg);
+            acc_ld32<SC>(p, tbase, tbase + b + 64 + c, grow, n0, ru);
             float a[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] = silu_f(f32(rg[j])) * f32(ru[j]);
@@ -436,7 +460,7 @@ __device__ __forceinline__ void epi_swiglu_tma(const Params& p, EpiStage& st, ui
 
 // QKV: q/k heads normalised and rotated, staged as 64-column bf16 boxes (one or
 // two per head); v heads (transposed) and gate blocks stored directly.
-template <int BN>
+template <int BN, bool SC>
 __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint32_t tbase,
                                             int grow, int n0, const CUtensorMap* tmQ,
                                             const CUtensorMap* tmK) {
@@ -456,7 +480,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + c, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
                 if (live) {
                     float y[32];
 #pragma unroll
@@ -475,7 +499,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + c, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ss = fmaf(f32(r[j]), f32(r[j]), ss);
             }
@@ -488,8 +512,8 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int i0 = 0; i0 < half; i0 += 32) {
                 uint32_t ra[32], rb[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + i0, ra);
-                ptx::tmem_ld32(th + half + i0, rb);
+                acc_ld32<SC>(p, tbase, th + i0, grow, n0, ra);
+                acc_ld32<SC>(p, tbase, th + half + i0, grow, n0, rb);
                 const float2* cs = ea.rope + (size_t)(live ? pos : 0) * half + i0;
                 float ya[32], yb[32];
 #pragma unroll
@@ -511,7 +535,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int c = ea.rope_dims; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + c, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
                 float y[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) y[j] = f32(r[j]) * rstd * w[c + j];
@@ -532,7 +556,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                ptx::tmem_ld32(th + c, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
                 if (live) {
                     const int tcol = ea.tok_vcol ? ea.tok_vcol[grow] : grow;
                     __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
@@ -552,7 +576,9 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
 }
 
 // ----------------------------------------------------------------------------- kernel
-template <int BN, int EPI, bool TF = false>
+enum { OP_BF16 = 0, OP_TF32 = 1, OP_E4M3 = 2 };
+
+template <int BN, int EPI, int OPK = OP_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmY2,
@@ -621,8 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            ERRBIT_TIMEOUT))
                         goto producer_done;
                     ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    // a stage holds 128 bytes of K per row: 64 bf16 or 32 tf32
-                    const int k0 = kb * (TF ? BK / 2 : BK);
+                    // a stage holds 128 bytes of K per row: 64 bf16, 32 tf32, 128 e4m3
+                    const int k0 = kb * (OPK == OP_TF32 ? BK / 2 : OPK == OP_E4M3 ? 2 * BK : BK);
                     ptx::tma_load_2d(&tmA, &full[stage], sA + stage * C::A_BYTES, k0, mb * BM);
                     ptx::tma_load_2d(&tmB, &full[stage], sB + stage * C::B_BYTES, k0, nb * BN);
                     ++issued;
@@ -650,7 +676,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = TF ? ptx::idesc_tf32_f32(BM, BN) : ptx::idesc_bf16_f32(BM, BN);
+            const uint32_t idesc = OPK == OP_TF32   ? ptx::idesc_tf32_f32(BM, BN)
+                                   : OPK == OP_E4M3 ? ptx::idesc_e4m3_f32(BM, BN)
+                                                    : ptx::idesc_bf16_f32(BM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -675,8 +703,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the descriptor's 16-byte address units)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        if constexpr (TF)
+                        if constexpr (OPK == OP_TF32)
                             ptx::umma_tf32_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                              (kb > 0 || kk > 0) ? 1u : 0u);
+                        else if constexpr (OPK == OP_E4M3)
+                            ptx::umma_e4m3_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
                                               (kb > 0 || kk > 0) ? 1u : 0u);
                         else
                             ptx::umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
@@ -729,13 +760,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool eok = true;
             if (tma_out) {
                 if (EPI == EPI_STORE)
-                    eok = epi_store_tma<BN>(p, st, tbase, n0, &tmY, &tmR, abort_flag);
-                if (EPI == EPI_QKV) epi_qkv_tma<BN>(p, st, tbase, grow, n0, &tmY, &tmY2);
-                if (EPI == EPI_SWIGLU) epi_swiglu_tma<BN>(p, st, tbase, n0, &tmY);
+                    eok = epi_store_tma<BN, OPK == OP_E4M3>(p, st, tbase, n0, &tmY, &tmR, abort_flag);
+                if (EPI == EPI_QKV) epi_qkv_tma<BN, OPK == OP_E4M3>(p, st, tbase, grow, n0, &tmY, &tmY2);
+                if (EPI == EPI_SWIGLU) epi_swiglu_tma<BN, OPK == OP_E4M3>(p, st, tbase, n0, &tmY);
             } else {
-                if (EPI == EPI_STORE) epi_store<BN>(p, tbase, grow, n0);
-                if (EPI == EPI_QKV) epi_qkv<BN>(p, tbase, grow, n0);
-                if (EPI == EPI_SWIGLU) epi_swiglu<BN>(p, tbase, grow, n0);
+                if (EPI == EPI_STORE) epi_store<BN, OPK == OP_E4M3>(p, tbase, grow, n0);
+                if (EPI == EPI_QKV) epi_qkv<BN, OPK == OP_E4M3>(p, tbase, grow, n0);
+                if (EPI == EPI_SWIGLU) epi_swiglu<BN, OPK == OP_E4M3>(p, tbase, grow, n0);
             }
             __syncwarp();
             ptx::tc_fence_before();
@@ -766,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, int EPI, bool TF = false>
+template <int BN, int EPI, int OPK = OP_BF16>
 cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                         const CUtensorMap& ty2, const CUtensorMap& tr, const Params& p,
                         cudaStream_t s) {
@@ -774,14 +805,14 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, TF>,
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, OPK>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    gemm_tc_kernel<BN, EPI, TF><<<grid, kThreads, C::SMEM_BYTES, s>>>(ta, tb, ty, ty2, tr, p);
+    gemm_tc_kernel<BN, EPI, OPK><<<grid, kThreads, C::SMEM_BYTES, s>>>(ta, tb, ty, ty2, tr, p);
     return cudaGetLastError();
 }
 
@@ -801,15 +832,17 @@ static int pick_bn(int M, int N, GemmEpi epi, int y_dtype) {
     return 20 * cost(224) < 19 * cost(256) ? 224 : 256;
 }
 
-static cudaError_t launch_gemm(const void* x, const void* W, bool tf32, int M, int N, int K,
+static cudaError_t launch_gemm(const void* x, const void* W, int opk, int M, int N, int K,
                                GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind) {
+    const bool tf32 = opk == OP_TF32, e4m3 = opk == OP_E4M3;
     int BN = pick_bn(M, N, epi, ea.y_dtype);
     if (tf32 && BN == 224) BN = 256;         // tf32 instantiates the 256 and 128 tiles only
-    // operand boxes: 128 bytes of K per row (64 bf16 or 32 float32)
-    const int bke = tf32 ? BK / 2 : BK;
-    const CUtensorMapDataType odt =
-        tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const int oeb = tf32 ? 4 : 2;
+    // operand boxes: 128 bytes of K per row (64 bf16, 32 float32 or 128 e4m3)
+    const int bke = tf32 ? BK / 2 : e4m3 ? 2 * BK : BK;
+    const CUtensorMapDataType odt = tf32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                    : e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int oeb = tf32 ? 4 : e4m3 ? 1 : 2;
     CUtensorMap ta, tb;
     if (!make_tmap_2d(&ta, x, odt, oeb, M, K, K, BM, bke)) return cudaErrorInvalidValue;
     if (!make_tmap_2d(&tb, W, odt, oeb, N, K, K, BN, bke)) return cudaErrorInvalidValue;
@@ -850,8 +883,18 @@ static cudaError_t launch_gemm(const void* x, const void* W, bool tf32, int M, i
     LaunchScope ls(kind, s);
     if (tf32) {
         if (epi != EPI_STORE) return cudaErrorNotSupported;
-        if (BN == 256) return launch_impl<256, EPI_STORE, true>(ta, tb, ty, ty2, tr, p, s);
-        return launch_impl<128, EPI_STORE, true>(ta, tb, ty, ty2, tr, p, s);
+        if (BN == 256) return launch_impl<256, EPI_STORE, OP_TF32>(ta, tb, ty, ty2, tr, p, s);
+        return launch_impl<128, EPI_STORE, OP_TF32>(ta, tb, ty, ty2, tr, p, s);
+    }
+    if (e4m3) {
+        if (BN == 256) {
+            if (epi == EPI_QKV) return launch_impl<256, EPI_QKV, OP_E4M3>(ta, tb, ty, ty2, tr, p, s);
+            if (epi == EPI_SWIGLU)
+                return launch_impl<256, EPI_SWIGLU, OP_E4M3>(ta, tb, ty, ty2, tr, p, s);
+            return launch_impl<256, EPI_STORE, OP_E4M3>(ta, tb, ty, ty2, tr, p, s);
+        }
+        if (BN == 224) return launch_impl<224, EPI_STORE, OP_E4M3>(ta, tb, ty, ty2, tr, p, s);
+        return launch_impl<128, EPI_STORE, OP_E4M3>(ta, tb, ty, ty2, tr, p, s);
     }
     if (BN == 256) {
         if (epi == EPI_QKV) return launch_impl<256, EPI_QKV>(ta, tb, ty, ty2, tr, p, s);
@@ -864,12 +907,22 @@ static cudaError_t launch_gemm(const void* x, const void* W, bool tf32, int M, i
 
 cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,
                            GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind) {
-    return launch_gemm(x, W, false, M, N, K, epi, ea, s, kind);
+    GemmEpiArgs e = ea;
+    e.a_scale = e.b_scale = nullptr;
+    return launch_gemm(x, W, OP_BF16, M, N, K, epi, e, s, kind);
 }
 
 cudaError_t launch_gemm_tc_tf32(const float* x, const float* W, int M, int N, int K,
                                 const GemmEpiArgs& ea, cudaStream_t s, int kind) {
-    return launch_gemm(x, W, true, M, N, K, EPI_STORE, ea, s, kind);
+    GemmEpiArgs e = ea;
+    e.a_scale = e.b_scale = nullptr;
+    return launch_gemm(x, W, OP_TF32, M, N, K, EPI_STORE, e, s, kind);
+}
+
+cudaError_t launch_gemm_tc_e4m3(const uint8_t* x, const uint8_t* W, int M, int N, int K,
+                                GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind) {
+    if (!ea.a_scale || !ea.b_scale) return cudaErrorInvalidValue;
+    return launch_gemm(x, W, OP_E4M3, M, N, K, epi, ea, s, kind);
 }
 
 }  // namespace dtp

@@ -69,6 +69,15 @@ cudaError_t launch_swiglu(const void* gate, const void* up, void* out, int dtype
 cudaError_t launch_swiglu_interleaved64(const float* gu, float* act, int T, int F,
                                         cudaStream_t s, int act_dtype = DTP_F32);
 cudaError_t launch_round_tf32(float* x, size_t n, cudaStream_t s);
+// Per-row e4m3 quantisation (quant.cu): codes q [rows, cols] (row-major, no
+// padding) and scale [rows] = max|row| / 448.
+cudaError_t launch_rmsnorm_e4m3(const float* x, const float* w, uint8_t* q, float* scale,
+                                int rows, int cols, float eps, cudaStream_t s,
+                                const int* row_idx = nullptr);
+cudaError_t launch_quant_rows_e4m3(const __nv_bfloat16* x, int ldx, int rows, int cols,
+                                   uint8_t* q, float* scale, cudaStream_t s);
+cudaError_t launch_pack_e4m3(const float* src, int rows, int cols, uint8_t* dst, float* dst_scale,
+                             int mode, cudaStream_t s);
 cudaError_t launch_gemm_simt(const float* x, int ldx, const float* W, void* y, int y_dtype,
                              int ldy, int M, int N, int K, const float* residual,
                              cudaStream_t s, int kind);
@@ -106,6 +115,9 @@ enum GemmEpi {
 };
 
 struct GemmEpiArgs {
+    // e4m3 operands: y = a_scale[m] * b_scale[n] * (A B^T)[m, n] before the epilogue
+    const float* a_scale = nullptr;   // [M]
+    const float* b_scale = nullptr;   // [N]
     // EPI_STORE
     void* y = nullptr;
     int y_dtype = DTP_F32;
@@ -137,6 +149,10 @@ cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M
 // EPI_STORE epilogue (float32 y, optional residual); K a multiple of 4.
 cudaError_t launch_gemm_tc_tf32(const float* x, const float* W, int M, int N, int K,
                                 const GemmEpiArgs& ea, cudaStream_t s, int kind);
+// The same GEMM on e4m3 operands (tcgen05 kind::f8f6f4) with a float32 scale per
+// row of x (ea.a_scale, [M]) and per row of W (ea.b_scale, [N]); K % 16 == 0.
+cudaError_t launch_gemm_tc_e4m3(const uint8_t* x, const uint8_t* W, int M, int N, int K,
+                                GemmEpi epi, const GemmEpiArgs& ea, cudaStream_t s, int kind);
 
 cudaError_t launch_selftest_wait(cudaStream_t s);
 

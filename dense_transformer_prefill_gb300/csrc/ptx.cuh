@@ -170,6 +170,24 @@ __host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with e4m3 A/B (format 0), f32 D, both
+// K-major.  One MMA consumes K = 32 e4m3 (32 bytes of each row).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T on e4m3 operands, one elected thread.
+__device__ __forceinline__ void umma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T on tf32 operands (f32 in shared memory; the
 // operands are rounded to tf32 by their producers), one elected thread.
 __device__ __forceinline__ void umma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,

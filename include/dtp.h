@@ -67,8 +67,15 @@ enum { DTP_F32 = 0, DTP_BF16 = 1, DTP_TF32 = 2 };
  *                  accumulation; residual stream, norms, QK-norm/RoPE, attention
  *                  (float32 SIMT kernel), SwiGLU and logits in float32.
  *   DTP_PREC_BF16: bf16 GEMM/attention operands, float32 accumulation, float32
- *                  residual stream, norms, softmax and logits (tcgen05 tensor cores). */
-enum { DTP_PREC_F32 = 0, DTP_PREC_TF32 = 1, DTP_PREC_BF16 = 2 };
+ *                  residual stream, norms, softmax and logits (tcgen05 tensor cores).
+ *   DTP_PREC_E4M3: quantised weights and GEMM inputs: every GEMM operand is OCP
+ *                  FP8 E4M3 with one float32 scale per row (weights per output
+ *                  channel, activations per token; scale = max|row| / 448, codes
+ *                  nearest-even), tcgen05 kind::f8f6f4 with float32 accumulation
+ *                  and the two scales applied in the epilogue; embedding, attention
+ *                  (q/k/v, P) and the SwiGLU / attention outputs before their
+ *                  quantisation are bf16, as in DTP_PREC_BF16. */
+enum { DTP_PREC_F32 = 0, DTP_PREC_TF32 = 1, DTP_PREC_BF16 = 2, DTP_PREC_E4M3 = 3 };
 
 typedef struct dtp_config {
     int n_layer;          /* decoder layers                                         */
@@ -81,7 +88,7 @@ typedef struct dtp_config {
     int n_vocab;          /* vocabulary V                                           */
     float rope_freq_base; /* RoPE base; theta_i = base^(-2i/r)                      */
     float rms_eps;        /* epsilon inside every RMSNorm's square root             */
-    int precision;        /* DTP_PREC_F32, DTP_PREC_TF32 or DTP_PREC_BF16           */
+    int precision;        /* DTP_PREC_F32, _TF32, _BF16 or _E4M3                    */
     int attn_gate;        /* 1: gated attention -- the Q projection also yields, per head,
                              head_dim gate values after its head_dim q values, and the
                              attention output is multiplied by sigmoid(gate) before the
@@ -114,8 +121,9 @@ typedef struct dtp_layer_src {
  * Wo, Wdown, and the four norm vectors; then tok_embd [V, d], output_norm [d]
  * and the lm_head [V, d].  Matrices are stored as bf16 (round to nearest even)
  * under DTP_PREC_BF16, float32 under DTP_PREC_F32, and float32 rounded to tf32
- * (nearest even) under DTP_PREC_TF32, except tok_embd, which stays float32;
- * norm vectors are float32.
+ * (nearest even) under DTP_PREC_TF32, except tok_embd, which stays float32.
+ * Under DTP_PREC_E4M3 the matrices are e4m3 codes, each followed by its float32
+ * row scales, and tok_embd is bf16.  Norm vectors are float32.
  * ------------------------------------------------------------------------------------ */
 
 /* Bytes of the packed buffer for `cfg` (0 if cfg is invalid). */
@@ -162,7 +170,7 @@ typedef struct dtp_fwd_outputs {
     float* hidden;   /* device float32 [n_layer + 1, T, n_embd], as in dtp_fwd_prefill      */
     void* k_cache;   /* device [n_layer, T, n_head_kv*head_dim]: every layer's keys after
                         QK-norm and RoPE (what attention consumed), token-major; bf16 under
-                        DTP_PREC_BF16, float32 otherwise -- a decode KV cache              */
+                        DTP_PREC_BF16 / _E4M3, float32 otherwise -- a decode KV cache      */
     void* v_cache;   /* device [n_layer, T, n_head_kv*head_dim]: every layer's values, same
                         dtype and layout as k_cache                                         */
 } dtp_fwd_outputs;
@@ -203,7 +211,8 @@ int dtp_fwd_prefill_varlen(const dtp_config* cfg, const void* packed, size_t pac
  * KV state (device, caller-owned, 256-byte aligned, dtp_kv_state_size bytes
  * for up to max_T positions; nk = n_head_kv*head_dim): per layer l, at byte
  * offset l * S with S the per-layer stride below,
- *   DTP_PREC_BF16: K  bf16 [max_T, nk] token-major, then (256-byte aligned)
+ *   DTP_PREC_BF16 / DTP_PREC_E4M3:
+ *                  K  bf16 [max_T, nk] token-major, then (256-byte aligned)
  *                  V^T bf16 [nk, ldvt], ldvt = max_T rounded up to 8
  *   DTP_PREC_F32 / DTP_PREC_TF32:
  *                  K  f32 [max_T, nk], then (256-byte aligned) V f32 [max_T, nk]
@@ -328,6 +337,33 @@ int dtp_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
  * residual may alias y (in-place residual add). */
 int dtp_linear(const void* x, const void* W, void* y, int dtype, int y_dtype, int M, int N, int K,
                const float* residual, dtp_stream_t stream);
+
+/* Per-row e4m3 quantisation of a GEMM operand (the DTP_PREC_E4M3 arithmetic; the
+ * pages' T-parallel path quantises each activation row to 8 bits before its
+ * matmul, `quantize_q8_1`): for each row r of x, scale[r] = max|x[r]| / 448 and
+ * q[r, c] = e4m3(x[r, c] * (448 / max|x[r]|)), nearest-even, saturating; a zero
+ * row gives scale 0 and zero codes.
+ *   x      device [rows, cols] of dtype DTP_F32 or DTP_BF16 (cols % 8 == 0 for bf16)
+ *   q      device uint8 [rows, cols] (e4m3 codes, row-major)
+ *   scale  device float32 [rows] */
+int dtp_quantize_rows_e4m3(const void* x, int dtype, int rows, int cols, uint8_t* q, float* scale,
+                           dtp_stream_t stream);
+
+/* rms_norm written as per-row e4m3 codes: y = rms_norm(x) * w as in dtp_rms_norm
+ * (float32), then quantised as in dtp_quantize_rows_e4m3 (q [rows, cols], scale
+ * [rows]); cols % 4 == 0 and cols <= 16384, x and w 16-byte aligned. */
+int dtp_rms_norm_e4m3(const float* x, const float* w, uint8_t* q, float* scale, int rows, int cols,
+                      float eps, dtp_stream_t stream);
+
+/* Linear on e4m3 operands: y[M, N] = x_scale[m] * w_scale[n] * (xq wq^T)[m, n]
+ * (+ residual), tcgen05 kind::f8f6f4 with float32 accumulation.
+ *   xq [M, K], wq [N, K]  device e4m3 codes (dtp_quantize_rows_e4m3), K % 16 == 0,
+ *                         16-byte aligned
+ *   x_scale [M], w_scale [N]  device float32 row scales
+ *   y      device float32 [M, N]; residual as for dtp_linear (may alias y) */
+int dtp_linear_e4m3(const uint8_t* xq, const float* x_scale, const uint8_t* wq,
+                    const float* w_scale, float* y, int M, int N, int K, const float* residual,
+                    dtp_stream_t stream);
 
 /* Fused QKV projection with per-head QK-RMSNorm and NeoX RoPE: the bf16 path's
  * first GEMM of a layer (forward.rs: the wq/wk/wv `e.matmul`s, the q/k

@@ -32,6 +32,8 @@ from .model import (  # noqa: F401
     rope_neox,
     round_bf16,
     round_tf32,
+    round_e4m3,
+    fake_quant_rows_e4m3,
     sdpa_causal_gqa,
     silu,
     swiglu,

@@ -31,6 +31,12 @@ sites, not their bodies):
   * tf32-operand mode: the same GEMM operands rounded to TensorFloat-32 (10-bit
     fraction, nearest, ties to even) instead; q/k/v and the gate stay unrounded
     (that mode's attention reads float32).
+  * fp8-operand mode (the quantised-weight variant; the pages' T-parallel path
+    quantises weights and activations to 8 bits in blocks): every GEMM operand
+    is quantised per row to OCP E4M3 with a float32 scale max|row| / 448 --
+    weights per output channel, activations per token -- and used dequantised;
+    the attention output and SwiGLU act are rounded to bf16 before that (they
+    are stored as bf16); the embedding, q/k/v and gate are bf16 as in bf16 mode.
 """
 from __future__ import annotations
 
@@ -62,18 +68,53 @@ def round_tf32(x) -> np.ndarray:
     return np.ldexp(np.rint(m * 2048.0), e - 11)
 
 
-def _rounders(bf16_operands: bool, tf32_operands: bool):
-    """(GEMM-operand rounding, attention-operand rounding) of a mode.  bf16 mode
-    rounds both (the tensor-core attention reads bf16 q/k/v); tf32 mode rounds
-    the GEMM operands only (its attention runs on float32 q/k/v)."""
+E4M3_MAX = 448.0
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Round to the nearest OCP FP8 E4M3 value, ties to even, saturating at
+    +-448: 4 significant bits for |x| >= 2^-6 (x = m * 2^e, m in [0.5, 1):
+    keep round-half-even(m * 2^4) / 2^4), and the fixed subnormal step 2^-9
+    below 2^-6."""
+    x = np.asarray(x, dtype=F64)
+    _, e = np.frexp(x)
+    quantum = np.ldexp(1.0, np.maximum(e - 4, -9))
+    return np.clip(np.rint(x / quantum) * quantum, -E4M3_MAX, E4M3_MAX)
+
+
+def fake_quant_rows_e4m3(a) -> np.ndarray:
+    """Per-row e4m3 quantisation, returned dequantised: each row r gets the
+    scale s_r = max|a[r]| / 448 (0 for a zero row) and a[r] -> s_r * e4m3(a[r] / s_r).
+    A GEMM of two such operands is s_a s_w (q_a q_w^T): the row scales of the
+    activation (per token) and of the weight (per output channel) factor out of
+    every dot product."""
+    a = np.asarray(a, dtype=F64)
+    amax = np.max(np.abs(a), axis=-1, keepdims=True)
+    s = amax / E4M3_MAX
+    safe = np.where(s > 0, s, 1.0)
+    return np.where(s > 0, round_e4m3(a / safe) * s, 0.0)
+
+
+def _rounders(bf16_operands: bool, tf32_operands: bool, fp8_operands: bool = False):
+    """Roundings of a mode: (GEMM input written from float32 -- the normed h, z and
+    final hn; GEMM input stored as bf16 first -- attention output and SwiGLU act;
+    weight matrices; attention operands q/k/v and the gate).
+      bf16: bf16 everywhere (the tensor-core attention reads bf16 q/k/v).
+      tf32: tf32 for the GEMM operands; attention operands unrounded (that mode's
+            attention runs on float32).
+      fp8:  per-row e4m3 for the GEMM operands (the attention output and act are
+            bf16 before they are quantised); bf16 attention operands."""
     ident = lambda a: a
-    if bf16_operands and tf32_operands:
-        raise ValueError("bf16_operands and tf32_operands are exclusive")
+    if bf16_operands + tf32_operands + fp8_operands > 1:
+        raise ValueError("the operand modes are exclusive")
     if bf16_operands:
-        return round_bf16, round_bf16
+        return round_bf16, round_bf16, round_bf16, round_bf16
     if tf32_operands:
-        return round_tf32, ident
-    return ident, ident
+        return round_tf32, round_tf32, round_tf32, ident
+    if fp8_operands:
+        fq = fake_quant_rows_e4m3
+        return fq, (lambda a: fq(round_bf16(a))), fq, round_bf16
+    return ident, ident, ident, ident
 
 
 # --------------------------------------------------------------------------------------
@@ -194,7 +235,8 @@ def _mats(w: dict, rnd) -> dict:
 
 
 def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=None,
-                  kv_prefix=None, tf32_operands: bool = False) -> np.ndarray:
+                  kv_prefix=None, tf32_operands: bool = False,
+                  fp8_operands: bool = False) -> np.ndarray:
     """One decoder layer, forward.rs `Model::forward` loop body, on the residual
     stream x [T, n_embd]; returns the new x.  If `kv_out` is a list, the layer's
     attention inputs (k after QK-norm and RoPE, and v) are appended to it.
@@ -202,8 +244,8 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     `kv_prefix` = (k, v) of the p0 positions before x (which then sits at
     positions pos = p0 .. p0+T-1): attention runs over those keys followed by
     x's own, the only way earlier positions reach later ones."""
-    op, opa = _rounders(bf16_operands, tf32_operands)
-    L = _mats(lw, op)
+    op, opm, opw, opa = _rounders(bf16_operands, tf32_operands, fp8_operands)
+    L = _mats(lw, opw)
     d, h, g, hd = cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim
     eps = cfg.rms_eps
     scale = 1.0 / np.sqrt(F64(hd))
@@ -231,16 +273,17 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     attn = sdpa_causal_gqa(q, k, v, h, g, hd, scale, p0=p0)
     if gate is not None:
         attn = attn / (1.0 + np.exp(-gate))          # attn * sigmoid(gate)
-    attn = op(attn)
+    attn = opm(attn)
     x1 = x + linear(attn, L["wo"])
     # ffn block (dense SwiGLU)
     z = op(rms_norm(x1, L["ffn_norm"], eps))
-    act = op(swiglu(linear(z, L["w_gate"]), linear(z, L["w_up"])))
+    act = opm(swiglu(linear(z, L["w_gate"]), linear(z, L["w_up"])))
     return x1 + linear(act, L["w_down"])
 
 
 def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidden: bool = False,
-            layer_source=None, kv_out=None, tf32_operands: bool = False):
+            layer_source=None, kv_out=None, tf32_operands: bool = False,
+            fp8_operands: bool = False):
     """forward.rs `Model::forward`: logits [T, n_vocab] for `tokens`, positions 0..T-1.
 
     weights: {"tok_embd" [V,d], "layers": [dict per layer], "output_norm" [d],
@@ -251,29 +294,28 @@ def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidd
     stream entering output_norm."""
     tokens = np.asarray(tokens, dtype=np.int64)
     T = tokens.shape[0]
-    op, _ = _rounders(bf16_operands, tf32_operands)
+    op, _, opw, _ = _rounders(bf16_operands, tf32_operands, fp8_operands)
     emb = np.asarray(weights["tok_embd"], dtype=F64)
-    if bf16_operands:
-        emb = round_bf16(emb[tokens])
-        x = emb
-    else:
-        x = emb[tokens]
+    x = emb[tokens]
+    if bf16_operands or fp8_operands:       # the table is stored as bf16
+        x = round_bf16(x)
     pos = np.arange(T)
     hidden = [x.copy()] if return_hidden else None
     for l in range(cfg.n_layer):
         lw = layer_source(l) if layer_source is not None else weights["layers"][l]
-        x = forward_layer(cfg, lw, x, pos, bf16_operands, kv_out, tf32_operands=tf32_operands)
+        x = forward_layer(cfg, lw, x, pos, bf16_operands, kv_out, tf32_operands=tf32_operands,
+                          fp8_operands=fp8_operands)
         if return_hidden:
             hidden.append(x.copy())
     hn = op(rms_norm(x, np.asarray(weights["output_norm"], dtype=F64), cfg.rms_eps))
-    logits = linear(hn, op(np.asarray(weights["output"], dtype=F64)))
+    logits = linear(hn, opw(np.asarray(weights["output"], dtype=F64)))
     if return_hidden:
         return logits, np.stack(hidden)
     return logits
 
 
 def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: bool = False,
-                  tf32_operands: bool = False):
+                  tf32_operands: bool = False, fp8_operands: bool = False):
     """Chunked prefill: logits [C, n_vocab] for the next C tokens of a sequence
     whose first p0 positions went through earlier calls.  forward.rs
     `Model::forward` is causal, so those positions reach these only through
@@ -282,18 +324,18 @@ def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: boo
     with this chunk's.  The chunks' logits, concatenated, are forward(tokens)'s."""
     tokens = np.asarray(tokens, dtype=np.int64)
     C = tokens.shape[0]
-    op, _ = _rounders(bf16_operands, tf32_operands)
+    op, _, opw, _ = _rounders(bf16_operands, tf32_operands, fp8_operands)
     first = len(kv_state) == 0
     p0 = 0 if first else kv_state[0][0].shape[0]
     x = np.asarray(weights["tok_embd"], dtype=F64)[tokens]
-    if bf16_operands:
+    if bf16_operands or fp8_operands:
         x = round_bf16(x)
     pos = p0 + np.arange(C)
     for l in range(cfg.n_layer):
         new = []
         prefix = None if first else kv_state[l]
         x = forward_layer(cfg, weights["layers"][l], x, pos, bf16_operands, new, prefix,
-                          tf32_operands)
+                          tf32_operands, fp8_operands)
         k, v = new[0]
         if first:
             kv_state.append((k, v))
@@ -301,7 +343,7 @@ def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: boo
             kv_state[l] = (np.concatenate([kv_state[l][0], k]),
                            np.concatenate([kv_state[l][1], v]))
     hn = op(rms_norm(x, np.asarray(weights["output_norm"], dtype=F64), cfg.rms_eps))
-    return linear(hn, op(np.asarray(weights["output"], dtype=F64)))
+    return linear(hn, opw(np.asarray(weights["output"], dtype=F64)))
 
 
 # --------------------------------------------------------------------------------------

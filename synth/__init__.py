@@ -103,7 +103,8 @@ class ModelConfig:
     rope_freq_base: float = 1e6
     rms_eps: float = 1e-6
     precision: str = "bf16"          # "f32" (exact), "tf32" or "bf16" (tf32 / bf16 GEMM
-                                     # operands, f32 accumulate)
+                                     # operands, f32 accumulate), "e4m3" (per-row e4m3
+                                     # weights and GEMM inputs)
     attn_gate: bool = False          # sigmoid output gate fused into the Q projection
 
     def replace(self, **kw) -> "ModelConfig":

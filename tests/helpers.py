@@ -42,13 +42,15 @@ def load_model(dtp, cfg, seed=0):
     return m
 
 
-def oracle_forward(cfg, seed=0, T=None, bf16=None, tf32=None):
-    """The oracle in the operand mode of cfg.precision (bf16 / tf32 rounding of
-    the GEMM operands; "f32" exact), unless bf16 / tf32 say otherwise."""
+def oracle_forward(cfg, seed=0, T=None, bf16=None, tf32=None, fp8=None):
+    """The oracle in the operand mode of cfg.precision (bf16 / tf32 rounding or
+    per-row e4m3 quantisation of the GEMM operands; "f32" exact), unless bf16 /
+    tf32 / fp8 say otherwise."""
     bf16 = (cfg.precision == "bf16") if bf16 is None else bf16
     tf32 = (cfg.precision == "tf32") if tf32 is None else tf32
+    fp8 = (cfg.precision == "e4m3") if fp8 is None else fp8
     w = synth.model_weights(cfg, seed)
     toks = synth.tokens(cfg, seed, T)
     logits, hidden = oracle.forward(cfg, w, toks, bf16_operands=bf16, tf32_operands=tf32,
-                                    return_hidden=True)
+                                    fp8_operands=fp8, return_hidden=True)
     return toks, logits, hidden

@@ -120,3 +120,24 @@ def test_chunk_state_size_and_rejections(dtp):
     assert call(16, 0, 64, sb=dtp.kv_state_size(c, 64) - 1) == -4   # short state
     kv = dtp._binding.FwdOutputs(0x10000, 0, None, 0x10000, None)
     assert call(16, 0, 64, o=kv) == -1               # the state is the cache
+
+
+def test_e4m3_entry_points_reject_on_the_host(dtp):
+    L = dtp.lib()
+    fake = ctypes.c_void_p(0x10000)   # never dereferenced
+    assert L.dtp_linear_e4m3(fake, fake, fake, fake, fake, 4, 4, 24, None, None) == -2   # K % 16
+    assert L.dtp_linear_e4m3(None, fake, fake, fake, fake, 4, 4, 32, None, None) == -1
+    assert L.dtp_linear_e4m3(fake, fake, fake, fake, fake, 0, 4, 32, None, None) == -1
+    assert L.dtp_quantize_rows_e4m3(fake, 7, 4, 16, fake, fake, None) == -1             # dtype
+    assert L.dtp_quantize_rows_e4m3(fake, 1, 4, 12, fake, fake, None) == -2             # bf16 cols % 8
+    assert L.dtp_rms_norm_e4m3(fake, fake, fake, fake, 4, 6, 1e-6, None) == -2          # cols % 4
+    # e4m3 configs: the tensor-core tiling rules of the bf16 path
+    c = _cfg(dtp, precision="e4m3")
+    assert dtp.packed_size(c) > 0 and dtp.workspace_size(c, 256) > dtp.workspace_size(_cfg(dtp), 256)
+    assert dtp.packed_size(_cfg(dtp, precision="e4m3", head_dim=48)) == 0
+    # packed e4m3 weights: 1 byte per matrix element, a float32 scale per row
+    cfg = synth.CONFIGS["qwen3-8b-shape"]
+    n8 = dtp.packed_size(dtp.config_from(cfg.replace(precision="e4m3")))
+    n16 = dtp.packed_size(dtp.config_from(cfg))
+    emb = cfg.n_vocab * cfg.n_embd * 2
+    assert abs((n8 - emb) / (n16 - emb) - 0.5) < 0.01

@@ -1,0 +1,150 @@
+"""Quantised-weight mode (DTP_PREC_E4M3): every GEMM operand as per-row OCP
+E4M3 codes with float32 row scales, tcgen05 kind::f8f6f4.
+
+Per op, the quantisers are checked bit-exactly against a numpy statement of
+the same float32 arithmetic (scale = amax / 448, codes = e4m3(x * (448 / amax))
+via torch's float8_e4m3fn cast), and the e4m3 GEMM against float64 on the
+decoded codes (e4m3 products are exact in float32; float32 accumulation).
+
+Whole forward, against the oracle's fp8-operand mode.  The GPU and the oracle
+quantise values that differ at the float32 level (and, for T > 1, by the bf16
+rounding of P inside flash attention), so some e4m3 roundings differ by one code
+(2^-4 relative) and the difference cascades through the later roundings until
+the two quantisations are independent.  Bars:
+  * T = 1 (no P rounding: the seeds are float32-level only): per-layer relative
+    L2 <= 2^-4 / 4 (a small fraction of the one-code flips);
+  * any T: per-layer relative L2 <= 1.5 * sqrt(2) * D_l, where D_l is the
+    oracle's own fp8-vs-exact distance at layer l -- no worse than two
+    independent quantisations of the same exact pass (1.5x margin); the
+    logits likewise."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import oracle_forward, rel_l2
+from test_forward_gpu import run_gpu
+
+pytestmark = pytest.mark.gpu
+dev = torch.device("cuda")
+
+
+def t32(a):
+    return torch.as_tensor(np.ascontiguousarray(a, np.float32), device=dev)
+
+
+def quant_ref(x32):
+    """numpy/torch statement of the per-row quantiser on float32 rows."""
+    x32 = np.ascontiguousarray(x32, np.float32)
+    amax = np.abs(x32).max(axis=1).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(amax > 0, np.float32(448.0) / amax, np.float32(0.0)).astype(np.float32)
+    s = (amax / np.float32(448.0)).astype(np.float32)
+    y = (x32 * inv[:, None]).astype(np.float32)
+    q = torch.as_tensor(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return q, s
+
+
+def decode(q):
+    return torch.as_tensor(np.ascontiguousarray(q)).view(torch.float8_e4m3fn).float().numpy()
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 8), (37, 512), (300, 4096), (5, 12288)])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_quantize_rows_e4m3_bitexact(dtp, rows, cols, dt):
+    x = synth.normal(13, 1300, (rows, cols)) * np.exp(synth.normal(13, 1301, (rows, 1)) * 3)
+    if rows > 3:
+        x[2] = 0.0
+    xt = t32(x).to(dt)
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    s = torch.empty(rows, dtype=torch.float32, device=dev)
+    dtp.quantize_rows_e4m3(xt, q, s)
+    torch.cuda.synchronize()
+    dtp.check()
+    want_q, want_s = quant_ref(xt.float().cpu().numpy())
+    np.testing.assert_array_equal(q.cpu().numpy(), want_q)
+    np.testing.assert_array_equal(s.cpu().numpy(), want_s)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 64), (100, 512), (33, 4096)])
+def test_rms_norm_e4m3_is_the_quantised_rms_norm(dtp, rows, cols):
+    """Bit-exact: the fused kernel's codes are the quantiser applied to the
+    float32 RMSNorm kernel's output (same row reduction)."""
+    x = synth.normal(14, 1400, (rows, cols)) * 2
+    w = synth.normal(14, 1401, (cols,), mean=1.0, std=0.1)
+    y = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    s = torch.empty(rows, dtype=torch.float32, device=dev)
+    dtp.rms_norm(t32(x), t32(w), y, 1e-6)
+    dtp.rms_norm_e4m3(t32(x), t32(w), q, s, 1e-6)
+    torch.cuda.synchronize()
+    want_q, want_s = quant_ref(y.cpu().numpy())
+    np.testing.assert_array_equal(q.cpu().numpy(), want_q)
+    np.testing.assert_array_equal(s.cpu().numpy(), want_s)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 16), (128, 256, 128), (130, 200, 144), (300, 1000, 272),
+                                   (513, 2048, 1024), (64, 384, 4096), (77, 1001, 144)])
+@pytest.mark.parametrize("resid", [False, True])
+def test_linear_e4m3_tensor_core(dtp, M, N, K, resid):
+    x = synth.normal(15, 1500, (M, K))
+    W = synth.normal(15, 1501, (N, K), std=0.05)
+    xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    xs = torch.empty(M, dtype=torch.float32, device=dev)
+    ws = torch.empty(N, dtype=torch.float32, device=dev)
+    dtp.quantize_rows_e4m3(t32(x), xq, xs)
+    dtp.quantize_rows_e4m3(t32(W), wq, ws)
+    r = synth.normal(15, 1502, (M, N)) if resid else None
+    y = t32(r) if resid else torch.empty((M, N), dtype=torch.float32, device=dev)
+    dtp.linear_e4m3(xq, xs, wq, ws, y, residual=y if resid else None)
+    torch.cuda.synchronize()
+    dtp.check()
+    a = decode(xq.cpu().numpy()).astype(np.float64)
+    b = decode(wq.cpu().numpy()).astype(np.float64)
+    acc = a @ b.T
+    ref = acc * xs.cpu().numpy().astype(np.float64)[:, None] * ws.cpu().numpy().astype(np.float64)[None, :]
+    if resid:
+        ref = ref + r
+    # exact products, float32 accumulation (about one rounding per K=32 MMA step)
+    # plus the two scale multiplies: bound (2 * K/32 + 4) * 2^-23 * max|y|
+    tol = (2 * max(K / 32, 1) + 4) * 2.0 ** -23 * np.abs(ref).max()
+    np.testing.assert_allclose(y.cpu().numpy(), ref, rtol=0, atol=tol)
+    # and the codes decode to the oracle's per-row quantisation of the same rows,
+    # except where float32 (x * 448/amax) and float64 (x / (amax/448)) land on
+    # opposite sides of a rounding boundary
+    fq = oracle.fake_quant_rows_e4m3(x.astype(np.float32))
+    same = np.isclose(a * xs.cpu().numpy()[:, None], fq, rtol=2e-7, atol=0)
+    assert same.mean() >= 0.999, same.mean()
+
+
+def _metrics(cfg, gl, gh, rl, rh, xl, xh):
+    L = cfg.n_layer
+    m = {"layer_rel_l2": [round(rel_l2(gh[l], rh[l]), 5) for l in range(L + 1)],
+         "fp8_vs_exact": [round(rel_l2(rh[l], xh[l]), 5) for l in range(L + 1)],
+         "logit_rel_l2": rel_l2(gl, rl), "oracle_logit_rel_l2": rel_l2(rl, xl),
+         "argmax_vs_fp8_oracle": float(np.mean(np.argmax(gl, 1) == np.argmax(rl, 1))),
+         "argmax_fp8_oracle_vs_exact": float(np.mean(np.argmax(rl, 1) == np.argmax(xl, 1))),
+         "gpu_vs_exact_max_layer": max(rel_l2(gh[l], xh[l]) for l in range(1, L + 1))}
+    print(f"\ne4m3 {cfg.name} T={cfg.T}: {m}")
+    return m
+
+
+@pytest.mark.parametrize("name,T,kw", [("small", 256, {}), ("small", 1, {}),
+                                       ("small", 129, dict(attn_gate=True, n_layer=2)),
+                                       ("qwen3-0.6b-shape", 512, {})])
+def test_forward_e4m3(dtp, name, T, kw):
+    cfg = synth.CONFIGS[name].replace(precision="e4m3", T=T, **kw)
+    _, gl, gh = run_gpu(dtp, cfg, T=T)
+    _, rl, rh = oracle_forward(cfg, T=T)
+    _, xl, xh = oracle_forward(cfg, T=T, fp8=False)
+    m = _metrics(cfg, gl, gh, rl, rh, xl, xh)
+    assert np.isfinite(gl).all()
+    # the embedding rows are the same bf16 values on both sides
+    assert m["layer_rel_l2"][0] == 0.0
+    for l in range(1, cfg.n_layer + 1):
+        if T == 1:
+            assert m["layer_rel_l2"][l] <= 2.0 ** -4 / 4, (l, m)
+        assert m["layer_rel_l2"][l] <= 1.5 * np.sqrt(2) * m["fp8_vs_exact"][l], (l, m)
+    assert m["logit_rel_l2"] <= 1.5 * np.sqrt(2) * m["oracle_logit_rel_l2"], m

@@ -329,7 +329,7 @@ def _run_chunks(dtp, m, cfg, toks, plan, max_T, state=None, last_only=False):
 CHUNK_PLANS = [(256, 256, 88), (100, 300, 200), (1, 598, 1), (600,)]
 
 
-@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16", "e4m3"])
 @pytest.mark.parametrize("plan", CHUNK_PLANS)
 def test_chunked_prefill(dtp, prec, plan):
     """dtp_fwd_prefill_chunk: positions p0..p0+C-1 against the KV state of the
@@ -345,7 +345,7 @@ def test_chunked_prefill(dtp, prec, plan):
     _, full_l, full_h = run_gpu(dtp, cfg, T=T, model=m)
     np.testing.assert_array_equal(gl, full_l)
     np.testing.assert_array_equal(gh, full_h)
-    if plan == CHUNK_PLANS[0]:
+    if plan == CHUNK_PLANS[0] and prec != "e4m3":     # e4m3 parity: test_e4m3_gpu.py
         _, rl, rh = oracle_forward(cfg, T=T)
         assert_parity(cfg, gl, gh, rl, rh)
 

@@ -523,3 +523,60 @@ def test_forward_tf32_mode_between_exact_and_bf16(tiny_weights):
     rb = np.linalg.norm(a - b) / np.linalg.norm(a)
     # 3 more significant bits: the error shrinks about 8x
     assert 1e-6 < rt < rb / 3
+
+
+# ---------------------------------------------------------------- e4m3 quantisation
+def test_round_e4m3_hand_fixture():
+    """OCP E4M3: 4 significant bits, subnormal step 2^-9 below 2^-6, max 448,
+    nearest with ties to even (hand-worked values)."""
+    cases = [(1.0, 1.0), (1.0625, 1.0),                  # tie between 1 and 1.125 -> even (1)
+             (1.1875, 1.25),                            # tie between 1.125 and 1.25 -> even
+             (1.09, 1.125), (-3.3, -3.25), (448.0, 448.0), (464.0, 448.0),   # tie -> even (448)
+             (470.0, 448.0), (1e6, 448.0), (-1e6, -448.0),                    # saturation
+             (2.0 ** -6, 2.0 ** -6), (2.0 ** -9, 2.0 ** -9), (2.0 ** -10, 0.0),  # tie -> 0
+             (3 * 2.0 ** -11, 2.0 ** -9), (5 * 2.0 ** -10, 2.0 ** -8),       # tie 2.5 ulp -> 2
+             (0.0137, 7 * 2.0 ** -9), (0.0, 0.0)]
+    for x, want in cases:
+        assert oracle.round_e4m3(x) == want, (x, oracle.round_e4m3(x), want)
+
+
+def test_round_e4m3_matches_torch_float8_in_range():
+    """torch's float8_e4m3fn cast (nearest-even) agrees on every value below the
+    saturation point, including the subnormal range and exact ties."""
+    x = synth.normal(10, 1000, (30000,)) * np.exp2(np.round(synth.normal(10, 1001, (30000,)) * 5))
+    x = x[np.abs(x) < 464].astype(np.float32)
+    ties = (np.arange(1, 64, dtype=np.float32) + 0.5) * np.float32(2.0 ** -9)
+    x = np.concatenate([x, ties, -ties])
+    want = torch.as_tensor(x).to(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    np.testing.assert_array_equal(oracle.round_e4m3(x), want)
+
+
+def test_fake_quant_rows_e4m3_properties():
+    a = synth.normal(10, 1002, (64, 300)) * np.exp(synth.normal(10, 1003, (64, 1)) * 3)
+    a[5] = 0.0
+    q = oracle.fake_quant_rows_e4m3(a)
+    amax = np.abs(a).max(axis=1)
+    # each row's largest element maps to +-448, so it comes back (up to the
+    # float64 rounding of s = amax / 448)
+    np.testing.assert_allclose(np.abs(q).max(axis=1), amax, rtol=1e-15, atol=0)
+    assert not q[5].any()
+    # relative error at most half an e4m3 ulp (2^-4) in the normal range; the
+    # subnormal range (|a| < 2^-6 * s) has absolute error <= 2^-10 * s
+    s = (amax / 448.0)[:, None]
+    err = np.abs(q - a)
+    assert np.all(err <= np.maximum(2.0 ** -4 * np.abs(a), 2.0 ** -10 * s) * (1 + 1e-12))
+    # scaling a row by a power of two scales its quantisation exactly
+    np.testing.assert_array_equal(oracle.fake_quant_rows_e4m3(a * 2.0 ** 7), q * 2.0 ** 7)
+    # per-row: rows are independent
+    np.testing.assert_array_equal(oracle.fake_quant_rows_e4m3(a[:7])[3], q[3])
+
+
+def test_forward_fp8_mode_is_coarser_than_bf16(tiny_weights):
+    toks = synth.tokens(TINY)
+    a = oracle.forward(TINY, tiny_weights, toks)
+    b = oracle.forward(TINY, tiny_weights, toks, bf16_operands=True)
+    f = oracle.forward(TINY, tiny_weights, toks, fp8_operands=True)
+    rb = np.linalg.norm(a - b) / np.linalg.norm(a)
+    rf = np.linalg.norm(a - f) / np.linalg.norm(a)
+    # 4 significant bits instead of 8, partly offset by the per-row scales
+    assert rb < rf < 0.2
