@@ -337,26 +337,33 @@ def main():
     # ------------------------------------------------------------------ end to end (host buffers)
     e2e = None
     if not args.no_e2e:
-        tok_h = torch.as_tensor(toks_np).pin_memory()
-        log_h = torch.empty((cfg.T, cfg.n_vocab), dtype=torch.float32).pin_memory()
-        ws_h = m.workspace(cfg.T, host=True)
-        for _ in range(2):
-            dtp.fwd_prefill_host(m.c, m.packed, tok_h, log_h, ws_h)
+        # one prompt per step, host to host: tokens in, the forward pass, all
+        # logits out; the batch call overlaps prompt j's logits copy with prompt
+        # j+1's forward pass (two pinned host logit buffers, used alternately)
+        tok_h = [torch.as_tensor(synth.tokens(cfg, seed=2000 + 97 * rank + j).astype(np.int32))
+                 .pin_memory() for j in range(args.steps)]
+        log_h = [torch.empty((cfg.T, cfg.n_vocab), dtype=torch.float32).pin_memory()
+                 for _ in range(2)]
+        ws_h = torch.empty(dtp.workspace_size_host_batch(m.c, cfg.T), dtype=torch.uint8,
+                           device=dev)
+        outs = [log_h[j % 2] for j in range(args.steps)]
+        dtp.fwd_prefill_host_batch(m.c, m.packed, tok_h[:2], log_h, ws_h)
         torch.cuda.synchronize(dev)
         barrier()
         e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e_start.record(stream)
-        for _ in range(args.steps):
-            dtp.fwd_prefill_host(m.c, m.packed, tok_h, log_h, ws_h)
+        dtp.fwd_prefill_host_batch(m.c, m.packed, tok_h, outs, ws_h)
         e_end.record(stream)
         torch.cuda.synchronize(dev)
         dtp.check()
         ems = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
         e2e = {"value": replica_throughput(world, cfg.T, args.steps, ems), "unit": UNIT,
-               "h2d_bytes_per_step": int(tok_h.numel() * 4),
-               "d2h_bytes_per_step": int(log_h.numel() * 4),
-               "path": "dtp_fwd_prefill_host (pinned host tokens in, pinned host logits out)"}
-        del log_h
+               "h2d_bytes_per_step": int(tok_h[0].numel() * 4),
+               "d2h_bytes_per_step": int(log_h[0].numel() * 4),
+               "path": "dtp_fwd_prefill_host_batch: one prompt per step, pinned host tokens in, "
+                       "all pinned host logits out; each prompt's logits copy overlaps the next "
+                       "prompt's forward pass"}
+        del log_h, outs, ws_h
 
     if rank != 0:
         if world > 1:

@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     fwd_prefill_chunk,
     fwd_prefill_ex,
     fwd_prefill_host,
+    fwd_prefill_host_batch,
     fwd_prefill_varlen,
     gate_up_swiglu,
     kv_state_size,
@@ -48,5 +49,6 @@ from ._binding import (  # noqa: F401
     timer_read,
     workspace_size,
     workspace_size_host,
+    workspace_size_host_batch,
     workspace_size_varlen,
 )

@@ -68,6 +68,9 @@ _SIGS = {
                           c_int),
     "dtp_linear_e4m3": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                          c_void_p, c_void_p], c_int),
+    "dtp_workspace_size_host_batch": ([ctypes.POINTER(Config), c_int], c_size_t),
+    "dtp_fwd_prefill_host_batch": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int,
+                                    c_int, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "dtp_kv_state_size": ([ctypes.POINTER(Config), c_int], c_size_t),
     "dtp_fwd_prefill_chunk": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int, c_int,
                                c_void_p, c_size_t, c_int, ctypes.POINTER(FwdOutputs), c_void_p,
@@ -247,6 +250,30 @@ def fwd_prefill_host(c: Config, packed: torch.Tensor, tokens_host: torch.Tensor,
                                    tokens_host.numel(), logits_host.data_ptr(),
                                    workspace.data_ptr(),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def workspace_size_host_batch(c: Config, T: int) -> int:
+    return lib().dtp_workspace_size_host_batch(ctypes.byref(c), T)
+
+
+def fwd_prefill_host_batch(c: Config, packed: torch.Tensor, tokens_host: list, logits_host: list,
+                           workspace: torch.Tensor, stream=None) -> None:
+    """n prompts host to host; the logits copy of prompt j overlaps the forward
+    pass of prompt j + 1.  tokens_host: n CPU uint32/int32 tensors [T];
+    logits_host: n CPU float32 tensors [T, n_vocab] (pinned for asynchronous copies)."""
+    n = len(tokens_host)
+    assert n == len(logits_host) and n > 0
+    T = tokens_host[0].numel()
+    for t, lg in zip(tokens_host, logits_host):
+        assert t.device.type == "cpu" and t.numel() == T and t.is_contiguous()
+        assert lg.device.type == "cpu" and lg.dtype == torch.float32 and lg.is_contiguous()
+    toks = (c_void_p * n)(*[t.data_ptr() for t in tokens_host])
+    logs = (c_void_p * n)(*[lg.data_ptr() for lg in logits_host])
+    _ok(lib().dtp_fwd_prefill_host_batch(ctypes.byref(c), packed.data_ptr(),
+                                         packed.numel() * packed.element_size(), toks, n, T, logs,
+                                         workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
 
 
 def check(stream=None) -> None:

@@ -202,14 +202,16 @@ struct Workspace {
     size_t q, k, vt, rope, gate;                 // bf16 path
     long long ldvt;
     size_t q8, s8;                               // e4m3 GEMM operand + row scales
-    size_t tokens, logits;                       // _host staging
+    size_t tokens, logits, logits2;              // _host staging (logits2: batch ping-pong)
     size_t tile_start, vcol_start, last_row, tok_pos, tok_vcol;   // packed sequences
     size_t total;
 };
 
 // Workspace for T tokens; n_seq > 0 adds the packed-sequence schedule and pads
-// each sequence's v^T block to a multiple of 8 columns.
-static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_seq = 0) {
+// each sequence's v^T block to a multiple of 8 columns; host adds the token and
+// logit staging (a second logit buffer with batch).
+static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_seq = 0,
+                                  bool batch = false) {
     Workspace W = {};
     const size_t d = c->n_embd, hd = c->head_dim, nq = (size_t)c->n_head * hd,
                  nk = (size_t)c->n_head_kv * hd, F = c->n_ff;
@@ -244,6 +246,7 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_s
     if (host) {
         W.tokens = take((size_t)T * 4);
         W.logits = take((size_t)T * c->n_vocab * 4);
+        if (batch) W.logits2 = take((size_t)T * c->n_vocab * 4);
     }
     if (n_seq > 0) {
         W.tile_start = take(((size_t)n_seq + 2) * 4);
@@ -790,6 +793,97 @@ int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packe
     DTP_CUDA_CHECK(cudaMemcpyAsync(logits_host, logit_d, (size_t)T * cfg->n_vocab * 4,
                                    cudaMemcpyDeviceToHost, s));
     return DTP_OK;
+}
+
+size_t dtp_workspace_size_host_batch(const dtp_config* cfg, int T) {
+    if (validate_config(cfg) != DTP_OK || T <= 0) return 0;
+    return workspace_layout(cfg, T, true, 0, true).total;
+}
+
+// The library's device-to-host copy stream of the current device (created once).
+static cudaStream_t copy_stream() {
+    static std::mutex mu;
+    static cudaStream_t streams[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+        streams[dev] = nullptr;
+    return streams[dev];
+}
+
+int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                               const uint32_t* const* tokens_host, int n, int T,
+                               float* const* logits_host, void* workspace, size_t ws_bytes,
+                               dtp_stream_t stream) {
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (n <= 0 || T <= 0) return fail(DTP_ERR_INVALID_ARG, "n and T must be >= 1");
+    if (!tokens_host || !logits_host || !workspace)
+        return fail(DTP_ERR_INVALID_ARG, "NULL tokens_host, logits_host or workspace");
+    for (int j = 0; j < n; ++j) {
+        if (!tokens_host[j] || !logits_host[j])
+            return fail(DTP_ERR_INVALID_ARG, "NULL host buffer for prompt %d", j);
+        for (int t = 0; t < T; ++t)
+            if (tokens_host[j][t] >= (uint32_t)cfg->n_vocab)
+                return fail(DTP_ERR_TOKEN_RANGE, "prompt %d: token %u at position %d >= n_vocab %d",
+                            j, tokens_host[j][t], t, cfg->n_vocab);
+    }
+    Workspace W = workspace_layout(cfg, T, true, 0, true);
+    if (ws_bytes < W.total)
+        return fail(DTP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, W.total);
+    if (!aligned(workspace, 256)) return fail(DTP_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaStream_t k = copy_stream();
+    if (!k) return fail(DTP_ERR_CUDA, "could not create the copy stream");
+    uint8_t* ws = (uint8_t*)workspace;
+    uint32_t* tok_d = (uint32_t*)(ws + W.tokens);
+    float* buf[2] = {(float*)(ws + W.logits), (float*)(ws + W.logits2)};
+    const size_t lbytes = (size_t)T * cfg->n_vocab * 4;
+    // ready[j]: prompt j's logits are on the device; copied[b]: buffer b is free again
+    std::vector<cudaEvent_t> ev;
+    auto new_event = [&](cudaEvent_t* e) {
+        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+        ev.push_back(*e);
+        return true;
+    };
+    cudaEvent_t copied[2] = {nullptr, nullptr};
+    rc = DTP_OK;
+    for (int j = 0; j < n && rc == DTP_OK; ++j) {
+        const int b = j & 1;
+        cudaError_t e = cudaSuccess;
+        if (copied[b]) e = cudaStreamWaitEvent(s, copied[b], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(tok_d, tokens_host[j], (size_t)T * 4, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) {
+            rc = fail(DTP_ERR_CUDA, "%s", cudaGetErrorString(e));
+            break;
+        }
+        dtp_fwd_outputs o = {};
+        o.logits = buf[b];
+        rc = fwd_checked(cfg, packed, packed_bytes, tok_d, T, o, workspace, ws_bytes, true, stream);
+        if (rc) break;
+        cudaEvent_t ready, done;
+        if (!new_event(&ready) || !new_event(&done)) {
+            rc = fail(DTP_ERR_CUDA, "cudaEventCreate failed");
+            break;
+        }
+        // the copy of prompt j overlaps the forward of prompt j + 1
+        if ((e = cudaEventRecord(ready, s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(k, ready, 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(logits_host[j], buf[b], lbytes, cudaMemcpyDeviceToHost, k)) !=
+                cudaSuccess ||
+            (e = cudaEventRecord(done, k)) != cudaSuccess) {
+            rc = fail(DTP_ERR_CUDA, "%s", cudaGetErrorString(e));
+            break;
+        }
+        copied[b] = done;
+    }
+    // `stream` completes only after every copy has landed
+    for (int b = 0; b < 2; ++b)
+        if (copied[b]) cudaStreamWaitEvent(s, copied[b], 0);
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);      // released once they complete
+    return rc;
 }
 
 int dtp_check(dtp_stream_t stream) {

@@ -246,6 +246,24 @@ int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packe
                          const uint32_t* tokens_host, int T, float* logits_host, void* workspace,
                          size_t ws_bytes, dtp_stream_t stream);
 
+/* n prompts of T tokens each, host to host, in order: prompt j's tokens are
+ * copied in, its forward pass runs on `stream`, and its logits are copied out to
+ * logits_host[j] on a device-to-host stream of the library's own, so that the
+ * copy of prompt j overlaps the forward pass of prompt j + 1 (two device logit
+ * buffers alternate).  Everything is enqueued before the call returns; `stream`
+ * completes only after the last copy has landed, so synchronising `stream`
+ * makes every logits_host[j] readable.
+ *   tokens_host  n host pointers to uint32 [T] (range-checked on the host first)
+ *   logits_host  n host pointers to float32 [T, n_vocab] (page-locked memory makes
+ *                the copies asynchronous)
+ *   workspace    >= dtp_workspace_size_host_batch(cfg, T) bytes
+ * One call at a time per device: the library's copy stream is shared. */
+size_t dtp_workspace_size_host_batch(const dtp_config* cfg, int T);
+int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t packed_bytes,
+                               const uint32_t* const* tokens_host, int n, int T,
+                               float* const* logits_host, void* workspace, size_t ws_bytes,
+                               dtp_stream_t stream);
+
 /* Synchronise `stream`, then report and clear the device error words raised
  * by this library's kernels since the last call: DTP_OK,
  * DTP_ERR_TOKEN_RANGE, DTP_ERR_DEVICE_TIMEOUT, or DTP_ERR_CUDA (a sticky

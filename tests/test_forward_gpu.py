@@ -403,3 +403,24 @@ def test_chunked_prefill_head_dim_128_gated(dtp):
     np.testing.assert_array_equal(gl, full_l)
     _, rl, rh = oracle_forward(cfg, T=T)
     assert_parity(cfg, gl, gh, rl, rh)
+
+
+def test_host_batch_matches_single_calls(dtp):
+    """dtp_fwd_prefill_host_batch: n prompts host to host with the logits copies
+    overlapping the next forward pass give exactly the logits of n separate
+    dtp_fwd_prefill_host calls (odd n exercises both device buffers unevenly)."""
+    cfg = synth.CONFIGS["small"].replace(n_layer=2)
+    m = load_model(dtp, cfg)
+    T, n = 200, 5
+    toks = [torch.as_tensor(synth.uniform_int(7, 70 + j, T, cfg.n_vocab).astype(np.int32)).pin_memory()
+            for j in range(n)]
+    outs = [torch.full((T, cfg.n_vocab), float("nan")).pin_memory() for _ in range(n)]
+    ws = torch.empty(dtp.workspace_size_host_batch(m.c, T), dtype=torch.uint8, device=dev)
+    dtp.fwd_prefill_host_batch(m.c, m.packed, toks, outs, ws)
+    torch.cuda.current_stream().synchronize()
+    dtp.check()
+    for j in range(n):
+        one = torch.empty((T, cfg.n_vocab)).pin_memory()
+        dtp.fwd_prefill_host(m.c, m.packed, toks[j], one, m.workspace(T, host=True))
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(outs[j], one), j
