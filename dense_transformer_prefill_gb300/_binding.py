@@ -301,10 +301,12 @@ def sdpa_workspace_size(T: int, n_head_kv: int, head_dim: int, dtype: int) -> in
 
 
 def sdpa_causal_gqa(q, k, v, out, n_head: int, n_head_kv: int, head_dim: int, scale: float,
-                    workspace=None, stream=None) -> None:
+                    workspace=None, tf32: bool = False, stream=None) -> None:
+    """tf32=True: float32 q/k/v holding tf32 values on the tcgen05 kind::tf32 kernel."""
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    dt = DTP_TF32 if tf32 else _dtype_code(q)
     _ok(lib().dtp_sdpa_causal_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                  _dtype_code(q), q.shape[0], n_head, n_head_kv, head_dim, scale,
+                                  dt, q.shape[0], n_head, n_head_kv, head_dim, scale,
                                   _ptr(workspace), ws_bytes, _stream(stream)))
 
 

@@ -17,6 +17,9 @@
 //               unless it grows by more than 8 (then O is rescaled in TMEM),
 //               P = 2^(s - m) rounded to bf16 into 128-byte-swizzled shared
 //               memory, row sums in float32
+// The same kernel runs on float32 operands holding tf32 values (F32: kind::tf32,
+// 32-key tiles so that both heads' float32 Q tiles fit in shared memory, P
+// rounded to tf32, float32 output).
 // Causality: key tiles up to the one holding the tile's last query position;
 // tiles that reach past the first query position mask key > query.  Queries may
 // start at a position p0 > 0 (chunked prefill against earlier keys).
@@ -46,16 +49,21 @@ bool attn_tc_supported(int n_head, int n_head_kv, int head_dim) {
 namespace {
 
 constexpr int BQ = 128;          // query rows per tile
-constexpr int BKV = 128;         // keys per tile
 constexpr int kThreads = 320;    // 10 warps
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int HD>
+// F32: tf32 operands in float32 storage.  A 128-byte shared-memory row holds
+// AE elements (64 bf16 or 32 float32); one MMA consumes 32 bytes of K per row.
+template <int HD, bool F32>
 struct ACfg {
-    static constexpr int Q_BYTES = BQ * HD * 2;
-    static constexpr int K_BYTES = BKV * HD * 2;
-    static constexpr int V_BYTES = HD * BKV * 2;
-    static constexpr int P_BYTES = BQ * BKV * 2;
+    static constexpr int EB = F32 ? 4 : 2;
+    static constexpr int AE = 128 / EB;
+    static constexpr int KSTEP = 32 / EB;
+    static constexpr int BKV = F32 ? 32 : 128;       // keys per tile
+    static constexpr int Q_BYTES = BQ * HD * EB;
+    static constexpr int K_BYTES = BKV * HD * EB;
+    static constexpr int V_BYTES = HD * BKV * EB;
+    static constexpr int P_BYTES = BQ * BKV * EB;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_V = OFF_K + K_BYTES;
@@ -69,14 +77,15 @@ struct ACfg {
 struct AParams {
     int T, n_head, n_head_kv, n_qt;   // n_qt: query tiles in the schedule (an upper bound for varlen)
     float scale_log2;
-    __nv_bfloat16* out;
+    void* out;                        // bf16, or float32 with F32
     int ldo;
+    int q_head_stride;                // Q tile column of head h = h * q_head_stride
     // several sequences packed along the token axis (n_seq == 0: one sequence of T tokens)
     int n_seq;
     const int* cu_seqlens;   // [n_seq + 1] token offsets
     const int* tile_start;   // [n_seq + 1] prefix of ceil(len / 128)
     const int* vcol_start;   // [n_seq] first v^T column of each sequence (multiple of 8)
-    const __nv_bfloat16* gate;   // optional [T, n_head*hd]: out *= sigmoid(gate)
+    const __nv_bfloat16* gate;   // optional [T, n_head*hd]: out *= sigmoid(gate) (bf16 only)
     // one sequence (n_seq == 0): queries sit at positions p0 .. p0+T-1 and see
     // keys 0 .. p0+T-1 (kv_len = p0 + T)
     int p0, kv_len;
@@ -93,7 +102,7 @@ __device__ __forceinline__ float ex2(float x) {
 // to bf16 into the row's 128-byte-swizzled shared-memory slots, rs += sum(P).
 // DIAG masks keys past the query: key column col is hidden from this row when
 // col > row + dof (dof = first query position of the tile - first key position).
-template <bool DIAG, bool WRITE>
+template <bool DIAG, bool WRITE, int BKV>
 __device__ __forceinline__ void tile_pass(uint32_t tS, uint8_t* Prow, int sw, int row, int dof,
                                           float sl2, float m_ref, float& mx, float& rs) {
 #pragma unroll
@@ -129,11 +138,57 @@ __device__ __forceinline__ void tile_pass(uint32_t tS, uint8_t* Prow, int sw, in
     }
 }
 
-template <int HD>
+// Round a float32 to tf32 (10 fraction bits), nearest with ties to even.
+__device__ __forceinline__ float tf32_rne(float x) {
+    uint32_t u = __float_as_uint(x);
+    u += 0xFFFu + ((u >> 13) & 1u);
+    return __uint_as_float(u & ~0x1FFFu);
+}
+
+// The same pass on a 32-key tile with P as tf32 in float32 storage (one
+// 128-byte row per query: 16-byte chunk c/4 holds keys c .. c+3).
+template <bool DIAG, bool WRITE>
+__device__ __forceinline__ void tile_pass_f32(uint32_t tS, uint8_t* Prow, int sw, int row, int dof,
+                                              float sl2, float m_ref, float& mx, float& rs) {
+    uint32_t r[32];
+    __syncwarp();
+    ptx::tmem_ld32(tS, r);
+#pragma unroll
+    for (int c4 = 0; c4 < 8; ++c4) {
+        float e[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int col = c4 * 4 + t;
+            const float sv = __uint_as_float(r[col]);
+            const bool masked = DIAG && col > row + dof;
+            mx = masked ? mx : fmaxf(mx, sv);
+            if (WRITE) {
+                e[t] = masked ? 0.f : tf32_rne(ex2(fmaf(sv, sl2, -m_ref)));
+                rs += e[t];
+            }
+        }
+        if (WRITE)
+            *reinterpret_cast<uint4*>(Prow + ((c4 ^ sw) << 4)) =
+                make_uint4(__float_as_uint(e[0]), __float_as_uint(e[1]), __float_as_uint(e[2]),
+                           __float_as_uint(e[3]));
+    }
+}
+
+template <bool DIAG, bool WRITE, bool F32, int BKV>
+__device__ __forceinline__ void pass(uint32_t tS, uint8_t* Prow, int sw, int row, int dof,
+                                     float sl2, float m_ref, float& mx, float& rs) {
+    if constexpr (F32)
+        tile_pass_f32<DIAG, WRITE>(tS, Prow, sw, row, dof, sl2, m_ref, mx, rs);
+    else
+        tile_pass<DIAG, WRITE, BKV>(tS, Prow, sw, row, dof, sl2, m_ref, mx, rs);
+}
+
+template <int HD, bool F32>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const AParams p) {
-    using C = ACfg<HD>;
+    using C = ACfg<HD, F32>;
+    constexpr int BKV = C::BKV, AE = C::AE, KSTEP = C::KSTEP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -214,16 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tmV);
             ptx::mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
             for (int i = 0; i < 2; ++i)
-                for (int a = 0; a < HD / 64; ++a)
+                for (int a = 0; a < HD / AE; ++a)
                     ptx::tma_load_2d(&tmQ, q_full, sQ + i * C::Q_BYTES + a * BQ * 128,
-                                     (h0 + i) * HD + a * 64, seq_start + qt * BQ);
+                                     (h0 + i) * p.q_head_stride + a * AE, seq_start + qt * BQ);
             int k_issued = 0, v_issued[2] = {0, 0};
             for (int j = 0; j < n_kv; ++j) {
                 if (!ptx::wait_bounded(k_empty, (j & 1) ^ 1, abort_flag, &g_attn_err, ERRBIT_TIMEOUT))
                     break;
                 ptx::mbar_arrive_expect_tx(k_full, C::K_BYTES);
-                for (int a = 0; a < HD / 64; ++a)
-                    ptx::tma_load_2d(&tmK, k_full, sK + a * BKV * 128, g * HD + a * 64,
+                for (int a = 0; a < HD / AE; ++a)
+                    ptx::tma_load_2d(&tmK, k_full, sK + a * BKV * 128, g * HD + a * AE,
                                      seq_start + j * BKV);
                 ++k_issued;
                 const int vs = j & 1;
@@ -231,9 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        ERRBIT_TIMEOUT))
                     break;
                 ptx::mbar_arrive_expect_tx(&v_full[vs], C::V_BYTES);
-                for (int a = 0; a < BKV / 64; ++a)
+                for (int a = 0; a < BKV / AE; ++a)
                     ptx::tma_load_2d(&tmV, &v_full[vs], sV + vs * C::V_BYTES + a * HD * 128,
-                                     vstart + j * BKV + a * 64, g * HD);
+                                     vstart + j * BKV + a * AE, g * HD);
                 ++v_issued[vs];
             }
             if (*abort_flag) {
@@ -253,29 +308,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
-            const uint32_t idS = ptx::idesc_bf16_f32(BQ, BKV);
-            const uint32_t idO = ptx::idesc_bf16_f32(BQ, HD);
+            const uint32_t idS = F32 ? ptx::idesc_tf32_f32(BQ, BKV) : ptx::idesc_bf16_f32(BQ, BKV);
+            const uint32_t idO = F32 ? ptx::idesc_tf32_f32(BQ, HD) : ptx::idesc_bf16_f32(BQ, HD);
+            auto mma = [&](uint32_t d, uint64_t da, uint64_t db, uint32_t id, uint32_t acc) {
+                if constexpr (F32) ptx::umma_tf32_ss(d, da, db, id, acc);
+                else ptx::umma_bf16_ss(d, da, db, id, acc);
+            };
             auto issue_S = [&](int i) {
                 const uint32_t d = tmem_base + C::S_COL0 + i * BKV;
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
+                for (int kk = 0; kk < HD / KSTEP; ++kk) {
                     const int a = kk / 4, off = (kk % 4) * 32;
                     const uint64_t da =
                         ptx::sdesc_sw128(ptx::smem_u32(sQ + i * C::Q_BYTES + a * BQ * 128 + off));
                     const uint64_t db = ptx::sdesc_sw128(ptx::smem_u32(sK + a * BKV * 128 + off));
-                    ptx::umma_bf16_ss(d, da, db, idS, kk > 0 ? 1u : 0u);
+                    mma(d, da, db, idS, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_PV = [&](int i, int vs, int j) {
                 const uint32_t d = tmem_base + C::O_COL0 + i * HD;
 #pragma unroll
-                for (int kk = 0; kk < BKV / 16; ++kk) {
+                for (int kk = 0; kk < BKV / KSTEP; ++kk) {
                     const int a = kk / 4, off = (kk % 4) * 32;
                     const uint64_t da =
                         ptx::sdesc_sw128(ptx::smem_u32(sP + i * C::P_BYTES + a * BQ * 128 + off));
                     const uint64_t db = ptx::sdesc_sw128(
                         ptx::smem_u32(sV + vs * C::V_BYTES + a * HD * 128 + off));
-                    ptx::umma_bf16_ss(d, da, db, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma(d, da, db, idO, (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };
             auto W = [&](uint64_t* b, uint32_t par) {
@@ -359,11 +418,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the warp redoes the pass.
             float mx = -INFINITY, rs = 0.f;
             if (j > 0) {
-                if (diag) tile_pass<true, true>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
-                else tile_pass<false, true>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
+                if (diag) pass<true, true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
+                else pass<false, true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
             } else {
-                if (diag) tile_pass<true, false>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
-                else tile_pass<false, false>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
+                if (diag) pass<true, false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
+                else pass<false, false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
             }
             const float m_tile = mx * sl2;
             const bool need = (j == 0) || (m_tile > m + kRescaleLog2);
@@ -388,8 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 rs = 0.f;
                 float unused = -INFINITY;
-                if (diag) tile_pass<true, true>(tS, Prow, sw, row, dof, sl2, m, unused, rs);
-                else tile_pass<false, true>(tS, Prow, sw, row, dof, sl2, m, unused, rs);
+                if (diag) pass<true, true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, unused, rs);
+                else pass<false, true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, unused, rs);
             }
             l += rs;
             ptx::fence_proxy_async_smem();
@@ -402,13 +461,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__all_sync(0xffffffffu, ok)) {
                 ptx::tc_fence_after();
                 const float inv = 1.0f / l;
-                __nv_bfloat16* orow = p.out + (size_t)qrow * p.ldo + (size_t)(h0 + i) * HD;
+                const size_t obase = (size_t)qrow * p.ldo + (size_t)(h0 + i) * HD;
+                __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + obase;
+                float* orow32 = reinterpret_cast<float*>(p.out) + obase;
 #pragma unroll 1
                 for (int c = 0; c < HD; c += 32) {
                     uint32_t r[32];
                     __syncwarp();
                     ptx::tmem_ld32(tO + c, r);
-                    if (qrel < seq_len && qrow < p.T) {
+                    if (F32 && qrel < seq_len && qrow < p.T) {
+#pragma unroll
+                        for (int t = 0; t < 32; t += 4)
+                            *reinterpret_cast<float4*>(orow32 + c + t) =
+                                make_float4(__uint_as_float(r[t]) * inv, __uint_as_float(r[t + 1]) * inv,
+                                            __uint_as_float(r[t + 2]) * inv,
+                                            __uint_as_float(r[t + 3]) * inv);
+                    } else if (qrel < seq_len && qrow < p.T) {
 #pragma unroll
                         for (int t = 0; t < 32; t += 8) {
                             float o[8];
@@ -444,21 +512,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int HD>
+template <int HD, bool F32>
 cudaError_t launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const AParams& p, cudaStream_t s) {
-    using C = ACfg<HD>;
+    using C = ACfg<HD, F32>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<HD>,
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<HD, F32>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int G = p.n_head / p.n_head_kv;
     const int grid = p.n_qt * p.n_head_kv * (G / 2);
-    attn_tc_kernel<HD><<<grid, kThreads, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
+    attn_tc_kernel<HD, F32><<<grid, kThreads, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
+}
+
+// q [T, ldq] (head h at column h * q_head_stride), k [kv rows, ldk], v^T
+// [n_head_kv * hd, ldvt] (vt_cols columns), out [T, n_head * hd].
+template <bool F32>
+cudaError_t launch_attn(const void* q, long long ldq, int q_head_stride, const void* k,
+                        long long ldk, const void* vt, long long ldvt, long long vt_cols, void* out,
+                        int T, int n_head, int n_head_kv, int head_dim, float scale,
+                        const AttnVarlen& vl, cudaStream_t s) {
+    if (!attn_tc_supported(n_head, n_head_kv, head_dim)) return cudaErrorNotSupported;
+    if (F32 && vl.gate) return cudaErrorNotSupported;
+    using C = ACfg<128, F32>;     // element geometry does not depend on HD
+    const CUtensorMapDataType dt =
+        F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tq, tk, tv;
+    const int hd = head_dim;
+    // keys: T rows, or p0 + T rows of a KV state (the map ends there, so keys past
+    // the last query read zeros, never stale state)
+    const int kv_len = vl.n_seq > 0 ? T : vl.p0 + T;
+    if (!make_tmap_2d(&tq, q, dt, C::EB, T, (uint64_t)n_head * q_head_stride, (uint64_t)ldq, BQ,
+                      C::AE) ||
+        !make_tmap_2d(&tk, k, dt, C::EB, kv_len, (uint64_t)n_head_kv * hd, (uint64_t)ldk, C::BKV,
+                      C::AE) ||
+        !make_tmap_2d(&tv, vt, dt, C::EB, (uint64_t)n_head_kv * hd, (uint64_t)vt_cols,
+                      (uint64_t)ldvt, hd, C::AE))
+        return cudaErrorInvalidValue;
+    AParams p;
+    p.T = T;
+    p.n_head = n_head;
+    p.n_head_kv = n_head_kv;
+    p.n_qt = vl.n_seq > 0 ? (T + BQ - 1) / BQ + vl.n_seq : (T + BQ - 1) / BQ;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = out;
+    p.ldo = n_head * hd;
+    p.q_head_stride = q_head_stride;
+    p.n_seq = vl.n_seq;
+    p.cu_seqlens = vl.cu_seqlens;
+    p.tile_start = vl.tile_start;
+    p.vcol_start = vl.vcol_start;
+    p.gate = vl.gate;
+    p.p0 = vl.n_seq > 0 ? 0 : vl.p0;
+    p.kv_len = kv_len;
+    LaunchScope ls(DTP_K_ATTN, s);
+    if (hd == 128) return launch_hd<128, F32>(tq, tk, tv, p, s);
+    return launch_hd<64, F32>(tq, tk, tv, p, s);
 }
 
 }  // namespace
@@ -476,37 +589,17 @@ cudaError_t launch_attn_tc_varlen(const __nv_bfloat16* q, const __nv_bfloat16* k
                                   __nv_bfloat16* out, int T, int n_head, int n_head_kv,
                                   int head_dim, float scale, const AttnVarlen& vl,
                                   cudaStream_t s) {
-    if (!attn_tc_supported(n_head, n_head_kv, head_dim)) return cudaErrorNotSupported;
-    CUtensorMap tq, tk, tv;
-    const int hd = head_dim;
-    // keys: T rows, or p0 + T rows of a KV state (the map ends there, so keys past
-    // the last query read zeros, never stale state)
-    const int kv_len = vl.n_seq > 0 ? T : vl.p0 + T;
-    if (!make_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, (uint64_t)n_head * hd,
-                      (uint64_t)n_head * hd, BQ, 64) ||
-        !make_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_len, (uint64_t)n_head_kv * hd,
-                      (uint64_t)n_head_kv * hd, BKV, 64) ||
-        !make_tmap_2d(&tv, vt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)n_head_kv * hd,
-                      (uint64_t)vt_cols, (uint64_t)ldvt, hd, 64))
-        return cudaErrorInvalidValue;
-    AParams p;
-    p.T = T;
-    p.n_head = n_head;
-    p.n_head_kv = n_head_kv;
-    p.n_qt = vl.n_seq > 0 ? (T + BQ - 1) / BQ + vl.n_seq : (T + BQ - 1) / BQ;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.out = out;
-    p.ldo = n_head * hd;
-    p.n_seq = vl.n_seq;
-    p.cu_seqlens = vl.cu_seqlens;
-    p.tile_start = vl.tile_start;
-    p.vcol_start = vl.vcol_start;
-    p.gate = vl.gate;
-    p.p0 = vl.n_seq > 0 ? 0 : vl.p0;
-    p.kv_len = kv_len;
-    LaunchScope ls(DTP_K_ATTN, s);
-    if (hd == 128) return launch_hd<128>(tq, tk, tv, p, s);
-    return launch_hd<64>(tq, tk, tv, p, s);
+    const long long nq = (long long)n_head * head_dim, nk = (long long)n_head_kv * head_dim;
+    return launch_attn<false>(q, nq, head_dim, k, nk, vt, ldvt, vt_cols, out, T, n_head,
+                              n_head_kv, head_dim, scale, vl, s);
+}
+
+cudaError_t launch_attn_tc_f32(const float* q, long long ldq, int q_head_stride, const float* k,
+                               long long ldk, const float* vt, long long ldvt, long long vt_cols,
+                               float* out, int T, int n_head, int n_head_kv, int head_dim,
+                               float scale, const AttnVarlen& vl, cudaStream_t s) {
+    return launch_attn<true>(q, ldq, q_head_stride, k, ldk, vt, ldvt, vt_cols, out, T, n_head,
+                             n_head_kv, head_dim, scale, vl, s);
 }
 
 }  // namespace dtp

@@ -242,6 +242,10 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_s
     } else {
         W.qkv = take((size_t)T * (nq * (1 + c->attn_gate) + 2 * nk) * 4);
         W.gu = take((size_t)T * 2 * F * 4);
+        if (c->precision == DTP_PREC_TF32) {     // v^T for the tcgen05 tf32 attention
+            W.ldvt = (long long)align_up((size_t)T, 8);
+            W.vt = take(nk * (size_t)W.ldvt * 4);
+        }
     }
     if (host) {
         W.tokens = take((size_t)T * 4);
@@ -299,10 +303,12 @@ struct KvState {
 static KvState kv_state_layout(const dtp_config* c, int max_T) {
     KvState S;
     const size_t nk = (size_t)c->n_head_kv * c->head_dim;
-    if (c->precision == DTP_PREC_BF16 || c->precision == DTP_PREC_E4M3) {
+    if (c->precision == DTP_PREC_BF16 || c->precision == DTP_PREC_E4M3 ||
+        c->precision == DTP_PREC_TF32) {       // K, then V^T (what the tcgen05 attention reads)
+        const size_t eb = c->precision == DTP_PREC_TF32 ? 4 : 2;
         S.ldvt = (long long)align_up((size_t)max_T, 8);
-        S.v_off = align_up((size_t)max_T * nk * 2, 256);
-        S.layer_bytes = S.v_off + align_up(nk * (size_t)S.ldvt * 2, 256);
+        S.v_off = align_up((size_t)max_T * nk * eb, 256);
+        S.layer_bytes = S.v_off + align_up(nk * (size_t)S.ldvt * eb, 256);
     } else {
         S.v_off = align_up((size_t)max_T * nk * 4, 256);
         S.layer_bytes = 2 * S.v_off;
@@ -332,6 +338,10 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
     // rounded to tf32 by the kernel that writes it; otherwise the SIMT GEMM
     const bool tc = c->precision == DTP_PREC_TF32;
     const int opd = tc ? DTP_TF32 : DTP_F32;
+    // the tcgen05 tf32 attention covers a single sequence (packed sequences and
+    // chunks run the float32 SIMT attention on the same tf32 values)
+    const bool tca = tc && !V.n_seq && attn_tc_supported(h, g, hd) && aligned(qkv, 16) &&
+                     nqkv % 4 == 0 && nqc % 4 == 0;
     auto gemm = [&](const float* a, const float* w, float* y, int M, int N, int K,
                     const float* res, int kind) -> cudaError_t {
         if (!tc) return launch_gemm_simt(a, K, w, y, DTP_F32, N, M, N, K, res, s, kind);
@@ -354,19 +364,33 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
                                       c->rms_eps, s));
         DTP_CUDA_CHECK(gemm(hb, (const float*)(lp + L.w_qkv), qkv, T, nqkv, d, nullptr,
                             DTP_K_GEMM_QKV));
-        DTP_CUDA_CHECK(launch_qk_norm_rope(qkv, DTP_F32, nqkv, (const float*)(lp + L.q_norm),
+        // tf32 mode: q, k and v are rounded to tf32 here (the tensor-core
+        // attention's operands); the other attention paths see the same values
+        DTP_CUDA_CHECK(launch_qk_norm_rope(qkv, opd, nqkv, (const float*)(lp + L.q_norm),
                                            V.tok_pos, T, h, hd, c->rope_dim_count,
                                            c->rope_freq_base, c->rms_eps, s, qstride, S.p0));
-        DTP_CUDA_CHECK(launch_qk_norm_rope(qkv + nqc, DTP_F32, nqkv, (const float*)(lp + L.k_norm),
+        DTP_CUDA_CHECK(launch_qk_norm_rope(qkv + nqc, opd, nqkv, (const float*)(lp + L.k_norm),
                                            V.tok_pos, T, g, hd, c->rope_dim_count,
                                            c->rope_freq_base, c->rms_eps, s, 0, S.p0));
+        if (tc) DTP_CUDA_CHECK(launch_round_tf32_rows(qkv + nqc + nk, nqkv, T, nk, s));
         if (o.k_cache)
             DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc, nqkv,
                                                 (float*)o.k_cache + (size_t)l * T * nk, nk, T, nk, s));
         if (o.v_cache)
             DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc + nk, nqkv,
                                                 (float*)o.v_cache + (size_t)l * T * nk, nk, T, nk, s));
-        if (S.base) {           // chunked: append this chunk's keys and values to the state
+        if (S.base && tca) {    // chunked, tf32: K rows and V^T columns at p0, tcgen05 attention
+            float* ks = (float*)S.k(l);
+            float* vts = (float*)S.v(l);
+            DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc, nqkv, ks + (size_t)S.p0 * nk, nk, T,
+                                                nk, s));
+            DTP_CUDA_CHECK(launch_transpose_v_f32(qkv + nqc + nk, nqkv, vts + S.p0, T, nk,
+                                                  (int)S.ldvt, s));
+            AttnVarlen vl;
+            vl.p0 = S.p0;
+            DTP_CUDA_CHECK(launch_attn_tc_f32(qkv, nqkv, qstride, ks, nk, vts, S.ldvt, S.p0 + T,
+                                              attn, T, h, g, hd, scale, vl, s));
+        } else if (S.base) {    // chunked: append this chunk's keys and values to the state
             float* ks = (float*)S.k(l);
             float* vs = (float*)S.v(l);
             DTP_CUDA_CHECK(launch_copy_rows_f32(qkv + nqc, nqkv, ks + (size_t)S.p0 * nk, nk, T,
@@ -375,6 +399,13 @@ static int fwd_f32(const dtp_config* c, const uint8_t* P, const PackedLayout& L,
                                                 T, nk, s));
             DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, ks, nk, vs, nk, 0, attn, nq, DTP_F32, T, h,
                                             g, hd, scale, s, nullptr, qstride, S.p0));
+        } else if (tca) {
+            // one sequence: the tcgen05 attention on tf32 q / k / v^T
+            float* vt = (float*)(ws + W.vt);
+            DTP_CUDA_CHECK(launch_transpose_v_f32(qkv + nqc + nk, nqkv, vt, T, nk, (int)W.ldvt, s));
+            AttnVarlen none;
+            DTP_CUDA_CHECK(launch_attn_tc_f32(qkv, nqkv, qstride, qkv + nqc, nqkv, vt, W.ldvt, T,
+                                              attn, T, h, g, hd, scale, none, s));
         } else {
             DTP_CUDA_CHECK(launch_attn_simt(qkv, nqkv, qkv + nqc, nqkv, qkv + nqc + nk, nqkv, 0,
                                             attn, nq, DTP_F32, T, h, g, hd, scale, s, V.tok_pos,
@@ -934,15 +965,18 @@ int dtp_qk_norm_rope_neox(void* x, int dtype, const float* w_norm, const int32_t
 }
 
 size_t dtp_sdpa_workspace_size(int T, int n_head_kv, int head_dim, int dtype) {
-    if (T <= 0 || n_head_kv <= 0 || head_dim <= 0 || dtype != DTP_BF16) return 0;
-    return align_up((size_t)n_head_kv * head_dim * align_up(T, 8) * 2, 256);
+    if (T <= 0 || n_head_kv <= 0 || head_dim <= 0 || (dtype != DTP_BF16 && dtype != DTP_TF32))
+        return 0;
+    const size_t eb = dtype == DTP_TF32 ? 4 : 2;
+    return align_up((size_t)n_head_kv * head_dim * align_up(T, 8) * eb, 256);
 }
 
 int dtp_sdpa_causal_gqa(const void* q, const void* k, const void* v, void* out, int dtype, int T,
                         int n_head, int n_head_kv, int head_dim, float scale, void* workspace,
                         size_t ws_bytes, dtp_stream_t stream) {
     if (!q || !k || !v || !out) return fail(DTP_ERR_INVALID_ARG, "NULL pointer");
-    if (dtype != DTP_F32 && dtype != DTP_BF16) return fail(DTP_ERR_INVALID_ARG, "bad dtype");
+    if (dtype != DTP_F32 && dtype != DTP_BF16 && dtype != DTP_TF32)
+        return fail(DTP_ERR_INVALID_ARG, "bad dtype");
     if (T <= 0 || n_head <= 0 || n_head_kv <= 0 || head_dim <= 0)
         return fail(DTP_ERR_INVALID_ARG, "sizes must be >= 1");
     if (n_head % n_head_kv) return fail(DTP_ERR_INVALID_ARG, "n_head %% n_head_kv != 0");
@@ -956,13 +990,23 @@ int dtp_sdpa_causal_gqa(const void* q, const void* k, const void* v, void* out, 
     }
     if (!attn_tc_supported(n_head, n_head_kv, head_dim))
         return fail(DTP_ERR_UNSUPPORTED,
-                    "bf16 attention: head_dim must be 64 or 128 and n_head/n_head_kv even");
+                    "tensor-core attention: head_dim must be 64 or 128 and n_head/n_head_kv even");
     const size_t need = dtp_sdpa_workspace_size(T, n_head_kv, head_dim, dtype);
     if (!workspace || ws_bytes < need)
         return fail(DTP_ERR_WORKSPACE, "sdpa workspace %zu < %zu bytes", ws_bytes, need);
     if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(k, 16) || !aligned(out, 16))
         return fail(DTP_ERR_INVALID_ARG, "q, k, out must be 16-byte and workspace 256-byte aligned");
     const long long ldvt = (long long)align_up(T, 8);
+    if (dtype == DTP_TF32) {
+        const int nq = n_head * head_dim, nk = n_head_kv * head_dim;
+        float* vt32 = (float*)workspace;
+        DTP_CUDA_CHECK(launch_transpose_v_f32((const float*)v, nk, vt32, T, nk, (int)ldvt, s));
+        AttnVarlen none;
+        DTP_CUDA_CHECK(launch_attn_tc_f32((const float*)q, nq, head_dim, (const float*)k, nk, vt32,
+                                          ldvt, T, (float*)out, T, n_head, n_head_kv, head_dim,
+                                          scale, none, s));
+        return DTP_OK;
+    }
     __nv_bfloat16* vt = (__nv_bfloat16*)workspace;
     DTP_CUDA_CHECK(launch_transpose_v((const __nv_bfloat16*)v, vt, T, n_head_kv * head_dim,
                                       (int)ldvt, s));

@@ -69,6 +69,10 @@ cudaError_t launch_swiglu(const void* gate, const void* up, void* out, int dtype
 cudaError_t launch_swiglu_interleaved64(const float* gu, float* act, int T, int F,
                                         cudaStream_t s, int act_dtype = DTP_F32);
 cudaError_t launch_round_tf32(float* x, size_t n, cudaStream_t s);
+cudaError_t launch_round_tf32_rows(float* x, int ld, int rows, int cols, cudaStream_t s);
+// v [T, ldv] float32 -> vt [width, ldt] (key index contiguous)
+cudaError_t launch_transpose_v_f32(const float* v, int ldv, float* vt, int T, int width, int ldt,
+                                   cudaStream_t s);
 // Per-row e4m3 quantisation (quant.cu): codes q [rows, cols] (row-major, no
 // padding) and scale [rows] = max|row| / 448.
 cudaError_t launch_rmsnorm_e4m3(const float* x, const float* w, uint8_t* q, float* scale,
@@ -178,6 +182,14 @@ cudaError_t launch_attn_tc_varlen(const __nv_bfloat16* q, const __nv_bfloat16* k
                                   __nv_bfloat16* out, int T, int n_head, int n_head_kv,
                                   int head_dim, float scale, const AttnVarlen& vl,
                                   cudaStream_t s);
+// The same flash attention on float32 q / k / v^T holding tf32 values (kind::tf32,
+// P rounded to tf32, float32 output; no gate): q [T, ldq] with head h at column
+// h * q_head_stride, k [rows, ldk], v^T [n_head_kv * hd, ldvt]; ldq, ldk, ldvt
+// multiples of 4, 16-byte aligned bases.
+cudaError_t launch_attn_tc_f32(const float* q, long long ldq, int q_head_stride, const float* k,
+                               long long ldk, const float* vt, long long ldvt, long long vt_cols,
+                               float* out, int T, int n_head, int n_head_kv, int head_dim,
+                               float scale, const AttnVarlen& vl, cudaStream_t s);
 bool attn_tc_supported(int n_head, int n_head_kv, int head_dim);
 
 }  // namespace dtp

@@ -297,6 +297,10 @@ cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
         qk_norm_rope_kernel<<<T, warps * 32, smem, s>>>((__nv_bfloat16*)x, ld, w_norm, pos,
                                                         n_heads, head_dim, rope_dims,
                                                         (double)freq_base, eps, head_stride, pos0);
+    else if (dtype == DTP_TF32)     // float32 storage, results rounded to tf32
+        qk_norm_rope_kernel<<<T, warps * 32, smem, s>>>((tf32_t*)x, ld, w_norm, pos, n_heads,
+                                                        head_dim, rope_dims, (double)freq_base,
+                                                        eps, head_stride, pos0);
     else
         qk_norm_rope_kernel<<<T, warps * 32, smem, s>>>((float*)x, ld, w_norm, pos, n_heads,
                                                         head_dim, rope_dims, (double)freq_base,
@@ -544,13 +548,14 @@ cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, con
 
 // ----------------------------------------------------------------------------- v transpose
 // v [T, width] -> vt [width, ldt] (key index contiguous), 32x32 tiles via smem.
-__global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v,
-                                   __nv_bfloat16* __restrict__ vt, int T, int width, int ldt) {
-    __shared__ __nv_bfloat16 tile[32][33];
+template <typename E>
+__global__ void transpose_v_kernel(const E* __restrict__ v, int ldv, E* __restrict__ vt, int T,
+                                   int width, int ldt) {
+    __shared__ E tile[32][33];
     const int t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
     for (int i = threadIdx.y; i < 32; i += blockDim.y) {
         const int t = t0 + i, c = c0 + threadIdx.x;
-        tile[i][threadIdx.x] = (t < T && c < width) ? v[(size_t)t * width + c] : __float2bfloat16(0.f);
+        tile[i][threadIdx.x] = (t < T && c < width) ? v[(size_t)t * ldv + c] : E(0.f);
     }
     __syncthreads();
     for (int i = threadIdx.y; i < 32; i += blockDim.y) {
@@ -563,7 +568,33 @@ cudaError_t launch_transpose_v(const __nv_bfloat16* v, __nv_bfloat16* vt, int T,
                                int ldt, cudaStream_t s) {
     LaunchScope ls(DTP_K_OTHER, s);
     dim3 grid((T + 31) / 32, (width + 31) / 32), block(32, 8);
-    transpose_v_kernel<<<grid, block, 0, s>>>(v, vt, T, width, ldt);
+    transpose_v_kernel<<<grid, block, 0, s>>>(v, width, vt, T, width, ldt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_v_f32(const float* v, int ldv, float* vt, int T, int width, int ldt,
+                                   cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    dim3 grid((T + 31) / 32, (width + 31) / 32), block(32, 8);
+    transpose_v_kernel<<<grid, block, 0, s>>>(v, ldv, vt, T, width, ldt);
+    return cudaGetLastError();
+}
+
+// x[r, c] = round_tf32(x[r, c]) for r < rows, c < cols (row stride ld).
+__global__ void round_tf32_rows_kernel(float* __restrict__ x, int ld, int rows, int cols) {
+    const size_t n = (size_t)rows * cols;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float* e = x + (i / cols) * ld + (i % cols);
+        *e = round_tf32(*e);
+    }
+}
+
+cudaError_t launch_round_tf32_rows(float* x, int ld, int rows, int cols, cudaStream_t s) {
+    LaunchScope ls(DTP_K_OTHER, s);
+    size_t n = (size_t)rows * cols, blocks = (n + 255) / 256;
+    if (blocks > 65535 * 8) blocks = 65535 * 8;
+    round_tf32_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, ld, rows, cols);
     return cudaGetLastError();
 }
 

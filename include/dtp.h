@@ -214,8 +214,10 @@ int dtp_fwd_prefill_varlen(const dtp_config* cfg, const void* packed, size_t pac
  *   DTP_PREC_BF16 / DTP_PREC_E4M3:
  *                  K  bf16 [max_T, nk] token-major, then (256-byte aligned)
  *                  V^T bf16 [nk, ldvt], ldvt = max_T rounded up to 8
- *   DTP_PREC_F32 / DTP_PREC_TF32:
- *                  K  f32 [max_T, nk], then (256-byte aligned) V f32 [max_T, nk]
+ *   DTP_PREC_TF32: the same with float32 elements (with a head_dim other than 64
+ *                  or 128, or an odd n_head / n_head_kv, V is token-major
+ *                  [max_T, nk] inside the V^T region instead)
+ *   DTP_PREC_F32:  K  f32 [max_T, nk], then (256-byte aligned) V f32 [max_T, nk]
  * Positions >= p0 + C are neither read nor written.  Calls on one state run
  * in position order (the stream orders them).
  *   tokens     device uint32 [C]
@@ -308,9 +310,10 @@ size_t dtp_sdpa_workspace_size(int T, int n_head_kv, int head_dim, int dtype);
  * q, out device [T, n_head*head_dim]; k, v device [T, n_head_kv*head_dim];
  * all of dtype.  DTP_F32: float32 SIMT kernel.  DTP_BF16: tcgen05 flash
  * attention (bf16 operands, float32 scores/softmax/accumulation, P rounded to
- * bf16 for the PV product); requires head_dim 64 or 128 and an even group
- * size n_head / n_head_kv, and a workspace of dtp_sdpa_workspace_size bytes
- * (device, 256-byte aligned). */
+ * bf16 for the PV product).  DTP_TF32: the same on float32 buffers holding tf32
+ * values (kind::tf32, P rounded to tf32, float32 output).  The tensor-core
+ * kinds require head_dim 64 or 128 and an even group size n_head / n_head_kv,
+ * and a workspace of dtp_sdpa_workspace_size bytes (device, 256-byte aligned). */
 int dtp_sdpa_causal_gqa(const void* q, const void* k, const void* v, void* out, int dtype, int T,
                         int n_head, int n_head_kv, int head_dim, float scale, void* workspace,
                         size_t ws_bytes, dtp_stream_t stream);

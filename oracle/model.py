@@ -29,8 +29,8 @@ sites, not their bodies):
     q/k/v handed to attention are rounded to bf16 (nearest, ties to even); all
     sums and the residual stream stay in float64.
   * tf32-operand mode: the same GEMM operands rounded to TensorFloat-32 (10-bit
-    fraction, nearest, ties to even) instead; q/k/v and the gate stay unrounded
-    (that mode's attention reads float32).
+    fraction, nearest, ties to even) instead, and q/k/v as well (that mode's
+    tensor-core attention reads tf32); the gate stays unrounded.
   * fp8-operand mode (the quantised-weight variant; the pages' T-parallel path
     quantises weights and activations to 8 bits in blocks): every GEMM operand
     is quantised per row to OCP E4M3 with a float32 scale max|row| / 448 --
@@ -98,23 +98,23 @@ def fake_quant_rows_e4m3(a) -> np.ndarray:
 def _rounders(bf16_operands: bool, tf32_operands: bool, fp8_operands: bool = False):
     """Roundings of a mode: (GEMM input written from float32 -- the normed h, z and
     final hn; GEMM input stored as bf16 first -- attention output and SwiGLU act;
-    weight matrices; attention operands q/k/v and the gate).
-      bf16: bf16 everywhere (the tensor-core attention reads bf16 q/k/v).
-      tf32: tf32 for the GEMM operands; attention operands unrounded (that mode's
-            attention runs on float32).
+    weight matrices; attention operands q/k/v; the attention gate).
+      bf16: bf16 everywhere (the tensor-core attention reads bf16 q/k/v and gate).
+      tf32: tf32 for the GEMM operands and for q/k/v (that mode's tensor-core
+            attention reads tf32); the gate stays float32.
       fp8:  per-row e4m3 for the GEMM operands (the attention output and act are
-            bf16 before they are quantised); bf16 attention operands."""
+            bf16 before they are quantised); bf16 attention operands and gate."""
     ident = lambda a: a
     if bf16_operands + tf32_operands + fp8_operands > 1:
         raise ValueError("the operand modes are exclusive")
     if bf16_operands:
-        return round_bf16, round_bf16, round_bf16, round_bf16
+        return round_bf16, round_bf16, round_bf16, round_bf16, round_bf16
     if tf32_operands:
-        return round_tf32, round_tf32, round_tf32, ident
+        return round_tf32, round_tf32, round_tf32, round_tf32, ident
     if fp8_operands:
         fq = fake_quant_rows_e4m3
-        return fq, (lambda a: fq(round_bf16(a))), fq, round_bf16
-    return ident, ident, ident, ident
+        return fq, (lambda a: fq(round_bf16(a))), fq, round_bf16, round_bf16
+    return ident, ident, ident, ident, ident
 
 
 # --------------------------------------------------------------------------------------
@@ -244,7 +244,7 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     `kv_prefix` = (k, v) of the p0 positions before x (which then sits at
     positions pos = p0 .. p0+T-1): attention runs over those keys followed by
     x's own, the only way earlier positions reach later ones."""
-    op, opm, opw, opa = _rounders(bf16_operands, tf32_operands, fp8_operands)
+    op, opm, opw, opa, opg = _rounders(bf16_operands, tf32_operands, fp8_operands)
     L = _mats(lw, opw)
     d, h, g, hd = cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim
     eps = cfg.rms_eps
@@ -255,7 +255,7 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     gate = None
     if getattr(cfg, "attn_gate", False):
         qg = q.reshape(q.shape[0], h, 2, hd)
-        q, gate = qg[:, :, 0, :].reshape(-1, h * hd), opa(qg[:, :, 1, :].reshape(-1, h * hd))
+        q, gate = qg[:, :, 0, :].reshape(-1, h * hd), opg(qg[:, :, 1, :].reshape(-1, h * hd))
     k = linear(hN, L["wk"])
     v = linear(hN, L["wv"])
     q = qk_norm(q, L["q_norm"], hd, eps)
@@ -294,7 +294,7 @@ def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidd
     stream entering output_norm."""
     tokens = np.asarray(tokens, dtype=np.int64)
     T = tokens.shape[0]
-    op, _, opw, _ = _rounders(bf16_operands, tf32_operands, fp8_operands)
+    op, _, opw, _, _ = _rounders(bf16_operands, tf32_operands, fp8_operands)
     emb = np.asarray(weights["tok_embd"], dtype=F64)
     x = emb[tokens]
     if bf16_operands or fp8_operands:       # the table is stored as bf16
@@ -324,7 +324,7 @@ def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: boo
     with this chunk's.  The chunks' logits, concatenated, are forward(tokens)'s."""
     tokens = np.asarray(tokens, dtype=np.int64)
     C = tokens.shape[0]
-    op, _, opw, _ = _rounders(bf16_operands, tf32_operands, fp8_operands)
+    op, _, opw, _, _ = _rounders(bf16_operands, tf32_operands, fp8_operands)
     first = len(kv_state) == 0
     p0 = 0 if first else kv_state[0][0].shape[0]
     x = np.asarray(weights["tok_embd"], dtype=F64)[tokens]

@@ -94,13 +94,14 @@ def test_chunk_state_size_and_rejections(dtp):
     rejects bad ranges and buffers before enqueueing anything."""
     L = dtp.lib()
     up = lambda x, a: (x + a - 1) // a * a
-    for prec in ("bf16", "f32"):
+    for prec in ("bf16", "e4m3", "tf32", "f32"):
         cfg = synth.CONFIGS["small"].replace(precision=prec)
         c = dtp.config_from(cfg)
         nk = cfg.n_head_kv * cfg.head_dim
         for max_T in (1, 100, 256, 4099):
-            if prec == "bf16":
-                per = up(max_T * nk * 2, 256) + up(nk * up(max_T, 8) * 2, 256)
+            if prec != "f32":           # K then V^T
+                eb = 4 if prec == "tf32" else 2
+                per = up(max_T * nk * eb, 256) + up(nk * up(max_T, 8) * eb, 256)
             else:
                 per = 2 * up(max_T * nk * 4, 256)
             assert dtp.kv_state_size(c, max_T) == cfg.n_layer * per

@@ -49,14 +49,14 @@ def assert_parity(cfg, gl, gh, rl, rh):
         return metrics
     if cfg.precision == "tf32":
         # Against the oracle's tf32-operand mode: the same operands are rounded
-        # on both sides, so differences are float32-level, amplified only where
-        # that moves a value across a tf32 rounding boundary (one tf32 ulp,
-        # u = 2^-11); bounded like the bf16 case with the tf32 u and no factor 2.
+        # on both sides, but the tensor-core attention also rounds P to tf32
+        # before the PV product, which the oracle's definition does not model --
+        # the bf16 situation with u = 2^-11, so the bf16 bounds with that u.
         u = 2.0 ** -11
         assert layer_err[0] == 0.0, metrics
         for l in range(1, cfg.n_layer + 1):
-            assert layer_err[l] <= u * np.sqrt(l), (l, metrics)
-        assert metrics["logit_rel_l2"] <= u * np.sqrt(cfg.n_layer + 1), metrics
+            assert layer_err[l] <= 2 * u * np.sqrt(l), (l, metrics)
+        assert metrics["logit_rel_l2"] <= 2 * u * np.sqrt(cfg.n_layer + 1) + u, metrics
         agree, structured = argmax_agreement_near_tie(gl, rl, 2 * metrics["logit_max_abs"])
         metrics.update(argmax_agreement=agree, structured_flips=structured)
         assert structured == 0 and agree >= 0.995, metrics
@@ -383,12 +383,12 @@ def test_chunked_prefill_state_is_the_kv_cache(dtp, prec):
         lay = state[l * per:(l + 1) * per]
         ks = lay[:max_T * nk * eb].view(cdt).view(max_T, nk)
         assert torch.equal(ks[:T], kc[l])
-        if prec != "bf16":
+        if prec == "f32":
             vs = lay[k_bytes:k_bytes + max_T * nk * 4].view(cdt).view(max_T, nk)
             assert torch.equal(vs[:T], vc[l])
-        else:
+        else:               # V^T, key index contiguous
             ldvt = up(max_T, 8)
-            vt = lay[k_bytes:k_bytes + nk * ldvt * 2].view(cdt).view(nk, ldvt)
+            vt = lay[k_bytes:k_bytes + nk * ldvt * eb].view(cdt).view(nk, ldvt)
             assert torch.equal(vt[:, :T].t(), vc[l])
 
 

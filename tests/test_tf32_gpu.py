@@ -99,3 +99,22 @@ def test_forward_tf32_gated(dtp):
     _, gl, gh = run_gpu(dtp, cfg, T=200)
     _, rl, rh = oracle_forward(cfg, T=200)
     assert_parity(cfg, gl, gh, rl, rh)
+
+
+@pytest.mark.parametrize("T,nh,nkv,hd", [(1, 4, 2, 64), (33, 4, 2, 64), (130, 8, 4, 128),
+                                         (300, 4, 2, 128), (1000, 8, 2, 128)])
+def test_sdpa_tf32_tensor_core(dtp, T, nh, nkv, hd):
+    """The tcgen05 kind::tf32 flash attention against float64 on the same tf32
+    q/k/v.  P is rounded to tf32 (2^-11 relative) before the PV product and both
+    products accumulate in float32: bound 2^-9 * max|out| (4x the P rounding)."""
+    a = synth.attention_inputs(T, nh, nkv, hd, seed=21)
+    q, k, v = (oracle.round_tf32(a[n]).astype(np.float32) for n in ("q", "k", "v"))
+    out = torch.empty((T, nh * hd), dtype=torch.float32, device=dev)
+    ws = torch.empty(dtp.sdpa_workspace_size(T, nkv, hd, dtp.DTP_TF32), dtype=torch.uint8,
+                     device=dev)
+    sc = 1 / np.sqrt(hd)
+    dtp.sdpa_causal_gqa(t32(q), t32(k), t32(v), out, nh, nkv, hd, sc, workspace=ws, tf32=True)
+    torch.cuda.synchronize()
+    dtp.check()
+    ref = oracle.sdpa_causal_gqa(q, k, v, nh, nkv, hd, sc)
+    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=0, atol=2.0 ** -9 * np.abs(ref).max())
