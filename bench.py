@@ -357,7 +357,17 @@ def main():
         torch.cuda.synchronize(dev)
         dtp.check()
         ems = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
+        # the device-to-host copy of one step's logits on its own: e2e is bound by
+        # max(forward pass, this copy), and the copy depends on the host's memory
+        c_start, c_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c_start.record(stream)
+        log_h[0].copy_(logits, non_blocking=True)
+        c_end.record(stream)
+        torch.cuda.synchronize(dev)
+        d2h_ms = c_start.elapsed_time(c_end)
         e2e = {"value": replica_throughput(world, cfg.T, args.steps, ems), "unit": UNIT,
+               "d2h_ms_per_step_alone": d2h_ms,
+               "d2h_gbs_alone": log_h[0].numel() * 4 / d2h_ms / 1e6,
                "h2d_bytes_per_step": int(tok_h[0].numel() * 4),
                "d2h_bytes_per_step": int(log_h[0].numel() * 4),
                "path": "dtp_fwd_prefill_host_batch: one prompt per step, pinned host tokens in, "
