@@ -124,11 +124,22 @@ __device__ __forceinline__ void acc_ld32(const Params& p, uint32_t tbase, uint32
     if constexpr (SC) {
         const int col = n0 + (int)(taddr - tbase);
         const float sa = grow < p.M ? p.ea.a_scale[grow] : 0.f;
+        float sb[32];
+        if (col + 32 <= p.N && (reinterpret_cast<uintptr_t>(p.ea.b_scale + col) & 15) == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float sb = col + j < p.N ? p.ea.b_scale[col + j] : 0.f;
-            r[j] = __float_as_uint(f32(r[j]) * (sa * sb));
+            for (int j = 0; j < 32; j += 4) {      // the same 32 scales in every lane
+                const float4 v = *reinterpret_cast<const float4*>(p.ea.b_scale + col + j);
+                sb[j] = v.x;
+                sb[j + 1] = v.y;
+                sb[j + 2] = v.z;
+                sb[j + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sb[j] = col + j < p.N ? p.ea.b_scale[col + j] : 0.f;
         }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(f32(r[j]) * (sa * sb[j]));
     }
 }
 

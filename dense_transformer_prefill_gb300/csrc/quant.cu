@@ -97,14 +97,31 @@ __global__ void rmsnorm_e4m3_kernel(const float* __restrict__ x, const float* __
 }
 
 // One block per row of bf16 x [rows, ldx]: cols % 8 == 0, 16-byte aligned rows.
+// Rows of up to 8 * 8 * blockDim elements are read once and held in registers
+// (8 16-byte chunks per thread); longer rows are read a second time.
 __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int ldx, int cols,
                                   uint8_t* __restrict__ q, float* __restrict__ scale) {
     __shared__ float red[32];
     const size_t r = blockIdx.x;
     const uint4* xr = reinterpret_cast<const uint4*>(x + r * ldx);
     const int n8 = cols >> 3;
+    constexpr int KEEP = 8;
+    uint4 held[KEEP];
     float amax = 0.f;
-    for (int c8 = threadIdx.x; c8 < n8; c8 += blockDim.x) {
+#pragma unroll
+    for (int i = 0; i < KEEP; ++i) {
+        const int c8 = threadIdx.x + i * blockDim.x;
+        if (c8 < n8) {
+            held[i] = xr[c8];
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&held[i]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __bfloat1622float2(h[j]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+    }
+    for (int c8 = threadIdx.x + KEEP * blockDim.x; c8 < n8; c8 += blockDim.x) {
         const uint4 u = xr[c8];
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
@@ -117,13 +134,18 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int ldx, 
     float inv, s;
     row_scale(amax, inv, s);
     uint2* qr = reinterpret_cast<uint2*>(q + r * cols);
-    for (int c8 = threadIdx.x; c8 < n8; c8 += blockDim.x) {
-        const uint4 u = xr[c8];
+    auto put = [&](int c8, const uint4& u) {
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
         const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]),
                      c = __bfloat1622float2(h[2]), d = __bfloat1622float2(h[3]);
         qr[c8] = make_uint2(pack4(a.x, a.y, b.x, b.y, inv), pack4(c.x, c.y, d.x, d.y, inv));
+    };
+#pragma unroll
+    for (int i = 0; i < KEEP; ++i) {
+        const int c8 = threadIdx.x + i * blockDim.x;
+        if (c8 < n8) put(c8, held[i]);
     }
+    for (int c8 = threadIdx.x + KEEP * blockDim.x; c8 < n8; c8 += blockDim.x) put(c8, xr[c8]);
     if (threadIdx.x == 0) scale[r] = s;
 }
 
