@@ -267,8 +267,9 @@ def test_varlen_packed_sequences(dtp, prec):
         assert rel_l2(k0, kv[0][0]) <= {"f32": 1e-5, "tf32": 2.0 ** -11, "bf16": 2.0 ** -8}[prec]
 
 
-def test_varlen_single_sequence_matches_plain_forward(dtp):
-    cfg = synth.CONFIGS["small"].replace(n_layer=2)
+@pytest.mark.parametrize("prec", ["bf16", "e4m3"])
+def test_varlen_single_sequence_matches_plain_forward(dtp, prec):
+    cfg = synth.CONFIGS["small"].replace(n_layer=2, precision=prec)
     m = load_model(dtp, cfg)
     tt = torch.as_tensor(synth.tokens(cfg).astype(np.int32), device=dev)
     plain = m.forward(tt)
