@@ -202,6 +202,7 @@ struct Workspace {
     size_t q, k, vt, rope, gate;                 // bf16 path
     long long ldvt;
     size_t q8, s8;                               // e4m3 GEMM operand + row scales
+    size_t ssp;                                  // bf16: fused RMSNorm partial sums [tiles][T]
     size_t tokens, logits, logits2;              // _host staging (logits2: batch ping-pong)
     size_t tile_start, vcol_start, last_row, tok_pos, tok_vcol;   // packed sequences
     size_t total;
@@ -238,6 +239,8 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_s
         if (e4) {       // one operand buffer, reused by each GEMM in turn
             W.q8 = take((size_t)T * std::max(std::max(d, nq), F));
             W.s8 = take(align_up((size_t)T, 128) * 4);
+        } else {        // one partial per 128 columns at most (the narrowest tile)
+            W.ssp = take(((d + 127) / 128) * (size_t)T * 4);
         }
     } else {
         W.qkv = take((size_t)T * (nq * (1 + c->attn_gate) + 2 * nk) * 4);
@@ -503,13 +506,36 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
     }
     // row t of the table holds position p0 + t
     DTP_CUDA_CHECK(launch_rope_table(rope, T, c->rope_dim_count, c->rope_freq_base, s, S.p0));
-    DTP_CUDA_CHECK(launch_embed(tokens, T, c->n_vocab, d, P + L.tok_embd, DTP_BF16, x, s));
+    // bf16: the RMSNorm before the QKV and gate/up GEMMs is fused (GemmEpiArgs,
+    // "RMSNorm fused across GEMMs"): whoever writes x -- the embedding, the O and
+    // down epilogues -- also writes hb = bf16(x) and per-tile row sums of x^2 into
+    // ssp; the next GEMM multiplies its rows by 1/rms, the norm weight being folded
+    // into its packed matrix.  e4m3 mode keeps the RMSNorm kernel (its codes need
+    // the normalised row's max).
+    const bool fused = !e4;
+    float* ssp = fused ? (float*)(ws + W.ssp) : nullptr;
+    int n_ss = 1;                                    // partials per row in ssp
+    auto norm_args = [&](GemmEpiArgs& a) {
+        a.ss_in = ssp;
+        a.n_ss = n_ss;
+        a.ld_ss = T;
+        a.norm_cols = d;
+        a.norm_eps = c->rms_eps;
+    };
+    auto norm_out = [&](GemmEpiArgs& a) {
+        a.xb = hb;
+        a.ss_out = ssp;
+        a.ld_ss = T;
+    };
+    DTP_CUDA_CHECK(launch_embed(tokens, T, c->n_vocab, d, P + L.tok_embd, DTP_BF16, x, s,
+                                fused ? hb : nullptr, ssp));
     for (int l = 0; l < c->n_layer; ++l) {
         const uint8_t* lp = P + (size_t)l * L.layer_bytes;
         if (hidden)
             DTP_CUDA_CHECK(launch_copy_f32(x, hidden + (size_t)l * T * d, (size_t)T * d, s));
-        DTP_CUDA_CHECK(norm(x, (const float*)(lp + L.attn_norm), T, nullptr));
+        if (!fused) DTP_CUDA_CHECK(norm(x, (const float*)(lp + L.attn_norm), T, nullptr));
         GemmEpiArgs e;
+        if (fused) norm_args(e);
         // with a KV cache the keys are written straight into it (attention reads them
         // there); a chunk writes its keys and values into the state at position p0
         bf* kl = o.k_cache ? (bf*)o.k_cache + (size_t)l * T * nk : k;
@@ -548,17 +574,21 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         eo.y_dtype = DTP_F32;
         eo.ldy = d;
         eo.residual = x;
+        if (fused) norm_out(eo);
         if (e4) DTP_CUDA_CHECK(launch_quant_rows_e4m3(attn, nq, T, nq, q8, s8, s));
         DTP_CUDA_CHECK(gemm(attn, lp + L.wo, (const float*)(lp + L.wo_s), T, d, nq, EPI_STORE, eo,
                             DTP_K_GEMM_O));
-        DTP_CUDA_CHECK(norm(x, (const float*)(lp + L.ffn_norm), T, nullptr));
+        n_ss = gemm_tc_tiles_n(T, d);
+        if (!fused) DTP_CUDA_CHECK(norm(x, (const float*)(lp + L.ffn_norm), T, nullptr));
         GemmEpiArgs eg;
         eg.act = act;
+        if (fused) norm_args(eg);
         DTP_CUDA_CHECK(gemm(hb, lp + L.w_gu, (const float*)(lp + L.w_gu_s), T, 2 * F, d, EPI_SWIGLU,
                             eg, DTP_K_GEMM_GATEUP));
         if (e4) DTP_CUDA_CHECK(launch_quant_rows_e4m3(act, F, T, F, q8, s8, s));
         DTP_CUDA_CHECK(gemm(act, lp + L.w_down, (const float*)(lp + L.w_down_s), T, d, F, EPI_STORE,
                             eo, DTP_K_GEMM_DOWN));
+        n_ss = gemm_tc_tiles_n(T, d);
     }
     if (hidden)
         DTP_CUDA_CHECK(
@@ -640,13 +670,19 @@ int dtp_pack_layer(const dtp_config* cfg, int layer, const dtp_layer_src* src, v
         DTP_CUDA_CHECK(launch_pack_e4m3(src->w_down, d, F, lp + L.w_down,
                                         (float*)(lp + L.w_down_s), 0, s));
     } else {
-    DTP_CUDA_CHECK(launch_pack_matrix(src->wq, nqc, d, lp + L.w_qkv, bf, 0, s));
-    DTP_CUDA_CHECK(launch_pack_matrix(src->wk, nk, d, lp + L.w_qkv + (size_t)nqc * d * L.elt, bf, 0, s));
+    // bf16: the RMSNorm that precedes the QKV and gate/up GEMMs is fused into them
+    // (its weight multiplies the matrix's columns here, its 1/rms scales the
+    // GEMM's rows in the epilogue)
+    const float* an = bf == DTP_BF16 ? src->attn_norm : nullptr;
+    const float* fn = bf == DTP_BF16 ? src->ffn_norm : nullptr;
+    DTP_CUDA_CHECK(launch_pack_matrix(src->wq, nqc, d, lp + L.w_qkv, bf, 0, s, an));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->wk, nk, d, lp + L.w_qkv + (size_t)nqc * d * L.elt, bf, 0,
+                                      s, an));
     DTP_CUDA_CHECK(launch_pack_matrix(src->wv, nk, d, lp + L.w_qkv + (size_t)(nqc + nk) * d * L.elt,
-                                      bf, 0, s));
+                                      bf, 0, s, an));
     DTP_CUDA_CHECK(launch_pack_matrix(src->wo, d, nq, lp + L.wo, bf, 0, s));
-    DTP_CUDA_CHECK(launch_pack_matrix(src->w_gate, F, d, lp + L.w_gu, bf, 1, s));
-    DTP_CUDA_CHECK(launch_pack_matrix(src->w_up, F, d, lp + L.w_gu, bf, 2, s));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->w_gate, F, d, lp + L.w_gu, bf, 1, s, fn));
+    DTP_CUDA_CHECK(launch_pack_matrix(src->w_up, F, d, lp + L.w_gu, bf, 2, s, fn));
     DTP_CUDA_CHECK(launch_pack_matrix(src->w_down, d, F, lp + L.w_down, bf, 0, s));
     }
     DTP_CUDA_CHECK(launch_pack_matrix(src->attn_norm, 1, d, lp + L.attn_norm, 0, 0, s));

@@ -119,11 +119,14 @@ __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 // when the operands carry scales (SC: OP_E4M3).  Whole warp.
 template <bool SC>
 __device__ __forceinline__ void acc_ld32(const Params& p, uint32_t tbase, uint32_t taddr, int grow,
-                                         int n0, uint32_t (&r)[32]) {
+                                         int n0, uint32_t (&r)[32], float rowmul = 1.f) {
     ptx::tmem_ld32(taddr, r);
-    if constexpr (SC) {
+    if constexpr (!SC) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(f32(r[j]) * rowmul);
+    } else {
         const int col = n0 + (int)(taddr - tbase);
-        const float sa = grow < p.M ? p.ea.a_scale[grow] : 0.f;
+        const float sa = (grow < p.M ? p.ea.a_scale[grow] : 0.f) * rowmul;
         float sb[32];
         if (col + 32 <= p.N && (reinterpret_cast<uintptr_t>(p.ea.b_scale + col) & 15) == 0) {
 #pragma unroll
@@ -163,10 +166,20 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// The fused RMSNorm's row scale 1 / sqrt(mean(x^2) + eps) from the producer's
+// per-tile partial sums (summed in tile order), or 1 when the GEMM has none.
+__device__ __forceinline__ float row_rstd(const GemmEpiArgs& ea, int grow, int M) {
+    if (!ea.ss_in || grow >= M) return 1.f;
+    float ss = 0.f;
+    for (int t = 0; t < ea.n_ss; ++t) ss += ea.ss_in[(size_t)t * ea.ld_ss + grow];
+    return 1.0f / sqrtf(ss / (float)ea.norm_cols + ea.norm_eps);
+}
+
 // ----------------------------------------------------------------------------- epilogues
 template <int BN, bool SC>
 __device__ __forceinline__ void epi_store(const Params& p, uint32_t tbase, int grow, int n0) {
     const GemmEpiArgs& ea = p.ea;
+    float ss = 0.f;                                  // fused RMSNorm: this tile's sum of y^2
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
@@ -191,6 +204,11 @@ __device__ __forceinline__ void epi_store(const Params& p, uint32_t tbase, int g
                 store_row32(reinterpret_cast<float*>(ea.y) + off, v);
             else
                 store_row32(reinterpret_cast<__nv_bfloat16*>(ea.y) + off, v);
+            if (ea.xb) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+                store_row32(ea.xb + off, v);
+            }
         } else {
             for (int j = 0; j < 32 && col0 + j < p.N; ++j) {
                 float x = v[j];
@@ -199,9 +217,14 @@ __device__ __forceinline__ void epi_store(const Params& p, uint32_t tbase, int g
                     reinterpret_cast<float*>(ea.y)[off + j] = x;
                 else
                     reinterpret_cast<__nv_bfloat16*>(ea.y)[off + j] = __float2bfloat16_rn(x);
+                if (ea.xb) {
+                    ss = fmaf(x, x, ss);
+                    ea.xb[off + j] = __float2bfloat16_rn(x);
+                }
             }
         }
     }
+    if (ea.ss_out && grow < p.M) ea.ss_out[(size_t)(n0 / BN) * ea.ld_ss + grow] = ss;
 }
 
 // q/k heads: RMSNorm over head_dim with q_norm/k_norm, then NeoX RoPE from the
@@ -209,6 +232,7 @@ __device__ __forceinline__ void epi_store(const Params& p, uint32_t tbase, int g
 template <int BN, bool SC>
 __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int grow, int n0) {
     const GemmEpiArgs& ea = p.ea;
+    const float rsc = row_rstd(ea, grow, p.M);     // fused RMSNorm row scale (or 1)
     const int hd = ea.head_dim, half = ea.rope_dims / 2;
     const int nq = ea.n_head * hd, nk = ea.n_head_kv * hd;
     const bool live = grow < p.M;
@@ -225,7 +249,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
                 if (live) {
                     float y[32];
 #pragma unroll
@@ -244,7 +268,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ss = fmaf(f32(r[j]), f32(r[j]), ss);
             }
@@ -255,8 +279,8 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int i0 = 0; i0 < half; i0 += 32) {
                 uint32_t ra[32], rb[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + i0, grow, n0, ra);
-                acc_ld32<SC>(p, tbase, th + half + i0, grow, n0, rb);
+                acc_ld32<SC>(p, tbase, th + i0, grow, n0, ra, rsc);
+                acc_ld32<SC>(p, tbase, th + half + i0, grow, n0, rb, rsc);
                 if (live) {
                     const int pos = ea.tok_pos ? ea.tok_pos[grow] : grow;
                     const float2* cs = ea.rope + (size_t)pos * half + i0;
@@ -277,7 +301,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int c = ea.rope_dims; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
                 if (live) {
                     float y[32];
 #pragma unroll
@@ -291,7 +315,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
                 if (live) {
                     const int tcol = ea.tok_vcol ? ea.tok_vcol[grow] : grow;
                     __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
@@ -315,6 +339,7 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
 template <int BN, bool SC>
 __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, int grow, int n0) {
     const GemmEpiArgs& ea = p.ea;
+    const float rsc = row_rstd(ea, grow, p.M);     // fused RMSNorm row scale (or 1)
     const int F = p.N / 2;
 #pragma unroll 1
     for (int b = 0; b < BN; b += 128) {
@@ -325,8 +350,8 @@ __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, int 
         for (int c = 0; c < 64; c += 32) {
             uint32_t rg[32], ru[32];
             __syncwarp();
-            acc_ld32<SC>(p, tbase, tbase + b + c, grow, n0, rg);
-            acc_ld32<SC>(p, tbase, tbase + b + 64 + c, grow, n0, ru);
+            acc_ld32<SC>(p, tbase, tbase + b + c, grow, n0, rg, rsc);
+            acc_ld32<SC>(p, tbase, tbase + b + 64 + c, grow, n0, ru, rsc);
             if (grow < p.M) {
                 float a[32];
 #pragma unroll
@@ -386,6 +411,7 @@ __device__ __forceinline__ bool epi_store_tma(const Params& p, EpiStage& st, uin
     const bool resid = ea.residual != nullptr;
     const int CW = f32out ? 32 : 64;
     const int grow = st.row0 + st.lane;
+    float ss = 0.f;                                  // fused RMSNorm: this tile's sum of y^2
 #pragma unroll 1
     for (int c = 0; c < BN; c += CW) {
         const int col0 = n0 + c;
@@ -431,6 +457,20 @@ __device__ __forceinline__ bool epi_store_tma(const Params& p, EpiStage& st, uin
                 stage_put16(st.buf[b], st.lane, j,
                             make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
                                        __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3])));
+            if (ea.xb && grow < p.M) {
+                float vv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    vv[j] = v[j];
+                    ss = col0 + j < p.N ? fmaf(v[j], v[j], ss) : ss;
+                }
+                if (col0 + 32 <= p.N) {
+                    store_row32(ea.xb + (size_t)grow * ea.ldy + col0, vv);
+                } else {
+                    for (int j = 0; j < 32 && col0 + j < p.N; ++j)
+                        ea.xb[(size_t)grow * ea.ldy + col0 + j] = __float2bfloat16_rn(vv[j]);
+                }
+            }
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) stage_put16(st.buf[b], st.lane, j, pack8_bf16(v + 8 * j));
@@ -438,6 +478,7 @@ __device__ __forceinline__ bool epi_store_tma(const Params& p, EpiStage& st, uin
         stage_flush(st, b, tmY, col0);
         ++st.cnt;
     }
+    if (ea.ss_out && grow < p.M) ea.ss_out[(size_t)(n0 / BN) * ea.ld_ss + grow] = ss;
     return true;
 }
 
@@ -446,6 +487,7 @@ template <int BN, bool SC>
 __device__ __forceinline__ void epi_swiglu_tma(const Params& p, EpiStage& st, uint32_t tbase,
                                                int n0, const CUtensorMap* tmY) {
     const int grow = st.row0 + st.lane;
+    const float rsc = row_rstd(p.ea, grow, p.M);   // fused RMSNorm row scale (or 1)
 #pragma unroll 1
     for (int b = 0; b < BN; b += 128) {
         const int colblk = n0 + b;
@@ -456,8 +498,8 @@ __device__ __forceinline__ void epi_swiglu_tma(const Params& p, EpiStage& st, ui
         for (int c = 0; c < 64; c += 32) {
             uint32_t rg[32], ru[32];
             __syncwarp();
-            acc_ld32<SC>(p, tbase, tbase + b + c, grow, n0, rg);
-            acc_ld32<SC>(p, tbase, tbase + b + 64 + c, grow, n0, ru);
+            acc_ld32<SC>(p, tbase, tbase + b + c, grow, n0, rg, rsc);
+            acc_ld32<SC>(p, tbase, tbase + b + 64 + c, grow, n0, ru, rsc);
             float a[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] = silu_f(f32(rg[j])) * f32(ru[j]);
@@ -476,6 +518,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
                                             int grow, int n0, const CUtensorMap* tmQ,
                                             const CUtensorMap* tmK) {
     const GemmEpiArgs& ea = p.ea;
+    const float rsc = row_rstd(ea, grow, p.M);     // fused RMSNorm row scale (or 1)
     const int hd = ea.head_dim, half = ea.rope_dims / 2;
     const int nq = ea.n_head * hd, nk = ea.n_head_kv * hd;
     const bool live = grow < p.M;
@@ -491,7 +534,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
                 if (live) {
                     float y[32];
 #pragma unroll
@@ -510,7 +553,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ss = fmaf(f32(r[j]), f32(r[j]), ss);
             }
@@ -523,8 +566,8 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int i0 = 0; i0 < half; i0 += 32) {
                 uint32_t ra[32], rb[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + i0, grow, n0, ra);
-                acc_ld32<SC>(p, tbase, th + half + i0, grow, n0, rb);
+                acc_ld32<SC>(p, tbase, th + i0, grow, n0, ra, rsc);
+                acc_ld32<SC>(p, tbase, th + half + i0, grow, n0, rb, rsc);
                 const float2* cs = ea.rope + (size_t)(live ? pos : 0) * half + i0;
                 float ya[32], yb[32];
 #pragma unroll
@@ -546,7 +589,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int c = ea.rope_dims; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
                 float y[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) y[j] = f32(r[j]) * rstd * w[c + j];
@@ -567,7 +610,7 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
             for (int c = 0; c < hd; c += 32) {
                 uint32_t r[32];
                 __syncwarp();
-                acc_ld32<SC>(p, tbase, th + c, grow, n0, r);
+                acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
                 if (live) {
                     const int tcol = ea.tok_vcol ? ea.tok_vcol[grow] : grow;
                     __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
@@ -914,6 +957,11 @@ static cudaError_t launch_gemm(const void* x, const void* W, int opk, int M, int
     }
     if (BN == 224) return launch_impl<224, EPI_STORE>(ta, tb, ty, ty2, tr, p, s);
     return launch_impl<128, EPI_STORE>(ta, tb, ty, ty2, tr, p, s);
+}
+
+int gemm_tc_tiles_n(int M, int N) {
+    const int bn = pick_bn(M, N, EPI_STORE, DTP_F32);
+    return (N + bn - 1) / bn;
 }
 
 cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,

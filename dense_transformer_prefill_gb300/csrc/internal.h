@@ -52,7 +52,8 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
 
 // ----------------------------------------------------------------------------- SIMT kernels
 cudaError_t launch_embed(const uint32_t* tokens, int T, int V, int d, const void* table,
-                         int table_dtype, float* x, cudaStream_t s);
+                         int table_dtype, float* x, cudaStream_t s, __nv_bfloat16* xb = nullptr,
+                         float* ss_out = nullptr);
 cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype, int rows,
                            int cols, float eps, cudaStream_t s, const int* row_idx = nullptr);
 cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
@@ -105,7 +106,7 @@ cudaError_t launch_transpose_v(const __nv_bfloat16* v, __nv_bfloat16* vt, int T,
                                int ldt, cudaStream_t s);
 // to_dtype: DTP_F32, DTP_BF16 or DTP_TF32 (float32 rounded to tf32)
 cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_dtype,
-                               int mode, cudaStream_t s);
+                               int mode, cudaStream_t s, const float* col_scale = nullptr);
 cudaError_t launch_copy_f32(const float* src, float* dst, size_t n, cudaStream_t s);
 // dst[r, 0:cols] = src[r, 0:cols] for r < rows (float32, row strides lds / ldd)
 cudaError_t launch_copy_rows_f32(const float* src, int lds, float* dst, int ldd, int rows,
@@ -144,7 +145,20 @@ struct GemmEpiArgs {
     float eps = 0.f;
     // EPI_SWIGLU
     __nv_bfloat16* act = nullptr;       // [M, N/2]
+    // RMSNorm fused across GEMMs (bf16 path).  Producer (EPI_STORE, f32 y): also
+    // writes xb = bf16(y) and, per row, the sum of y^2 over each BN-wide tile into
+    // ss_out[tile_n * ld_ss + row].  Consumer (EPI_QKV / EPI_SWIGLU, A = xb, the
+    // weights pre-multiplied by the norm weights): every row is scaled by
+    // 1 / sqrt(sum_t ss_in[t * ld_ss + row] / norm_cols + norm_eps) first.
+    __nv_bfloat16* xb = nullptr;
+    float* ss_out = nullptr;
+    const float* ss_in = nullptr;
+    int n_ss = 0, ld_ss = 0, norm_cols = 0;
+    float norm_eps = 0.f;
 };
+// N-tiles of one row that launch_gemm_tc's EPI_STORE with float32 output uses
+// (the number of ss_out partials it writes per row).
+int gemm_tc_tiles_n(int M, int N);
 
 // y-side work of one GEMM: x [M, K] bf16 (row stride K), W [N, K] bf16.
 cudaError_t launch_gemm_tc(const __nv_bfloat16* x, const __nv_bfloat16* W, int M, int N, int K,

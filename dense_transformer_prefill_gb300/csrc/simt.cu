@@ -69,30 +69,44 @@ __device__ float block_sum(float v, float* red) {
 // ----------------------------------------------------------------------------- embedding
 // forward.rs: `x = self.embed_tokens(e, tokens)` -- row t of x is row tokens[t]
 // of the embedding table.  An id >= V raises the token-range error bit and
-// leaves a zero row.
+// leaves a zero row.  With xb, also the bf16 copy of the row and its sum of
+// squares ss[t] (the first layer's fused RMSNorm input, one partial per row).
 template <typename Tt>
 __global__ void embed_kernel(const uint32_t* __restrict__ tokens, int V, int d,
-                             const Tt* __restrict__ table, float* __restrict__ x) {
+                             const Tt* __restrict__ table, float* __restrict__ x,
+                             __nv_bfloat16* __restrict__ xb, float* __restrict__ ss_out) {
+    __shared__ float red[32];
     const int t = blockIdx.x;
     const uint32_t id = tokens[t];
     float* xr = x + (size_t)t * d;
-    if (id >= (uint32_t)V) {
-        if (threadIdx.x == 0) atomicOr(&g_simt_err, ERRBIT_TOKEN_RANGE);
-        for (int c = threadIdx.x; c < d; c += blockDim.x) xr[c] = 0.f;
-        return;
+    const bool bad = id >= (uint32_t)V;
+    if (bad && threadIdx.x == 0) atomicOr(&g_simt_err, ERRBIT_TOKEN_RANGE);
+    const Tt* src = table + (size_t)(bad ? 0 : id) * d;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+        const float v = bad ? 0.f : ld_elt(src, c);
+        xr[c] = v;
+        if (xb) {
+            xb[(size_t)t * d + c] = __float2bfloat16_rn(v);
+            ss = fmaf(v, v, ss);
+        }
     }
-    const Tt* src = table + (size_t)id * d;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) xr[c] = ld_elt(src, c);
+    if (ss_out) {
+        ss = block_sum(ss, red);
+        if (threadIdx.x == 0) ss_out[t] = ss;
+    }
 }
 
 cudaError_t launch_embed(const uint32_t* tokens, int T, int V, int d, const void* table,
-                         int table_dtype, float* x, cudaStream_t s) {
+                         int table_dtype, float* x, cudaStream_t s, __nv_bfloat16* xb,
+                         float* ss_out) {
     LaunchScope ls(DTP_K_EMBED, s);
     int threads = d >= 256 ? 256 : 64;
     if (table_dtype == DTP_BF16)
-        embed_kernel<<<T, threads, 0, s>>>(tokens, V, d, (const __nv_bfloat16*)table, x);
+        embed_kernel<<<T, threads, 0, s>>>(tokens, V, d, (const __nv_bfloat16*)table, x, xb,
+                                           ss_out);
     else
-        embed_kernel<<<T, threads, 0, s>>>(tokens, V, d, (const float*)table, x);
+        embed_kernel<<<T, threads, 0, s>>>(tokens, V, d, (const float*)table, x, xb, ss_out);
     return cudaGetLastError();
 }
 
@@ -601,9 +615,12 @@ cudaError_t launch_round_tf32_rows(float* x, int ld, int rows, int cols, cudaStr
 // ----------------------------------------------------------------------------- packing
 // dst row for source row r: mode 0 -> r; mode 1 (gate) -> 128*(r/64) + r%64;
 // mode 2 (up) -> 128*(r/64) + 64 + r%64.
+// col_scale (optional, [cols]): dst = src * col_scale[c], rounded once (a norm
+// weight folded into the matrix that follows the norm).
 template <typename To>
 __global__ void pack_matrix_kernel(const float* __restrict__ src, int rows, int cols,
-                                   To* __restrict__ dst, int mode) {
+                                   To* __restrict__ dst, int mode,
+                                   const float* __restrict__ col_scale) {
     const size_t n = (size_t)rows * cols;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -611,22 +628,24 @@ __global__ void pack_matrix_kernel(const float* __restrict__ src, int rows, int 
         int dr = r;
         if (mode == 1) dr = 128 * (r / 64) + (r % 64);
         if (mode == 2) dr = 128 * (r / 64) + 64 + (r % 64);
-        st_elt(dst, (size_t)dr * cols + c, src[i]);
+        st_elt(dst, (size_t)dr * cols + c, col_scale ? src[i] * col_scale[c] : src[i]);
     }
 }
 
 cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_dtype,
-                               int mode, cudaStream_t s) {
+                               int mode, cudaStream_t s, const float* col_scale) {
     LaunchScope ls(DTP_K_OTHER, s);
     size_t n = (size_t)rows * cols, blocks = (n + 255) / 256;
     if (blocks > 65535 * 16) blocks = 65535 * 16;
     if (to_dtype == DTP_BF16)
         pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (__nv_bfloat16*)dst,
-                                                            mode);
+                                                            mode, col_scale);
     else if (to_dtype == DTP_TF32)
-        pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (tf32_t*)dst, mode);
+        pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (tf32_t*)dst, mode,
+                                                            col_scale);
     else
-        pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (float*)dst, mode);
+        pack_matrix_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, (float*)dst, mode,
+                                                            col_scale);
     return cudaGetLastError();
 }
 

@@ -122,6 +122,9 @@ typedef struct dtp_layer_src {
  * and the lm_head [V, d].  Matrices are stored as bf16 (round to nearest even)
  * under DTP_PREC_BF16, float32 under DTP_PREC_F32, and float32 rounded to tf32
  * (nearest even) under DTP_PREC_TF32, except tok_embd, which stays float32.
+ * Under DTP_PREC_BF16 the RMSNorm before the QKV and gate/up projections is
+ * fused into them: Wq;Wk;Wv are stored multiplied column-wise by attn_norm and
+ * Wgate/Wup by ffn_norm (rounded once, after the product).
  * Under DTP_PREC_E4M3 the matrices are e4m3 codes, each followed by its float32
  * row scales, and tok_embd is bf16.  Norm vectors are float32.
  * ------------------------------------------------------------------------------------ */

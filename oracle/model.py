@@ -249,15 +249,27 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     d, h, g, hd = cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim
     eps = cfg.rms_eps
     scale = 1.0 / np.sqrt(F64(hd))
+
+    def normed_linears(xin, w_norm, names):
+        """rms_norm(xin) * w_norm followed by each matrix.  In bf16-operand mode
+        the norm is fused the way the bf16 kernels compute it: the matrix input is
+        bf16(xin), the norm weight multiplies the matrix's columns before its bf16
+        rounding, and the row's 1/rms scales the product -- the same function of
+        xin, with those rounding points."""
+        if bf16_operands:
+            r = 1.0 / np.sqrt(np.mean(np.asarray(xin, F64) ** 2, axis=1) + eps)
+            a = round_bf16(xin)
+            wn = np.asarray(w_norm, F64)[None, :]
+            return [r[:, None] * linear(a, round_bf16(np.asarray(lw[n], F64) * wn)) for n in names]
+        hn = op(rms_norm(xin, w_norm, eps))
+        return [linear(hn, L[n]) for n in names]
+
     # attention block
-    hN = op(rms_norm(x, L["attn_norm"], eps))
-    q = linear(hN, L["wq"])
+    q, k, v = normed_linears(x, lw["attn_norm"], ("wq", "wk", "wv"))
     gate = None
     if getattr(cfg, "attn_gate", False):
         qg = q.reshape(q.shape[0], h, 2, hd)
         q, gate = qg[:, :, 0, :].reshape(-1, h * hd), opg(qg[:, :, 1, :].reshape(-1, h * hd))
-    k = linear(hN, L["wk"])
-    v = linear(hN, L["wv"])
     q = qk_norm(q, L["q_norm"], hd, eps)
     k = qk_norm(k, L["k_norm"], hd, eps)
     q = opa(rope_neox(q, pos, h, hd, cfg.rope_dim_count, cfg.rope_freq_base))
@@ -276,8 +288,8 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
     attn = opm(attn)
     x1 = x + linear(attn, L["wo"])
     # ffn block (dense SwiGLU)
-    z = op(rms_norm(x1, L["ffn_norm"], eps))
-    act = opm(swiglu(linear(z, L["w_gate"]), linear(z, L["w_up"])))
+    gt, up = normed_linears(x1, lw["ffn_norm"], ("w_gate", "w_up"))
+    act = opm(swiglu(gt, up))
     return x1 + linear(act, L["w_down"])
 
 
