@@ -85,7 +85,8 @@ def test_rms_norm_e4m3_is_the_quantised_rms_norm(dtp, rows, cols):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 16), (128, 256, 128), (130, 200, 144), (300, 1000, 272),
-                                   (513, 2048, 1024), (64, 384, 4096), (77, 1001, 144)])
+                                   (513, 2048, 1024), (64, 384, 4096), (77, 1001, 144),
+                                   (1152, 5000, 256)])   # odd M blocks, ragged N, more tiles than SMs
 @pytest.mark.parametrize("resid", [False, True])
 def test_linear_e4m3_tensor_core(dtp, M, N, K, resid):
     x = synth.normal(15, 1500, (M, K))

@@ -157,6 +157,36 @@ def test_linear_bf16_long_k_and_many_tiles(dtp):
     np.testing.assert_allclose(y.cpu().numpy()[rows], ref, rtol=0, atol=tol)
 
 
+@pytest.mark.parametrize("M,N", [(1024, 5120), (1024, 5000), (1152, 4900), (1, 4096)])
+@pytest.mark.parametrize("mode", ["f32", "bf16", "resid"])
+def test_linear_bf16_cluster_pairs(dtp, M, N, mode):
+    """The GEMM runs as CTA pairs on M-adjacent tiles, each CTA loading half of
+    the shared weight box for both.  More tiles than SMs, a ragged last N block
+    (N = 5000, 4900), an odd number of M blocks (1152 = 9 x 128: the last pair's
+    second tile lies wholly past M) and a single row."""
+    K = 512
+    x = bf16_round32(synth.normal(16, 1600, (M, K)))
+    W = bf16_round32(synth.normal(16, 1601, (N, K), std=0.05))
+    xt, Wt = t32(x).bfloat16(), t32(W).bfloat16()
+    ref = oracle.linear(x, W)
+    if mode == "bf16":
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        dtp.linear(xt, Wt, y)
+        torch.cuda.synchronize()
+        dtp.check()
+        np.testing.assert_allclose(y.float().cpu().numpy(), ref, rtol=2 ** -8,
+                                   atol=1e-5 * np.abs(ref).max())
+        return
+    r = synth.normal(16, 1602, (M, N)) if mode == "resid" else None
+    y = t32(r) if r is not None else torch.full((M, N), float("nan"), device=dev)
+    dtp.linear(xt, Wt, y, residual=y if r is not None else None)
+    torch.cuda.synchronize()
+    dtp.check()
+    if r is not None:
+        ref = ref + r
+    np.testing.assert_allclose(y.cpu().numpy(), ref, rtol=0, atol=1e-5 * np.abs(ref).max())
+
+
 # ----------------------------------------------------------------------------- attention
 @pytest.mark.parametrize("T,nh,nkv,hd", [(1, 4, 2, 16), (17, 4, 2, 64), (130, 8, 4, 64), (300, 4, 1, 128)])
 def test_sdpa_f32(dtp, T, nh, nkv, hd):
@@ -267,7 +297,9 @@ def test_attention_sweep(dtp, T, r):
 
 # ----------------------------------------------------------------------------- fused epilogues
 @pytest.mark.parametrize("T,d,nh,nkv,hd,r", [(1, 64, 2, 1, 64, 64), (130, 512, 8, 4, 64, 64),
-                                              (300, 1024, 4, 2, 128, 64), (257, 512, 8, 2, 128, 128)])
+                                              (300, 1024, 4, 2, 128, 64), (257, 512, 8, 2, 128, 128),
+                                              # more tiles than SMs (8 x 24, 32 x 6)
+                                              (1024, 512, 32, 8, 128, 128), (4096, 256, 16, 4, 64, 64)])
 def test_qkv_norm_rope_fused(dtp, T, d, nh, nkv, hd, r):
     """QKV GEMM with per-head RMSNorm + NeoX RoPE in its epilogue, against the oracle
     on the same bf16 operands; outputs agree to one bf16 rounding."""
@@ -295,7 +327,8 @@ def test_qkv_norm_rope_fused(dtp, T, d, nh, nkv, hd, r):
     assert not vt[:, T:].any()                       # padding columns untouched
 
 
-@pytest.mark.parametrize("T,d,F", [(1, 64, 64), (200, 512, 1536), (513, 1024, 3072)])
+@pytest.mark.parametrize("T,d,F", [(1, 64, 64), (200, 512, 1536), (513, 1024, 3072),
+                                   (1024, 256, 2560)])   # 8 x 20 tiles: more than SMs
 def test_gate_up_swiglu_fused(dtp, T, d, F):
     """gate/up GEMM with SwiGLU in its epilogue on the interleaved weight layout."""
     z = bf16_round32(synth.normal(14, 1400, (T, d)))

@@ -45,7 +45,8 @@ def test_rms_norm_tf32_output_is_rounded_f32_output(dtp):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 32), (128, 256, 64), (130, 200, 72), (300, 1000, 136),
-                                   (513, 2048, 1024), (64, 384, 4096), (77, 1001, 132)])
+                                   (513, 2048, 1024), (64, 384, 4096), (77, 1001, 132),
+                                   (1152, 5000, 256)])   # odd M blocks, ragged N, more tiles than SMs
 @pytest.mark.parametrize("resid", [False, True])
 def test_linear_tf32_tensor_core(dtp, M, N, K, resid):
     x = oracle.round_tf32(synth.normal(12, 1200, (M, K))).astype(np.float32)
