@@ -13,16 +13,21 @@
 //   OP_E4M3  e4m3 with a float32 scale per A row and per B row (kind::f8f6f4):
 //            the epilogue reads s_a[m] * s_b[n] * acc[m, n]
 // A stage holds 128 bytes of K per row (64 bf16, 32 tf32, 128 e4m3).  One
-// persistent CTA per SM walks 128 x BN output tiles:
-//   warp 0      TMA producer: 128-row A and BN-row B boxes (128-byte swizzle) into
-//               a STAGES-deep shared-memory ring (mbarrier full/empty pairs)
-//   warp 1      one thread issues tcgen05.mma (M=128, N=BN, K=16) into a TMEM
-//               accumulator; two accumulators (2*BN columns) so the epilogue of
-//               tile i overlaps the main loop of tile i+1
-//   warps 2..5  epilogue: tcgen05.ld (TMEM lane = output row), fused math,
-//               global stores
-// The plain-store GEMMs run as clusters of two CTAs on M-adjacent tiles of the
-// same weight columns: each loads half of every B box and multicasts it to both.
+// persistent CTA per SM; the CTAs run in clusters of two, and a pair walks
+// 256 x BN output tiles (CTA rank r: rows 128r..128r+127 of the tile):
+//   warp 0      TMA producer: the CTA's 128-row A box and its BN/2-row half of
+//               the B box (128-byte swizzle) into a STAGES-deep shared-memory
+//               ring; both CTAs count their bytes on the even CTA's full
+//               barrier, and each waits on its own empty barrier
+//   warp 1      (even CTA) one thread issues tcgen05.mma.cta_group::2 (M=256,
+//               N=BN, K=16): A from both CTAs' rings, B split between them, D
+//               rows of each CTA in its own TMEM; two accumulators (2*BN
+//               columns) so the epilogue of tile i overlaps the main loop of
+//               tile i+1; its commits arrive on the barriers of both CTAs
+//   warps 2..5  epilogue (both CTAs): tcgen05.ld (TMEM lane = output row),
+//               fused math, global stores
+// A pair holds one B tile between two SMs, so a stage is 32 KB instead of 48
+// and the ring 6 deep instead of 4 (BN = 256).
 #include <math.h>
 #include <mutex>
 
@@ -64,22 +69,26 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
-// CTAs per cluster (M-adjacent tiles sharing B boxes).  Measured on the 8B
-// shapes: pairs make the O and down projections 3-5% faster and the QKV GEMM
-// 3% slower, and leave gate/up unchanged; so the plain stores run in pairs and
-// the fused QKV and SwiGLU epilogues alone.
-constexpr int cluster_for(int epi) { return epi == EPI_STORE ? 2 : 1; }
+// CTAs per cluster: every GEMM runs as CTA pairs with cta_group::2 MMAs
+// (kernel parameter CL = 2).  Against single CTAs (CL = 1) on the 8B forward,
+// alternated in one process: gate/up 16.5 vs 17.4 ms per step, down 9.7 vs
+// 10.0, QKV 5.2 vs 5.4, O 4.0 vs 4.2, lm_head 2.6 vs 3.0.
+constexpr int kCluster = 2;
 
-template <int BN>
+constexpr int kSmemLimit = 232448;   // dynamic shared memory one CTA may use (227 KB)
+
+// CL = 2: a CTA pair computes a 256 x BN tile with cta_group::2 MMAs; each CTA
+// holds its 128 A rows and half of the B rows, so a stage is smaller and the
+// ring deeper.
+template <int BN, int CL = 1>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = (BN / CL) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // The 224-wide tile keeps a fifth pipeline stage instead of the epilogue
-    // staging (the main loop is latency-bound: its depth matters more than store
-    // efficiency there) and stores directly from registers.
+    // The 224-wide tile gives the epilogue staging to the pipeline (the main
+    // loop is latency-bound: its depth matters more than store efficiency
+    // there) and stores directly from registers.
     static constexpr bool TMA_OUT = BN != 224;
-    static constexpr int STAGES = BN == 128 ? 6 : (BN == 224 ? 5 : 4);
     // two accumulators; the second starts at a 256-column boundary when BN > 128
     static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;
     static constexpr int TMEM_COLS = 2 * ACC_STRIDE;
@@ -87,7 +96,12 @@ struct Cfg {
     static constexpr int EPI_BUF = 4096;
     static constexpr int EPI_BYTES = TMA_OUT ? 4 * 2 * EPI_BUF : 0;
     static constexpr int BAR_BYTES = 256;
+    // as many stages as fit: 6 / 5 / 4 for BN = 128 / 224 / 256, 8 / 7 / 6 in pairs
+    static constexpr int STAGES_FIT = (kSmemLimit - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static_assert((2 * STAGES + 13) * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(SMEM_BYTES <= kSmemLimit, "shared memory");
 };
 
 struct Params {
@@ -639,17 +653,21 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
 // ----------------------------------------------------------------------------- kernel
 enum { OP_BF16 = 0, OP_TF32 = 1, OP_E4M3 = 2 };
 
-// CL = 2: the kernel runs in clusters of two CTAs that take M-adjacent tiles of
-// the same weight columns in lockstep.  Each CTA loads half of every B box
-// (BN/2 rows) and multicasts it to both, so the pair reads each weight tile
-// from L2 once; a stage is refilled only after both CTAs' MMAs released it
-// (the commits arrive on the empty barriers of both).
+// CL = 2: clusters of two CTAs compute 256 x BN tiles with cta_group::2 MMAs.
+// The even CTA (rank 0) takes M block 2j, the odd one 2j + 1, of the same N
+// block.  Each CTA's producer loads its 128 A rows and its half of the B rows
+// (rank r: rows r*BN/2 ..) into its own shared memory; both count their bytes
+// on the even CTA's full barrier.  The even CTA's MMA thread issues the pair
+// MMAs and commits to the empty and accumulator-full barriers of both CTAs.
+// Each CTA's epilogue reads its own TMEM rows; its warps release the
+// accumulator on the even CTA's accumulator-empty barrier.
 template <int BN, int EPI, int OPK = OP_BF16, int CL = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmY2,
                    const __grid_constant__ CUtensorMap tmR, const Params p) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, CL>;
+    static_assert(CL == 1 || CL == 2, "single CTAs or pairs");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -667,14 +685,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = CL > 1 ? ptx::cluster_ctarank() : 0u;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], CL);
+            ptx::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&tfull[b], 1);
-            ptx::mbar_init(&tempty[b], 128);
+            // single: every epilogue thread arrives; pairs: lane 0 of the 4
+            // epilogue warps of both CTAs
+            ptx::mbar_init(&tempty[b], CL == 1 ? 128 : 8);
         }
         ptx::mbar_init(drain, 1);
         for (int i = 0; i < 8; ++i) ptx::mbar_init(&rbars[i], 1);
@@ -682,8 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
     }
     if (warp == 0) {
-        ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (CL == 1) {
+            ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
+            ptx::tmem_relinquish();
+        } else {
+            ptx::tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        }
     }
     if (warp == 1 && lane == 0) {
         ptx::tma_prefetch_desc(&tmA);
@@ -701,7 +727,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    constexpr uint16_t kPeers = (1u << CL) - 1u;
     const int num_tiles = p.tiles_m * p.tiles_n;
 
     if (warp == 0) {
@@ -710,23 +735,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
-            const int crank = CL > 1 ? (int)ptx::cluster_ctarank() : 0;
+            // pairs: the even CTA's full barriers count both CTAs' bytes
+            const uint32_t full_cl = CL > 1 ? ptx::mapa(ptx::smem_u32(full), 0) : 0u;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 const int mb = tile % p.tiles_m, nb = tile / p.tiles_m;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!ptx::wait_bounded(&empty[stage], phase ^ 1, abort_flag, &g_gemm_err,
                                            ERRBIT_TIMEOUT))
                         goto producer_done;
-                    ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                     // a stage holds 128 bytes of K per row: 64 bf16, 32 tf32, 128 e4m3
                     const int k0 = kb * (OPK == OP_TF32 ? BK / 2 : OPK == OP_E4M3 ? 2 * BK : BK);
-                    ptx::tma_load_2d(&tmA, &full[stage], sA + stage * C::A_BYTES, k0, mb * BM);
-                    if constexpr (CL == 1)
+                    if constexpr (CL == 1) {
+                        ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        ptx::tma_load_2d(&tmA, &full[stage], sA + stage * C::A_BYTES, k0, mb * BM);
                         ptx::tma_load_2d(&tmB, &full[stage], sB + stage * C::B_BYTES, k0, nb * BN);
-                    else
-                        ptx::tma_load_2d_mc(&tmB, &full[stage],
-                                            sB + stage * C::B_BYTES + crank * (C::B_BYTES / CL), k0,
-                                            nb * BN + crank * (BN / CL), kPeers);
+                    } else {
+                        if (crank == 0) ptx::mbar_arrive_expect_tx(&full[stage], CL * C::STAGE_BYTES);
+                        const uint32_t fb = full_cl + stage * 8u;
+                        ptx::tma_load_2d_pair(&tmA, fb, sA + stage * C::A_BYTES, k0, mb * BM);
+                        ptx::tma_load_2d_pair(&tmB, fb, sB + stage * C::B_BYTES, k0,
+                                              nb * BN + (int)crank * (BN / CL));
+                    }
                     ++issued;
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -735,8 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if constexpr (CL > 1) {
-                // the peer's last commits arrive on this CTA's empty barriers: see
-                // every stage released once more before the CTA may exit
+                // the even CTA's last commits arrive on this CTA's empty barriers:
+                // see every stage released once more before the CTA may exit
                 for (int i = 0; i < C::STAGES; ++i) {
                     if (!ptx::wait_bounded(&empty[stage], phase ^ 1, abort_flag, &g_gemm_err,
                                            ERRBIT_TIMEOUT))
@@ -748,7 +777,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         producer_done:
-            if (*abort_flag) {
+            // pairs: only the even CTA's full barriers count loads
+            if (*abort_flag && crank == 0) {
                 // let every load still in flight land before the CTA can exit
                 int s = stage;
                 uint32_t ph = phase;
@@ -763,11 +793,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && crank == 0) {
             // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = OPK == OP_TF32   ? ptx::idesc_tf32_f32(BM, BN)
-                                   : OPK == OP_E4M3 ? ptx::idesc_e4m3_f32(BM, BN)
-                                                    : ptx::idesc_bf16_f32(BM, BN);
+            constexpr int MM = CL * BM;
+            const uint32_t idesc = OPK == OP_TF32   ? ptx::idesc_tf32_f32(MM, BN)
+                                   : OPK == OP_E4M3 ? ptx::idesc_e4m3_f32(MM, BN)
+                                                    : ptx::idesc_bf16_f32(MM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -792,7 +823,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the descriptor's 16-byte address units)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        if constexpr (OPK == OP_TF32)
+                        if constexpr (CL == 2)
+                            ptx::umma_pair_ss<OPK>(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                                   (kb > 0 || kk > 0) ? 1u : 0u);
+                        else if constexpr (OPK == OP_TF32)
                             ptx::umma_tf32_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
                                               (kb > 0 || kk > 0) ? 1u : 0u);
                         else if constexpr (OPK == OP_E4M3)
@@ -805,19 +839,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (CL == 1)
                         ptx::umma_commit(&empty[stage]);
                     else
-                        ptx::umma_commit_mc(&empty[stage], kPeers);
+                        ptx::umma_commit_pair(&empty[stage], 3);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                ptx::umma_commit(&tfull[acc]);
+                if constexpr (CL == 1)
+                    ptx::umma_commit(&tfull[acc]);
+                else
+                    ptx::umma_commit_pair(&tfull[acc], 3);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1;
             }
             // every MMA issued above completes before TMEM can be released
-            ptx::umma_commit(drain);
+            if constexpr (CL == 1)
+                ptx::umma_commit(drain);
+            else
+                ptx::umma_commit_pair(drain, 1);
             volatile int never = 0;
             ptx::wait_bounded(drain, 0, &never, &g_gemm_err, ERRBIT_TIMEOUT);
         }
@@ -862,7 +902,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&tempty[acc]);
+            if constexpr (CL == 1) {
+                ptx::mbar_arrive(&tempty[acc]);
+            } else {
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&tempty[acc]), 0));
+            }
             if (!eok) break;
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
@@ -882,20 +927,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    // pairs: both CTAs are done with TMEM and every arrival on the other's
+    // barriers has landed before either frees anything
+    if constexpr (CL > 1) ptx::cluster_sync();
     if (warp == 0) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if constexpr (CL == 1)
+            ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+        else
+            ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     }
-    // neither CTA of a pair leaves while the other may still write to it
-    if constexpr (CL > 1) ptx::cluster_sync();
 }
 
 template <int BN, int EPI, int OPK = OP_BF16, int CL = 1>
 cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                         const CUtensorMap& ty2, const CUtensorMap& tr, const Params& p,
                         cudaStream_t s) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, CL>;
     auto kern = gemm_tc_kernel<BN, EPI, OPK, CL>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -980,15 +1029,15 @@ static cudaError_t launch_gemm(const void* x, const void* W, int opk, int M, int
     const int oeb = tf32 ? 4 : e4m3 ? 1 : 2;
     CUtensorMap ta, tb;
     if (!make_tmap_2d(&ta, x, odt, oeb, M, K, K, BM, bke)) return cudaErrorInvalidValue;
-    // in pairs, B boxes of BN/2 rows: each CTA of a pair loads one half for both
-    const int cl = cluster_for(epi);
+    // B boxes of BN/2 rows: each CTA of a pair holds half of the B tile
+    const int cl = kCluster;
     if (!make_tmap_2d(&tb, W, odt, oeb, N, K, K, BN / cl, bke)) return cudaErrorInvalidValue;
     Params p;
     p.M = M;
     p.N = N;
     p.K = K;
-    // in pairs, an even number of M blocks, so the CTAs of a pair share N
-    // blocks; a last block past M (odd M/128) reads zeros and stores nothing
+    // an even number of M blocks, so the CTAs of a pair share N blocks; a
+    // last block past M (odd M/128) reads zeros and stores nothing
     p.tiles_m = ((M + BM - 1) / BM + cl - 1) / cl * cl;
     p.tiles_n = (N + BN - 1) / BN;
     p.num_kb = (K + bke - 1) / bke;
@@ -1022,26 +1071,26 @@ static cudaError_t launch_gemm(const void* x, const void* W, int opk, int M, int
     LaunchScope ls(kind, s);
     if (tf32) {
         if (epi != EPI_STORE) return cudaErrorNotSupported;
-        if (BN == 256) return launch_impl<256, EPI_STORE, OP_TF32, 2>(ta, tb, ty, ty2, tr, p, s);
-        return launch_impl<128, EPI_STORE, OP_TF32, 2>(ta, tb, ty, ty2, tr, p, s);
+        if (BN == 256) return launch_impl<256, EPI_STORE, OP_TF32, kCluster>(ta, tb, ty, ty2, tr, p, s);
+        return launch_impl<128, EPI_STORE, OP_TF32, kCluster>(ta, tb, ty, ty2, tr, p, s);
     }
     if (e4m3) {
         if (BN == 256) {
-            if (epi == EPI_QKV) return launch_impl<256, EPI_QKV, OP_E4M3, 1>(ta, tb, ty, ty2, tr, p, s);
+            if (epi == EPI_QKV) return launch_impl<256, EPI_QKV, OP_E4M3, kCluster>(ta, tb, ty, ty2, tr, p, s);
             if (epi == EPI_SWIGLU)
-                return launch_impl<256, EPI_SWIGLU, OP_E4M3, 1>(ta, tb, ty, ty2, tr, p, s);
-            return launch_impl<256, EPI_STORE, OP_E4M3, 2>(ta, tb, ty, ty2, tr, p, s);
+                return launch_impl<256, EPI_SWIGLU, OP_E4M3, kCluster>(ta, tb, ty, ty2, tr, p, s);
+            return launch_impl<256, EPI_STORE, OP_E4M3, kCluster>(ta, tb, ty, ty2, tr, p, s);
         }
-        if (BN == 224) return launch_impl<224, EPI_STORE, OP_E4M3, 2>(ta, tb, ty, ty2, tr, p, s);
-        return launch_impl<128, EPI_STORE, OP_E4M3, 2>(ta, tb, ty, ty2, tr, p, s);
+        if (BN == 224) return launch_impl<224, EPI_STORE, OP_E4M3, kCluster>(ta, tb, ty, ty2, tr, p, s);
+        return launch_impl<128, EPI_STORE, OP_E4M3, kCluster>(ta, tb, ty, ty2, tr, p, s);
     }
     if (BN == 256) {
-        if (epi == EPI_QKV) return launch_impl<256, EPI_QKV, OP_BF16, 1>(ta, tb, ty, ty2, tr, p, s);
-        if (epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, OP_BF16, 1>(ta, tb, ty, ty2, tr, p, s);
-        return launch_impl<256, EPI_STORE, OP_BF16, 2>(ta, tb, ty, ty2, tr, p, s);
+        if (epi == EPI_QKV) return launch_impl<256, EPI_QKV, OP_BF16, kCluster>(ta, tb, ty, ty2, tr, p, s);
+        if (epi == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, OP_BF16, kCluster>(ta, tb, ty, ty2, tr, p, s);
+        return launch_impl<256, EPI_STORE, OP_BF16, kCluster>(ta, tb, ty, ty2, tr, p, s);
     }
-    if (BN == 224) return launch_impl<224, EPI_STORE, OP_BF16, 2>(ta, tb, ty, ty2, tr, p, s);
-    return launch_impl<128, EPI_STORE, OP_BF16, 2>(ta, tb, ty, ty2, tr, p, s);
+    if (BN == 224) return launch_impl<224, EPI_STORE, OP_BF16, kCluster>(ta, tb, ty, ty2, tr, p, s);
+    return launch_impl<128, EPI_STORE, OP_BF16, kCluster>(ta, tb, ty, ty2, tr, p, s);
 }
 
 int gemm_tc_tiles_n(int M, int N) {
