@@ -51,6 +51,7 @@ namespace {
 constexpr int BQ = 128;          // query rows per tile
 constexpr int kThreads = 320;    // 10 warps
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleSum = 256.0f;   // 2^kRescaleLog2
 
 // F32: tf32 operands in float32 storage.  A 128-byte shared-memory row holds
 // AE elements (64 bf16 or 32 float32); one MMA consumes 32 bytes of K per row.
@@ -97,14 +98,33 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// One pass over a 128-key score row of S in TMEM (64 columns per load):
-// mx <- max(mx, unmasked scores) and, when WRITE, P = 2^(s*sl2 - m_ref) rounded
-// to bf16 into the row's 128-byte-swizzled shared-memory slots, rs += sum(P).
-// DIAG masks keys past the query: key column col is hidden from this row when
-// col > row + dof (dof = first query position of the tile - first key position).
-template <bool DIAG, bool WRITE, int BKV>
-__device__ __forceinline__ void tile_pass(uint32_t tS, uint8_t* Prow, int sw, int row, int dof,
-                                          float sl2, float m_ref, float& mx, float& rs) {
+// Max of the unmasked scores of this thread's row of a bf16-mode score tile in
+// TMEM (64 columns per load).  DIAG masks keys past the query: key column col
+// is hidden from this row when col > row + dof (dof = first query position of
+// the tile - first key position).
+template <bool DIAG, int BKV>
+__device__ __forceinline__ void row_max_bf16(uint32_t tS, int row, int dof, float& mx) {
+#pragma unroll
+    for (int c = 0; c < BKV; c += 64) {
+        uint32_t r[64];
+        __syncwarp();
+        ptx::tmem_ld64(tS + c, r);
+#pragma unroll
+        for (int t = 0; t < 64; ++t) {
+            const bool masked = DIAG && c + t > row + dof;
+            mx = masked ? mx : fmaxf(mx, __uint_as_float(r[t]));
+        }
+    }
+}
+
+// P = 2^(s*sl2 - m_ref) of this thread's row, rounded to bf16 into the row's
+// 128-byte-swizzled shared-memory slots; rs += sum(P).  The scale-and-shift and
+// the row sum run on packed float pairs (two lanes of work per instruction).
+template <bool DIAG, int BKV>
+__device__ __forceinline__ void row_exp_bf16(uint32_t tS, uint8_t* Prow, int sw, int row, int dof,
+                                             float sl2, float m_ref, float& rs) {
+    const float2 k2 = make_float2(sl2, sl2), b2 = make_float2(-m_ref, -m_ref);
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < BKV; c += 64) {
         uint32_t r[64];
@@ -114,28 +134,31 @@ __device__ __forceinline__ void tile_pass(uint32_t tS, uint8_t* Prow, int sw, in
         for (int c8 = 0; c8 < 8; ++c8) {
             float e[8];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
+            for (int t = 0; t < 8; t += 2) {
                 const int col = c + c8 * 8 + t;
-                const float sv = __uint_as_float(r[c8 * 8 + t]);
-                const bool masked = DIAG && col > row + dof;
-                mx = masked ? mx : fmaxf(mx, sv);
-                if (WRITE) {
-                    e[t] = masked ? 0.f : ex2(fmaf(sv, sl2, -m_ref));
-                    rs += e[t];
+                const float2 x = __ffma2_rn(
+                    make_float2(__uint_as_float(r[c8 * 8 + t]), __uint_as_float(r[c8 * 8 + t + 1])),
+                    k2, b2);
+                float2 ev = make_float2(ex2(x.x), ex2(x.y));
+                if (DIAG) {
+                    ev.x = col > row + dof ? 0.f : ev.x;
+                    ev.y = col + 1 > row + dof ? 0.f : ev.y;
                 }
+                acc = __fadd2_rn(acc, ev);
+                e[t] = ev.x;
+                e[t + 1] = ev.y;
             }
-            if (WRITE) {
-                uint4 u;
-                u.x = ptx::pack_bf16x2(e[0], e[1]);
-                u.y = ptx::pack_bf16x2(e[2], e[3]);
-                u.z = ptx::pack_bf16x2(e[4], e[5]);
-                u.w = ptx::pack_bf16x2(e[6], e[7]);
-                const int chunk_all = (c >> 3) + c8;          // 16-byte chunk index 0..15
-                const int atom = chunk_all >> 3, chunk = chunk_all & 7;
-                *reinterpret_cast<uint4*>(Prow + atom * BQ * 128 + ((chunk ^ sw) << 4)) = u;
-            }
+            uint4 u;
+            u.x = ptx::pack_bf16x2(e[0], e[1]);
+            u.y = ptx::pack_bf16x2(e[2], e[3]);
+            u.z = ptx::pack_bf16x2(e[4], e[5]);
+            u.w = ptx::pack_bf16x2(e[6], e[7]);
+            const int chunk_all = (c >> 3) + c8;          // 16-byte chunk index 0..15
+            const int atom = chunk_all >> 3, chunk = chunk_all & 7;
+            *reinterpret_cast<uint4*>(Prow + atom * BQ * 128 + ((chunk ^ sw) << 4)) = u;
         }
     }
+    rs += acc.x + acc.y;
 }
 
 // Round a float32 to tf32 (10 fraction bits), nearest with ties to even.
@@ -174,13 +197,25 @@ __device__ __forceinline__ void tile_pass_f32(uint32_t tS, uint8_t* Prow, int sw
     }
 }
 
-template <bool DIAG, bool WRITE, bool F32, int BKV>
-__device__ __forceinline__ void pass(uint32_t tS, uint8_t* Prow, int sw, int row, int dof,
-                                     float sl2, float m_ref, float& mx, float& rs) {
-    if constexpr (F32)
-        tile_pass_f32<DIAG, WRITE>(tS, Prow, sw, row, dof, sl2, m_ref, mx, rs);
-    else
-        tile_pass<DIAG, WRITE, BKV>(tS, Prow, sw, row, dof, sl2, m_ref, mx, rs);
+// The row's tile max (row_max) and its P with row sum (row_exp), bf16 or tf32.
+template <bool DIAG, bool F32, int BKV>
+__device__ __forceinline__ void row_max(uint32_t tS, int row, int dof, float& mx) {
+    if constexpr (F32) {
+        float unused = 0.f;
+        tile_pass_f32<DIAG, false>(tS, nullptr, 0, row, dof, 0.f, 0.f, mx, unused);
+    } else {
+        row_max_bf16<DIAG, BKV>(tS, row, dof, mx);
+    }
+}
+template <bool DIAG, bool F32, int BKV>
+__device__ __forceinline__ void row_exp(uint32_t tS, uint8_t* Prow, int sw, int row, int dof,
+                                        float sl2, float m_ref, float& rs) {
+    if constexpr (F32) {
+        float unused = -INFINITY;
+        tile_pass_f32<DIAG, true>(tS, Prow, sw, row, dof, sl2, m_ref, unused, rs);
+    } else {
+        row_exp_bf16<DIAG, BKV>(tS, Prow, sw, row, dof, sl2, m_ref, rs);
+    }
 }
 
 template <int HD, bool F32>
@@ -245,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&v_full[i], 1);
             ptx::mbar_init(&v_empty[i], 1);
             ptx::mbar_init(&s_full[i], 1);
-            ptx::mbar_init(&p_full[i], 128);
+            ptx::mbar_init(&p_full[i], 4);     // lane 0 of each softmax warp of head i
             ptx::mbar_init(&o_done[i], 1);
         }
         ptx::mbar_init(drain, 1);
@@ -412,48 +447,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int dof = qpos0 - j * BKV;           // key col c hidden iff c > row + dof
             const bool diag = dof < BKV - 1;
             const float sl2 = p.scale_log2;
-            // Speculative single pass: P against the running max m while finding the
-            // tile max.  If the tile raises a row's max by more than 2^8 (always on
-            // the first tile), that row takes the new max, l and O are rescaled and
-            // the warp redoes the pass.
-            float mx = -INFINITY, rs = 0.f;
-            if (j > 0) {
-                if (diag) pass<true, true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
-                else pass<false, true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
+            // Speculative single pass: P against the running max m.  A score more
+            // than 2^8 above m makes its P, and so the row sum, exceed 2^8; only
+            // then is the tile max taken, and if it does raise the row's max by more
+            // than 2^8 that row takes the new max, l and O are rescaled and the warp
+            // redoes the pass.  The first tile takes its max before the pass.
+            float rs = 0.f;
+            if (j == 0) {
+                float mx = -INFINITY;
+                if (diag) row_max<true, F32, BKV>(tS, row, dof, mx);
+                else row_max<false, F32, BKV>(tS, row, dof, mx);
+                m = mx * sl2;                   // key 0 is never masked on the first tile
+                if (diag) row_exp<true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                else row_exp<false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
             } else {
-                if (diag) pass<true, false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
-                else pass<false, false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, mx, rs);
-            }
-            const float m_tile = mx * sl2;
-            const bool need = (j == 0) || (m_tile > m + kRescaleLog2);
-            if (__any_sync(0xffffffffu, need)) {
-                float alpha = 1.f;
-                if (need) {
-                    alpha = ex2(m - m_tile);       // 0 on the first tile (m = -inf)
-                    m = m_tile;
-                    l *= alpha;
-                }
-                if (j > 0) {
+                if (diag) row_exp<true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                else row_exp<false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                const bool suspect = !(rs <= kRescaleSum);
+                if (__any_sync(0xffffffffu, suspect)) {
+                    float mx = -INFINITY;
+                    if (diag) row_max<true, F32, BKV>(tS, row, dof, mx);
+                    else row_max<false, F32, BKV>(tS, row, dof, mx);
+                    const float m_tile = mx * sl2;
+                    const bool need = m_tile > m + kRescaleLog2;
+                    if (__any_sync(0xffffffffu, need)) {
+                        float alpha = 1.f;
+                        if (need) {
+                            alpha = ex2(m - m_tile);
+                            m = m_tile;
+                            l *= alpha;
+                        }
 #pragma unroll 1
-                    for (int c = 0; c < HD; c += 32) {
-                        uint32_t r[32];
-                        __syncwarp();
-                        ptx::tmem_ld32(tO + c, r);
+                        for (int c = 0; c < HD; c += 32) {
+                            uint32_t r[32];
+                            __syncwarp();
+                            ptx::tmem_ld32(tO + c, r);
 #pragma unroll
-                        for (int t = 0; t < 32; ++t)
-                            r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
-                        ptx::tmem_st32(tO + c, r);
+                            for (int t = 0; t < 32; ++t)
+                                r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+                            ptx::tmem_st32(tO + c, r);
+                        }
+                        rs = 0.f;
+                        if (diag) row_exp<true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                        else row_exp<false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
                     }
                 }
-                rs = 0.f;
-                float unused = -INFINITY;
-                if (diag) pass<true, true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, unused, rs);
-                else pass<false, true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, unused, rs);
             }
             l += rs;
+            // every lane's P row is visible to the tensor core before lane 0
+            // releases the warp's quarter of P_i
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&p_full[i]);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&p_full[i]);
         }
         if (ok) {
             ok = ptx::wait_bounded(&o_done[i], (n_kv - 1) & 1, abort_flag, &g_attn_err,
