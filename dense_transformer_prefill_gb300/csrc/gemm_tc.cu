@@ -304,13 +304,16 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
                 acc_ld32<SC>(p, tbase, th + half + i0, grow, n0, rb, rsc);
                 if (live) {
                     const int pos = ea.tok_pos ? ea.tok_pos[grow] : grow;
-                    const float2* cs = ea.rope + (size_t)pos * half + i0;
+                    // (cos, sin) pairs j, j+1 in one 16-byte load: rows of the table
+                    // and i0 are multiples of 32 pairs
+                    const float4* cs = reinterpret_cast<const float4*>(ea.rope + (size_t)pos * half + i0);
                     float ya[32], yb[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float a = f32(ra[j]) * rstd * w[i0 + j];
                         const float b = f32(rb[j]) * rstd * w[half + i0 + j];
-                        const float2 c = cs[j];
+                        const float4 c4 = cs[j >> 1];
+                        const float2 c = (j & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
                         ya[j] = a * c.x - b * c.y;
                         yb[j] = a * c.y + b * c.x;
                     }
@@ -589,13 +592,17 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
                 __syncwarp();
                 acc_ld32<SC>(p, tbase, th + i0, grow, n0, ra, rsc);
                 acc_ld32<SC>(p, tbase, th + half + i0, grow, n0, rb, rsc);
-                const float2* cs = ea.rope + (size_t)(live ? pos : 0) * half + i0;
+                // (cos, sin) pairs j, j+1 in one 16-byte load: rows of the table
+                // and i0 are multiples of 32 pairs
+                const float4* cs =
+                    reinterpret_cast<const float4*>(ea.rope + (size_t)(live ? pos : 0) * half + i0);
                 float ya[32], yb[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const float a = f32(ra[j]) * rstd * w[i0 + j];
                     const float bv = f32(rb[j]) * rstd * w[half + i0 + j];
-                    const float2 c2 = cs[j];
+                    const float4 c4 = cs[j >> 1];
+                    const float2 c2 = (j & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
                     ya[j] = a * c2.x - bv * c2.y;
                     yb[j] = a * c2.y + bv * c2.x;
                 }
