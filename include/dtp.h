@@ -31,6 +31,11 @@
  *     dtp_check() reports after synchronising the stream.
  *   - Every function returns DTP_OK (0) or a negative DTP_ERR_* code and, on
  *     error, sets a message readable with dtp_last_error() (per thread).
+ *   - Execution resources: the tensor-core GEMMs launch thread-block clusters
+ *     of two CTAs, one CTA per SM, and take as many clusters as can be
+ *     resident at once.  A context in which no two-CTA cluster of that size
+ *     fits gets DTP_ERR_CUDA from the first GEMM.  The tensor-core attention
+ *     launches one CTA of 320 threads per (query tile, head pair).
  */
 #ifndef DTP_H
 #define DTP_H
