@@ -206,6 +206,16 @@ def attention_sweep(dtp, dev, peak, Ts=(1024, 4096, 8192, 16384), reps=5) -> dic
     return out
 
 
+def l2_note(cfg) -> str:
+    """Whether a step's inputs exceed the 129 MB L2 (then no flush is needed
+    between timed steps): the packed GEMM weights alone, in the step's operand type."""
+    eb = {"e4m3": 1, "bf16": 2}.get(cfg.precision, 4)
+    wbytes = cfg.gemm_flops(1) / 2 * eb          # gemm_flops(1) = 2 * weight elements
+    if wbytes > 129e6:
+        return f"inputs larger than L2 (packed weights {wbytes / 1e9:.1f} GB exceed 129 MB)"
+    return f"inputs smaller than L2 (packed weights {wbytes / 1e6:.1f} MB): steps after the first run L2-warm"
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -237,11 +247,12 @@ def main():
               "n_head": cfg.n_head, "n_head_kv": cfg.n_head_kv, "head_dim": cfg.head_dim,
               "n_ff": cfg.n_ff, "n_vocab": cfg.n_vocab, "sequences_per_gpu": 1,
               "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-              "l2": "inputs larger than L2 (packed weights exceed 129 MB)"}
+              "l2": l2_note(cfg)}
 
     if args.impl == "reference":
         if rank != 0:
             return
+        config["l2"] = "not applicable (CPU oracle)"
         sampler = OracleSample(cfg)
         sampler.run()       # one untimed warm-up (BLAS thread pool); more would only repeat it
         samples = [sampler.run() for _ in range(args.steps)]
