@@ -21,6 +21,7 @@ invariants, brute force on tiny inputs, library routines in float64).
 """
 from .model import (  # noqa: F401
     argmax,
+    bf16_fused_normed_linear,
     forward,
     forward_chunk,
     forward_layer,

@@ -25,9 +25,17 @@ sites, not their bodies):
     0 .. p0-1 kept from earlier chunks, then to its own; its logits are the
     full pass's rows p0 .. p0+C-1.
   * bf16-operand mode: matrices are rounded to bf16 once; every GEMM input
-    activation (normed h, attention output, SwiGLU act, final normed x) and the
-    q/k/v handed to attention are rounded to bf16 (nearest, ties to even); all
-    sums and the residual stream stay in float64.
+    activation (normed h = bf16(rms_norm(x) * w), attention output, SwiGLU act,
+    final normed x) and the q/k/v handed to attention are rounded to bf16
+    (nearest, ties to even); all sums and the residual stream stay in float64.
+    This is the plain reading of "bf16 operands" and the default.
+  * bf16 mode with the norm fused (`bf16_fused_norm=True`, a diagnostic): the
+    RMSNorm before the QKV and gate/up projections is applied as a row scale
+    after the product, as a fused kernel may compute it.  The matrix input is
+    bf16(x), the matrix is bf16(W * w) (the norm weight multiplies W's columns
+    before the rounding), and 1/rms(x) scales each row of the product.  Without
+    rounding this is the same function as the plain mode; only the rounding
+    points move.
   * tf32-operand mode: the same GEMM operands rounded to TensorFloat-32 (10-bit
     fraction, nearest, ties to even) instead, and q/k/v as well (that mode's
     tensor-core attention reads tf32); the gate stays unrounded.
@@ -121,9 +129,9 @@ def _rounders(bf16_operands: bool, tf32_operands: bool, fp8_operands: bool = Fal
 # Ops
 # --------------------------------------------------------------------------------------
 def rms_norm(x, w, eps: float) -> np.ndarray:
-    """forward.rs, Model::forward, `e.rms_norm(x, w, out, ncols, nrows, eps)`:
-    each row (last axis, length ncols) is divided by sqrt(mean(row^2) + eps)
-    and multiplied elementwise by w."""
+    """forward.rs, Model::forward, the RMSNorm step (nrows rows of ncols values,
+    a weight vector and eps): each row (last axis) is divided by
+    sqrt(mean(row^2) + eps) and multiplied elementwise by w."""
     x = np.asarray(x, dtype=F64)
     ms = np.mean(x * x, axis=-1, keepdims=True)
     return x / np.sqrt(ms + eps) * np.asarray(w, dtype=F64)
@@ -148,8 +156,9 @@ def rope_angles(pos, n_dims: int, freq_base: float) -> np.ndarray:
 
 
 def rope_neox(x, pos, n_heads: int, head_dim: int, n_dims: int, freq_base: float) -> np.ndarray:
-    """forward.rs, Model::forward, `e.rope_neox(&mut q, &pos_d, head_dim,
-    rope_dim_count, n_head, t, freq_base, 1.0)`: rotate, for every (token,
+    """forward.rs, Model::forward, the NeoX RoPE step applied to q and to k
+    (rope_dim_count rotated dims, base freq_base, frequency scale 1, one
+    position per token): rotate, for every (token,
     head) row of head_dim, the pairs (i, i + n_dims/2), i < n_dims/2, by
     angle[token, i]; dims n_dims..head_dim pass through."""
     x = np.asarray(x, dtype=F64)
@@ -168,8 +177,8 @@ def rope_neox(x, pos, n_heads: int, head_dim: int, n_dims: int, freq_base: float
 
 def sdpa_causal_gqa(q, k, v, n_head: int, n_head_kv: int, head_dim: int, scale: float,
                     rows=None, p0: int = 0) -> np.ndarray:
-    """forward.rs, Model::forward, `e.sdpa_naive(q, k, v, attn, head_dim,
-    n_head, n_head_kv, t, t, scale, true)` with scale = 1/sqrt(head_dim):
+    """forward.rs, Model::forward, the attention step: causal, as many keys as
+    queries, scale = 1/sqrt(head_dim):
     out[t, head i] = sum_{s <= t} softmax_s(q[t,i] . k[s,j] * scale) v[s,j],
     j = i // (n_head / n_head_kv).  q [T, n_head*hd], k/v [T, n_head_kv*hd].
 
@@ -210,16 +219,29 @@ def silu(x) -> np.ndarray:
 
 
 def swiglu(gate, up) -> np.ndarray:
-    """forward.rs, Model::forward, `ffn_act(e, cfg, &gate, &up, &mut act, t*n_ff)`
-    (the dense arm; the T-parallel page calls the same step `silu_mul(g, u)`):
+    """forward.rs, Model::forward, the FFN activation of the dense arm over
+    t*n_ff values (the T-parallel page names the same step silu_mul):
     act = silu(gate) * up elementwise."""
     return silu(gate) * np.asarray(up, dtype=F64)
 
 
 def linear(x, W) -> np.ndarray:
-    """forward.rs, Model::forward, `e.matmul(&w, &x, t)`: W is [out_features,
+    """forward.rs, Model::forward, the projection matmul: W is [out_features,
     in_features] and x is token-major [T, in_features]; y = x W^T [T, out]."""
     return np.asarray(x, dtype=F64) @ np.asarray(W, dtype=F64).T
+
+
+def bf16_fused_normed_linear(x, w_norm, W, eps: float) -> np.ndarray:
+    """rms_norm(x) * w_norm followed by the projection W, with the rounding points
+    of a norm fused into a bf16 GEMM: the GEMM multiplies bf16(x) by
+    bf16(W * w_norm) (w_norm scales W's columns, i.e. the input features, before
+    the rounding) and each output row is then scaled by 1/sqrt(mean(x^2) + eps),
+    computed from the unrounded x.  Without the two roundings this equals
+    linear(rms_norm(x, w_norm, eps), W)."""
+    x = np.asarray(x, dtype=F64)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    Wn = np.asarray(W, dtype=F64) * np.asarray(w_norm, dtype=F64)[None, :]
+    return r * linear(round_bf16(x), round_bf16(Wn))
 
 
 # --------------------------------------------------------------------------------------
@@ -236,31 +258,39 @@ def _mats(w: dict, rnd) -> dict:
 
 def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=None,
                   kv_prefix=None, tf32_operands: bool = False,
-                  fp8_operands: bool = False) -> np.ndarray:
+                  fp8_operands: bool = False, bf16_fused_norm: bool = False,
+                  rows=None) -> np.ndarray:
     """One decoder layer, forward.rs `Model::forward` loop body, on the residual
     stream x [T, n_embd]; returns the new x.  If `kv_out` is a list, the layer's
     attention inputs (k after QK-norm and RoPE, and v) are appended to it.
+
+    `rows` (optional) returns only those rows of the new x [len(rows), n_embd]:
+    keys and values come from every row of x, attention runs for the listed
+    query rows only, and the O projection, residual and FFN, which act on each
+    row alone, only for them.
 
     `kv_prefix` = (k, v) of the p0 positions before x (which then sits at
     positions pos = p0 .. p0+T-1): attention runs over those keys followed by
     x's own, the only way earlier positions reach later ones."""
     op, opm, opw, opa, opg = _rounders(bf16_operands, tf32_operands, fp8_operands)
-    L = _mats(lw, opw)
+    if bf16_fused_norm and not bf16_operands:
+        raise ValueError("bf16_fused_norm needs bf16_operands")
+    if bf16_fused_norm:     # the normed projections round W * w themselves
+        lw_rest = {n: a for n, a in lw.items() if n not in ("wq", "wk", "wv", "w_gate", "w_up")}
+        L = _mats(lw_rest, opw)
+    else:
+        L = _mats(lw, opw)
     d, h, g, hd = cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim
     eps = cfg.rms_eps
     scale = 1.0 / np.sqrt(F64(hd))
 
     def normed_linears(xin, w_norm, names):
-        """rms_norm(xin) * w_norm followed by each matrix.  In bf16-operand mode
-        the norm is fused the way the bf16 kernels compute it: the matrix input is
-        bf16(xin), the norm weight multiplies the matrix's columns before its bf16
-        rounding, and the row's 1/rms scales the product -- the same function of
-        xin, with those rounding points."""
-        if bf16_operands:
-            r = 1.0 / np.sqrt(np.mean(np.asarray(xin, F64) ** 2, axis=1) + eps)
-            a = round_bf16(xin)
-            wn = np.asarray(w_norm, F64)[None, :]
-            return [r[:, None] * linear(a, round_bf16(np.asarray(lw[n], F64) * wn)) for n in names]
+        """rms_norm(xin) * w_norm followed by each matrix.  With bf16_fused_norm
+        the matrix input is bf16(xin), the norm weight multiplies the matrix's
+        columns before its bf16 rounding, and the row's 1/rms scales the product
+        -- the same function of xin, with those rounding points."""
+        if bf16_fused_norm:
+            return [bf16_fused_normed_linear(xin, w_norm, lw[n], eps) for n in names]
         hn = op(rms_norm(xin, w_norm, eps))
         return [linear(hn, L[n]) for n in names]
 
@@ -282,7 +312,11 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
         p0 = kv_prefix[0].shape[0]
         k = np.concatenate([np.asarray(kv_prefix[0], dtype=F64), k])
         v = np.concatenate([np.asarray(kv_prefix[1], dtype=F64), v])
-    attn = sdpa_causal_gqa(q, k, v, h, g, hd, scale, p0=p0)
+    if rows is not None:
+        rows = np.asarray(rows)
+        x = np.asarray(x, dtype=F64)[rows]
+        gate = None if gate is None else gate[rows]
+    attn = sdpa_causal_gqa(q, k, v, h, g, hd, scale, rows=rows, p0=p0)
     if gate is not None:
         attn = attn / (1.0 + np.exp(-gate))          # attn * sigmoid(gate)
     attn = opm(attn)
@@ -295,7 +329,7 @@ def forward_layer(cfg, lw: dict, x, pos, bf16_operands: bool = False, kv_out=Non
 
 def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidden: bool = False,
             layer_source=None, kv_out=None, tf32_operands: bool = False,
-            fp8_operands: bool = False):
+            fp8_operands: bool = False, bf16_fused_norm: bool = False):
     """forward.rs `Model::forward`: logits [T, n_vocab] for `tokens`, positions 0..T-1.
 
     weights: {"tok_embd" [V,d], "layers": [dict per layer], "output_norm" [d],
@@ -316,7 +350,7 @@ def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidd
     for l in range(cfg.n_layer):
         lw = layer_source(l) if layer_source is not None else weights["layers"][l]
         x = forward_layer(cfg, lw, x, pos, bf16_operands, kv_out, tf32_operands=tf32_operands,
-                          fp8_operands=fp8_operands)
+                          fp8_operands=fp8_operands, bf16_fused_norm=bf16_fused_norm)
         if return_hidden:
             hidden.append(x.copy())
     hn = op(rms_norm(x, np.asarray(weights["output_norm"], dtype=F64), cfg.rms_eps))
@@ -327,7 +361,8 @@ def forward(cfg, weights: dict, tokens, bf16_operands: bool = False, return_hidd
 
 
 def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: bool = False,
-                  tf32_operands: bool = False, fp8_operands: bool = False):
+                  tf32_operands: bool = False, fp8_operands: bool = False,
+                  bf16_fused_norm: bool = False):
     """Chunked prefill: logits [C, n_vocab] for the next C tokens of a sequence
     whose first p0 positions went through earlier calls.  forward.rs
     `Model::forward` is causal, so those positions reach these only through
@@ -347,7 +382,7 @@ def forward_chunk(cfg, weights: dict, tokens, kv_state: list, bf16_operands: boo
         new = []
         prefix = None if first else kv_state[l]
         x = forward_layer(cfg, weights["layers"][l], x, pos, bf16_operands, new, prefix,
-                          tf32_operands, fp8_operands)
+                          tf32_operands, fp8_operands, bf16_fused_norm)
         k, v = new[0]
         if first:
             kv_state.append((k, v))

@@ -42,15 +42,19 @@ def load_model(dtp, cfg, seed=0):
     return m
 
 
-def oracle_forward(cfg, seed=0, T=None, bf16=None, tf32=None, fp8=None):
+def oracle_forward(cfg, seed=0, T=None, bf16=None, tf32=None, fp8=None, fused=None):
     """The oracle in the operand mode of cfg.precision (bf16 / tf32 rounding or
     per-row e4m3 quantisation of the GEMM operands; "f32" exact), unless bf16 /
-    tf32 / fp8 say otherwise."""
+    tf32 / fp8 say otherwise.  In bf16 mode the RMSNorm before the QKV and
+    gate/up projections takes the rounding points of the library's fused
+    kernels (bf16(x) times bf16(W * w), then 1/rms) unless fused=False: the
+    kernels are checked against the oracle with the same rounding points."""
     bf16 = (cfg.precision == "bf16") if bf16 is None else bf16
     tf32 = (cfg.precision == "tf32") if tf32 is None else tf32
     fp8 = (cfg.precision == "e4m3") if fp8 is None else fp8
+    fused = bf16 if fused is None else (fused and bf16)
     w = synth.model_weights(cfg, seed)
     toks = synth.tokens(cfg, seed, T)
     logits, hidden = oracle.forward(cfg, w, toks, bf16_operands=bf16, tf32_operands=tf32,
-                                    fp8_operands=fp8, return_hidden=True)
+                                    fp8_operands=fp8, bf16_fused_norm=fused, return_hidden=True)
     return toks, logits, hidden

@@ -4,19 +4,20 @@ device-side token checks).
 
 Bars.  float32 path: per-layer hidden-state relative L2 <= 1e-5 (as stated).
 
-bf16 path, against the oracle's bf16-operand mode.  Both sides round every GEMM
-input to bf16 (relative ulp u = 2^-8), so any float32-level difference before a
-rounding -- summation order alone gives ~3e-7 -- flips some roundings, and each
-layer adds an independent ~1-ulp-sized relative difference to the residual
-stream; these add in quadrature over depth.  Derived bounds (2x margin):
+bf16 path, against the oracle's bf16-operand mode with the kernels' rounding
+points (the RMSNorm fused as a row scale).  Both sides round every GEMM input to
+bf16 (relative ulp u = 2^-8), so any float32-level difference before a rounding
+-- summation order alone gives ~3e-7 -- flips some roundings, and each layer
+adds an independent ~1-ulp-sized relative difference to the residual stream;
+these add in quadrature over depth.  Derived bounds (2x margin):
   hidden state entering layer l:  rel L2 <= 2 u sqrt(l)        (l >= 1; l = 0 exact)
   logits:                         rel L2 <= 2 u sqrt(L+1) + u  (one more rounding)
   argmax: >= 99.5% agreement, where a flip counts as agreement only if the
   reference's top1-top2 margin is within twice the observed max logit drift
   (the near-tie class of forward.rs `prime_gate_verdict`); no other flip.
-The stated bars (per-layer 2e-3, logit max |diff| 5e-2) are recorded in the
-returned metrics; they are not reachable by a bf16-activation pipeline at depth
-(measured and discussed in DESIGN.md)."""
+These bounds check the kernels.  The stated bars (per-layer 2e-3, logit max
+|diff| 5e-2, raw argmax 99.5%) are measured against the exact oracle in
+test_stated_bars_gpu.py and test_qwen3_8b_gpu.py."""
 import numpy as np
 import pytest
 import torch
@@ -69,9 +70,7 @@ def assert_parity(cfg, gl, gh, rl, rh):
     assert metrics["logit_rel_l2"] <= 2 * u * np.sqrt(cfg.n_layer + 1) + u, metrics
     agree, structured = argmax_agreement_near_tie(gl, rl, 2 * metrics["logit_max_abs"])
     metrics.update(argmax_agreement=agree, structured_flips=structured,
-                   raw_argmax_agreement=float(np.mean(np.argmax(gl, 1) == np.argmax(rl, 1))),
-                   stated_layer_bar_met=max(layer_err) <= 2e-3,
-                   stated_logit_bar_met=metrics["logit_max_abs"] <= 5e-2)
+                   raw_argmax_agreement=float(np.mean(np.argmax(gl, 1) == np.argmax(rl, 1))))
     assert structured == 0 and agree >= 0.995, metrics
     print(f"\nparity {cfg.name} T={cfg.T}: {metrics}")
     return metrics
@@ -149,52 +148,6 @@ def test_token_out_of_range_is_reported(dtp):
     dtp.check()                                      # the error word was cleared
 
 
-def test_qwen3_8b_shape_prefix_rows(dtp):
-    """Full 8B shape, T = 4096, in the launch configuration the bench times.
-    Causality makes rows 0..R-1 of that forward depend on the first R tokens
-    only, so the oracle runs the whole 36-layer model on the R-token prefix
-    (streamed layer by layer) and every layer's hidden rows and the logits of
-    those rows are compared."""
-    cfg = synth.CONFIGS["qwen3-8b-shape"]
-    R = 48
-    m = dtp.Model(cfg)
-    for l in range(cfg.n_layer):
-        m.load_layer(l, synth.layer_weights(cfg, l))
-    emb, onorm, W = synth.tok_embd(cfg), synth.output_norm(cfg), synth.output_weight(cfg)
-    m.load_globals(emb, onorm, W)
-    toks = synth.tokens(cfg)
-    logits, hidden = m.forward(torch.as_tensor(toks.astype(np.int32), device=dev), hidden=True)
-    torch.cuda.synchronize()
-    dtp.check()
-    gh = hidden[:, :R].cpu().numpy().astype(np.float64)
-    gl = logits[:R].cpu().numpy()
-    del logits, hidden
-    x = oracle.round_bf16(emb[toks[:R]].astype(np.float64))
-    del emb
-    pos = np.arange(R)
-    ref_hidden = [x]
-    forced = []
-    for l in range(cfg.n_layer):
-        lw = synth.layer_weights(cfg, l)
-        x = oracle.forward_layer(cfg, lw, x, pos, bf16_operands=True)
-        ref_hidden.append(x)
-        # teacher-forced: the oracle's layer l on the GPU's own input to layer l
-        forced.append(rel_l2(gh[l + 1], oracle.forward_layer(cfg, lw, gh[l], pos,
-                                                             bf16_operands=True)))
-        del lw
-    hn = oracle.round_bf16(oracle.rms_norm(x, onorm, cfg.rms_eps))
-    ref_logits = np.concatenate([oracle.linear(hn, oracle.round_bf16(W[v0:v0 + 16384]))
-                                 for v0 in range(0, cfg.n_vocab, 16384)], axis=1)
-    del W
-    sub = cfg.replace(T=R)
-    assert_parity(sub, gl, gh, ref_logits, np.stack(ref_hidden))
-    # each layer on its own: one layer's rounding differences (one bf16 ulp of the
-    # layer's inputs, 2x margin), with no accumulation over depth
-    print(f"\nteacher-forced per-layer rel L2 (8B, rows 0..{R - 1}): max {max(forced):.2e}, "
-          f"mean {np.mean(forced):.2e}")
-    assert max(forced) <= 2 * 2.0 ** -8, forced
-
-
 @pytest.mark.parametrize("prec", ["f32", "bf16"])
 def test_forward_last_and_kv_cache(dtp, prec):
     """dtp_fwd_prefill_ex: last-position logits (forward.rs `forward_last`) and the
@@ -216,7 +169,8 @@ def test_forward_last_and_kv_cache(dtp, prec):
     np.testing.assert_allclose(last.cpu().numpy()[0], full.cpu().numpy()[-1], rtol=0, atol=1e-6)
     w = synth.model_weights(cfg)
     kv = []
-    ref = oracle.forward(cfg, w, synth.tokens(cfg), bf16_operands=(prec == "bf16"), kv_out=kv)
+    ref = oracle.forward(cfg, w, synth.tokens(cfg), bf16_operands=(prec == "bf16"),
+                         bf16_fused_norm=(prec == "bf16"), kv_out=kv)
     got_k, got_v = kc.float().cpu().numpy(), vc.float().cpu().numpy()
     u = 2.0 ** -8
     for l, (rk, rv) in enumerate(kv):
@@ -271,7 +225,8 @@ def test_varlen_packed_sequences(dtp, prec):
         a = cu[b]
         kv = []
         rl, rh = oracle.forward(cfg, w, toks[a:a + n], bf16_operands=(prec == "bf16"),
-                                tf32_operands=(prec == "tf32"), return_hidden=True, kv_out=kv)
+                                bf16_fused_norm=(prec == "bf16"), tf32_operands=(prec == "tf32"),
+                                return_hidden=True, kv_out=kv)
         assert_parity(cfg.replace(T=n), gl[a:a + n], gh[:, a:a + n], rl, rh)
         np.testing.assert_allclose(glast[b], gl[a + n - 1], rtol=0, atol=1e-6)
         k0 = kc[0, a:a + n].float().cpu().numpy()
