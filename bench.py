@@ -134,9 +134,14 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- oracle timing
 class OracleSample:
     """A bounded sample of the workload for the float64 oracle, scaled to the whole
-    pass: one decoder layer over the first S_l tokens (t_layer) and the lm_head
-    over S_h rows x a V_s-row slice of the vocabulary (t_head);
-    tokens/s = T / (n_layer * t_layer * T/S_l + t_head * (T/S_h) * (V/V_s))."""
+    pass: one decoder layer over the first S_l tokens (t_layer), of which the
+    attention alone takes t_attn (timed on its own at the same shape), and the
+    lm_head over S_h rows x a V_s-row slice of the vocabulary (t_head).  The
+    layer's projections and FFN grow linearly in T and its attention
+    quadratically, so the whole pass is extrapolated as
+      n_layer * ((t_layer - t_attn) * T/S_l + t_attn * (T/S_l)^2)
+      + t_head * (T/S_h) * (V/V_s),
+    and tokens/s = T / that."""
 
     def __init__(self, cfg, s_layer: int = 1024, s_head: int = 512, v_slice: int = 8192):
         self.cfg = cfg
@@ -151,6 +156,9 @@ class OracleSample:
         self.x = synth.tok_embd(cfg)[toks].astype(np.float64)
         self.W = synth.normal(0, synth.TID_OUTPUT, (self.vs, cfg.n_embd), std=0.02)
         self.hn = synth.normal(0, 99, (self.sh, cfg.n_embd))
+        hd = cfg.head_dim
+        self.q = synth.normal(0, 97, (self.sl, cfg.n_head * hd)).astype(np.float64)
+        self.kv = synth.normal(0, 98, (self.sl, cfg.n_head_kv * hd)).astype(np.float64)
 
     def run(self) -> dict:
         import oracle
@@ -160,19 +168,27 @@ class OracleSample:
         oracle.forward_layer(cfg, self.lw, self.x, np.arange(self.sl), **self.mode)
         t_layer = time.perf_counter() - t0
         t0 = time.perf_counter()
+        oracle.sdpa_causal_gqa(self.q, self.kv, self.kv, cfg.n_head, cfg.n_head_kv, cfg.head_dim,
+                               cfg.head_dim ** -0.5)
+        t_attn = min(time.perf_counter() - t0, t_layer)
+        t0 = time.perf_counter()
         rnd = {"bf16": oracle.round_bf16, "tf32": oracle.round_tf32,
                "e4m3": oracle.fake_quant_rows_e4m3}.get(cfg.precision, lambda a: a)
         oracle.linear(rnd(self.hn), rnd(self.W))
         t_head = time.perf_counter() - t0
-        total = (cfg.n_layer * t_layer * T / self.sl
+        r = T / self.sl
+        total = (cfg.n_layer * ((t_layer - t_attn) * r + t_attn * r * r)
                  + t_head * (T / self.sh) * (cfg.n_vocab / self.vs))
         cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
         return {"value": T / total, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample_s": t_layer + t_attn + t_head, "extrapolated_step_s": total,
                 "sample": (f"float64 numpy oracle ({cfg.precision} operand mode,"
                            f" BLAS on all {cores} host cores) on {cfg.name}: 1 decoder layer over "
-                           f"the first {self.sl} tokens ({t_layer:.2f} s) + lm_head over "
-                           f"{self.sh} rows x {self.vs} vocab rows ({t_head:.2f} s), scaled to "
-                           f"{cfg.n_layer} layers x {T} tokens and the full {cfg.n_vocab} vocab")}
+                           f"the first {self.sl} tokens ({t_layer:.2f} s, of which attention "
+                           f"{t_attn:.2f} s) + lm_head over {self.sh} rows x {self.vs} vocab rows "
+                           f"({t_head:.2f} s), extrapolated to {cfg.n_layer} layers x {T} tokens "
+                           f"(attention quadratic, the rest linear in T) and the full "
+                           f"{cfg.n_vocab} vocab")}
 
 
 def attention_sweep(dtp, dev, peak, Ts=(1024, 4096, 8192, 16384), reps=5) -> dict:
@@ -204,6 +220,29 @@ def attention_sweep(dtp, dev, peak, Ts=(1024, 4096, 8192, 16384), reps=5) -> dic
         tf = flops / (ms / n / 1000.0) / 1e12
         out[str(T)] = {"ms": ms / n, "tflops": tf, "frac": tf / peak if peak else None}
     return out
+
+
+def span_summary(fwd, cpy) -> dict:
+    """Where an end-to-end batch's time goes, from per-prompt (start, end) spans in
+    ms: each prompt's pass on the compute stream and each logits copy on the copy
+    stream.  idle = compute-stream gaps between passes; a copy overlaps the next
+    pass when it starts before that pass ends."""
+    if not fwd:
+        return {}
+    f_ms = [e - b for b, e in fwd]
+    c_ms = [e - b for b, e in cpy]
+    idle = [max(0.0, fwd[j + 1][0] - fwd[j][1]) for j in range(len(fwd) - 1)]
+    overlap = [max(0.0, min(cpy[j][1], fwd[j + 1][1]) - max(cpy[j][0], fwd[j + 1][0]))
+               for j in range(min(len(cpy), len(fwd) - 1))]
+    wait = [max(0.0, cpy[j][0] - fwd[j][1]) for j in range(min(len(cpy), len(fwd)))]
+    end = max([e for _, e in fwd] + [e for _, e in cpy])
+    return {"prompts": len(fwd), "span_ms": end,
+            "forward_ms_mean": statistics.mean(f_ms), "forward_ms_max": max(f_ms),
+            "copy_ms_mean": statistics.mean(c_ms) if c_ms else None,
+            "copy_ms_max": max(c_ms) if c_ms else None,
+            "compute_idle_ms_total": sum(idle),
+            "copy_start_after_ready_ms_mean": statistics.mean(wait) if wait else None,
+            "copy_overlapped_with_next_forward_ms_total": sum(overlap)}
 
 
 def l2_note(cfg) -> str:
@@ -254,14 +293,21 @@ def main():
             return
         config["l2"] = "not applicable (CPU oracle)"
         sampler = OracleSample(cfg)
-        sampler.run()       # one untimed warm-up (BLAS thread pool); more would only repeat it
+        for _ in range(args.warmup):          # untimed samples (BLAS thread pool, page-in)
+            sampler.run()
         samples = [sampler.run() for _ in range(args.steps)]
         v = statistics.median(s["value"] for s in samples)
         cb = dict(samples[0])
         cb["value"] = v
+        # each step is one bounded sample; ms_per_step is the whole pass
+        # extrapolated from it (see cpu_baseline.sample), not a timed full pass
         print(json.dumps({"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
                           "steps": args.steps, "warmup": args.warmup,
-                          "ms_per_step": 1000.0 * cfg.T / v, "higher_is_better": True,
+                          "ms_per_step": 1000.0 * cfg.T / v,
+                          "ms_per_step_kind": "extrapolated from one bounded sample per step",
+                          "sample_ms_per_step": 1000.0 * statistics.median(
+                              s["sample_s"] for s in samples),
+                          "higher_is_better": True,
                           "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                           "data": "synthetic", "impl": "reference", "config": config,
                           "cpu_baseline": cb,
@@ -363,11 +409,27 @@ def main():
         barrier()
         e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e_start.record(stream)
+        h0 = time.perf_counter()
         dtp.fwd_prefill_host_batch(m.c, m.packed, tok_h, outs, ws_h)
+        host_enqueue_ms = (time.perf_counter() - h0) * 1e3
         e_end.record(stream)
         torch.cuda.synchronize(dev)
         dtp.check()
         ems = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
+        # the same call once more with a span around every prompt's pass (caller's
+        # stream) and every logits copy (the library's copy stream): where the
+        # end-to-end time goes
+        dtp.timer_enable(["prompt", "d2h"], args.steps)
+        d0 = time.perf_counter()
+        dtp.fwd_prefill_host_batch(m.c, m.packed, tok_h, outs, ws_h)
+        diag_enqueue_ms = (time.perf_counter() - d0) * 1e3
+        torch.cuda.synchronize(dev)
+        dtp.check()
+        fwd = dtp.timer_spans("prompt", "prompt")
+        cpy = dtp.timer_spans("d2h", "prompt")
+        dtp.timer_disable()
+        e2e_spans = span_summary(fwd, cpy)
+        e2e_spans["host_enqueue_ms"] = diag_enqueue_ms
         # the device-to-host copy of one step's logits on its own: e2e is bound by
         # max(forward pass, this copy), and the copy depends on the host's memory
         c_start, c_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -377,6 +439,9 @@ def main():
         torch.cuda.synchronize(dev)
         d2h_ms = c_start.elapsed_time(c_end)
         e2e = {"value": replica_throughput(world, cfg.T, args.steps, ems), "unit": UNIT,
+               "ms_per_step": ems / args.steps,
+               "host_enqueue_ms_per_step": host_enqueue_ms / args.steps,
+               "spans": e2e_spans,
                "d2h_ms_per_step_alone": d2h_ms,
                "d2h_gbs_alone": log_h[0].numel() * 4 / d2h_ms / 1e6,
                "h2d_bytes_per_step": int(tok_h[0].numel() * 4),
@@ -417,6 +482,16 @@ def main():
                                + ("" if cfg.precision == "bf16" else
                                   f" x the nominal {cfg.precision}/bf16 dense ratio"),
                 "avg_launch_ms": gu_ms / gu_n if gu_n else None}
+    clocks = clk.summary()
+    burst = {"bf16": peaks["bf16_tflops"], "tf32": peaks["bf16_tflops"] * 1.1 / 2.25,
+             "e4m3": peaks["bf16_tflops"] * 2.0}.get(cfg.precision)
+    roofline["frac_burst"] = (achieved / burst) if (achieved and burst) else None
+    # the sustained peak was measured at its own median SM clock; compare per MHz
+    peak_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+    if achieved and peak and peak_mhz and clocks.get("sm_mhz"):
+        roofline["frac_at_equal_clock"] = (achieved / clocks["sm_mhz"]) / (peak / peak_mhz)
+        roofline["clock_note"] = (f"this run's median SM clock {clocks['sm_mhz']:.0f} MHz; the "
+                                  f"sustained peak's {peak_mhz:.0f} MHz")
     at_n, at_ms = kstats["attn"]
     at_flops = cfg.attn_flops() / cfg.n_layer
     at_ach = at_flops / (at_ms / at_n / 1000.0) / 1e12 if at_n else None
@@ -428,6 +503,8 @@ def main():
                                                  ["attn_tc.cu", "ptx.cuh", "internal.h"]) if is8b else None,
                      "flops_per_launch": at_flops,
                      "avg_launch_ms": at_ms / at_n if at_n else None}
+    if at_ach and cfg.precision in ("bf16", "e4m3"):
+        roofline_attn["frac_burst"] = at_ach / peaks["bf16_tflops"]
     per_kernel = {}
     step_flops = 0.0
     for k, (n, kms) in kstats.items():
@@ -455,14 +532,18 @@ def main():
                    if (attn_ms and attn_peak) else None},
         "kernels": per_kernel,
         "instrumented_ms_per_step": instrumented_ms_per_step,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "gpu_launches": int(launches),
         "e2e": e2e,
         "setup_s": setup_s,
     }
     if not args.no_attn_sweep and cfg.precision == "bf16":
+        # timed alone, launch after launch: compared with the burst peak
+        burst = peaks["bf16_tflops"]
         out["attention_sweep"] = {"shape": "h=32, g=8, hd=128, bf16, causal; kernel time only",
-                                  "peak": peak, "T": attention_sweep(dtp, dev, peak)}
+                                  "peak": burst,
+                                  "peak_source": f"bf16_tflops (burst) of {peaks['source']} peaks",
+                                  "T": attention_sweep(dtp, dev, burst)}
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = OracleSample(cfg).run()
     print(json.dumps(out), flush=True)

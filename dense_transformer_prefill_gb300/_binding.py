@@ -14,7 +14,8 @@ from .build import LIB, build  # noqa: F401
 DTP_F32, DTP_BF16, DTP_TF32 = 0, 1, 2
 DTP_PREC_F32, DTP_PREC_TF32, DTP_PREC_BF16, DTP_PREC_E4M3 = 0, 1, 2, 3
 KERNEL_KINDS = {"embed": 0, "rmsnorm": 1, "gemm_qkv": 2, "attn": 3, "gemm_o": 4,
-                "gemm_gateup": 5, "gemm_down": 6, "gemm_lmhead": 7, "other": 8}
+                "gemm_gateup": 5, "gemm_down": 6, "gemm_lmhead": 7, "other": 8,
+                "prompt": 9, "d2h": 10}
 
 c_int, c_float, c_size_t, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
 
@@ -96,6 +97,8 @@ _SIGS = {
     "dtp_timer_enable": ([ctypes.c_uint, c_int], c_int),
     "dtp_timer_disable": ([], c_int),
     "dtp_timer_read": ([c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_float)], c_int),
+    "dtp_timer_spans": ([c_int, c_int, c_int, ctypes.POINTER(c_float), ctypes.POINTER(c_float),
+                         ctypes.POINTER(c_int)], c_int),
 }
 
 
@@ -387,6 +390,16 @@ def timer_read(kind) -> tuple[int, float]:
     _ok(lib().dtp_timer_read(KERNEL_KINDS[kind] if isinstance(kind, str) else kind,
                              ctypes.byref(n), ctypes.byref(ms)))
     return n.value, ms.value
+
+
+def timer_spans(kind, ref_kind, cap: int = 4096) -> list[tuple[float, float]]:
+    """(start, end) in ms of each recorded launch or span of `kind`, measured from
+    the start of the first recorded one of `ref_kind`."""
+    k = KERNEL_KINDS[kind] if isinstance(kind, str) else kind
+    r = KERNEL_KINDS[ref_kind] if isinstance(ref_kind, str) else ref_kind
+    st, en, n = (c_float * cap)(), (c_float * cap)(), c_int(0)
+    _ok(lib().dtp_timer_spans(k, r, cap, st, en, ctypes.byref(n)))
+    return [(st[i], en[i]) for i in range(min(n.value, cap))]
 
 
 def launch_count(reset: bool = False) -> int:

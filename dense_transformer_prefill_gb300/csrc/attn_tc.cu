@@ -1,7 +1,7 @@
-// tcgen05 causal grouped-query flash attention (forward.rs, Model::forward:
-// `e.sdpa_naive(q, k, v, attn, head_dim, n_head, n_head_kv, t, t, scale, true)`,
-// restated as an online-softmax tiled kernel; the pages' naive kernel is prior
-// art only).
+// tcgen05 causal grouped-query flash attention (docs.rs memra-engine 0.130.0,
+// src/forward.rs, Model::forward: the attention step, causal, over all T keys,
+// scaled by 1/sqrt(head_dim); restated as an online-softmax tiled kernel, the
+// pages' naive kernel being prior art only).
 //
 // One CTA = one 128-token query tile of TWO query heads of the same GQA group,
 // so every K/V tile brought into shared memory serves 256 query rows.

@@ -87,8 +87,8 @@ struct TimerState {
 static TimerState g_timer;
 static std::atomic<long long> g_launches{0};
 
-LaunchScope::LaunchScope(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
-    g_launches.fetch_add(1, std::memory_order_relaxed);
+LaunchScope::LaunchScope(int k, cudaStream_t s, bool counts) : kind(k), stream(s), slot(-1) {
+    if (counts) g_launches.fetch_add(1, std::memory_order_relaxed);
     if (!g_timer.mask) return;
     std::lock_guard<std::mutex> lk(g_timer.mu);
     if (!(g_timer.mask & (1u << kind)) || g_timer.used[kind] >= g_timer.capacity) return;
@@ -928,7 +928,11 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
         }
         dtp_fwd_outputs o = {};
         o.logits = buf[b];
-        rc = fwd_checked(cfg, packed, packed_bytes, tok_d, T, o, workspace, ws_bytes, true, stream);
+        {
+            LaunchScope span(DTP_K_PROMPT, s, false);
+            rc = fwd_checked(cfg, packed, packed_bytes, tok_d, T, o, workspace, ws_bytes, true,
+                             stream);
+        }
         if (rc) break;
         cudaEvent_t ready, done;
         if (!new_event(&ready) || !new_event(&done)) {
@@ -936,11 +940,13 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
             break;
         }
         // the copy of prompt j overlaps the forward of prompt j + 1
-        if ((e = cudaEventRecord(ready, s)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(k, ready, 0)) != cudaSuccess ||
-            (e = cudaMemcpyAsync(logits_host[j], buf[b], lbytes, cudaMemcpyDeviceToHost, k)) !=
-                cudaSuccess ||
-            (e = cudaEventRecord(done, k)) != cudaSuccess) {
+        if ((e = cudaEventRecord(ready, s)) == cudaSuccess &&
+            (e = cudaStreamWaitEvent(k, ready, 0)) == cudaSuccess) {
+            LaunchScope span(DTP_K_D2H, k, false);
+            e = cudaMemcpyAsync(logits_host[j], buf[b], lbytes, cudaMemcpyDeviceToHost, k);
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(done, k);
+        if (e != cudaSuccess) {
             rc = fail(DTP_ERR_CUDA, "%s", cudaGetErrorString(e));
             break;
         }
@@ -1248,6 +1254,25 @@ int dtp_timer_enable(unsigned kind_mask, int capacity) {
 int dtp_timer_disable(void) {
     std::lock_guard<std::mutex> lk(g_timer.mu);
     timer_destroy();
+    return DTP_OK;
+}
+
+int dtp_timer_spans(int kind, int ref_kind, int cap, float* start_ms, float* end_ms, int* count) {
+    if (kind < 0 || kind >= DTP_K_COUNT || ref_kind < 0 || ref_kind >= DTP_K_COUNT || cap < 0 ||
+        !count || (cap > 0 && (!start_ms || !end_ms)))
+        return fail(DTP_ERR_INVALID_ARG, "bad kind, capacity or NULL output");
+    std::lock_guard<std::mutex> lk(g_timer.mu);
+    const int n = g_timer.used[kind];
+    if (n > 0 && g_timer.used[ref_kind] == 0)
+        return fail(DTP_ERR_INVALID_ARG, "no span of the reference kind was recorded");
+    for (int i = 0; i < n && i < cap; ++i) {
+        cudaEvent_t origin = g_timer.ev[ref_kind][0][0];
+        cudaError_t e = cudaEventElapsedTime(&start_ms[i], origin, g_timer.ev[kind][0][i]);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&end_ms[i], origin, g_timer.ev[kind][1][i]);
+        if (e != cudaSuccess)
+            return fail(DTP_ERR_CUDA, "cudaEventElapsedTime: %s", cudaGetErrorString(e));
+    }
+    *count = n;
     return DTP_OK;
 }
 

@@ -1,10 +1,10 @@
 // tcgen05 tensor-core GEMM for the projections, the FFN and the lm_head
-// (forward.rs, Model::forward: every `e.matmul(&w, &x, t)`), with the
+// (forward.rs, Model::forward: every projection matmul of the layer and the head), with the
 // neighbouring elementwise steps fused into the epilogue:
 //   EPI_STORE   y = x W^T (+ residual)      -- O / down projections (residual adds,
-//                                              forward.rs `e.add`) and the lm_head
+//                                              forward.rs, the residual adds) and the lm_head
 //   EPI_QKV     per-head QK-RMSNorm + NeoX RoPE on q and k, v stored transposed
-//   EPI_SWIGLU  silu(gate) * up on the interleaved gate/up product (`ffn_act`)
+//   EPI_SWIGLU  silu(gate) * up on the interleaved gate/up product (the FFN activation)
 //
 // D[M, N] = A[M, K] B[N, K]^T with A = activations, B = weights, both
 // K-contiguous and of one operand kind:

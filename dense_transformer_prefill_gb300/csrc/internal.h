@@ -32,9 +32,10 @@ unsigned read_clear_attn_errors();
 
 // ----------------------------------------------------------------------------- timing
 // Brackets one kernel launch with the timer events of `kind` (if enabled) and
-// counts the launch.
+// counts the launch.  counts = false brackets a span that is not one kernel
+// (a whole prompt's pass, a copy): timed, not counted as a launch.
 struct LaunchScope {
-    LaunchScope(int kind, cudaStream_t s);
+    LaunchScope(int kind, cudaStream_t s, bool counts = true);
     ~LaunchScope();
     int kind;
     cudaStream_t stream;

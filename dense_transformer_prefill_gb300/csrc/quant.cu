@@ -6,7 +6,7 @@
 // (per token) and of the weight (per output channel) factor out of every dot
 // product, so the tcgen05 kind::f8f6f4 GEMM applies them in its epilogue.
 //
-//   rmsnorm_e4m3   forward.rs `e.rms_norm`, written straight as e4m3 codes
+//   rmsnorm_e4m3   forward.rs, the RMSNorm step, written straight as e4m3 codes
 //   quant_rows     bf16 rows (attention output, SwiGLU act) -> e4m3 codes
 //   pack_e4m3      float32 weight rows -> e4m3 codes (+ the gate/up interleave)
 #include <cuda_fp8.h>

@@ -67,10 +67,12 @@ __device__ float block_sum(float v, float* red) {
 }
 
 // ----------------------------------------------------------------------------- embedding
-// forward.rs: `x = self.embed_tokens(e, tokens)` -- row t of x is row tokens[t]
+// forward.rs, Model::forward, the embedding step -- row t of x is row tokens[t]
 // of the embedding table.  An id >= V raises the token-range error bit and
 // leaves a zero row.  With xb, also the bf16 copy of the row and its sum of
 // squares ss[t] (the first layer's fused RMSNorm input, one partial per row).
+// A bf16 table with d % 8 == 0 moves 8 elements per thread and step (one
+// 16-byte load, two 16-byte float stores, one 16-byte bf16 store).
 template <typename Tt>
 __global__ void embed_kernel(const uint32_t* __restrict__ tokens, int V, int d,
                              const Tt* __restrict__ table, float* __restrict__ x,
@@ -83,6 +85,33 @@ __global__ void embed_kernel(const uint32_t* __restrict__ tokens, int V, int d,
     if (bad && threadIdx.x == 0) atomicOr(&g_simt_err, ERRBIT_TOKEN_RANGE);
     const Tt* src = table + (size_t)(bad ? 0 : id) * d;
     float ss = 0.f;
+    if constexpr (sizeof(Tt) == 2) {
+        if ((d & 7) == 0) {
+            for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+                const uint4 u = bad ? make_uint4(0, 0, 0, 0)
+                                    : *reinterpret_cast<const uint4*>(src + c);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[2 * j] = __uint_as_float(w[j] << 16);
+                    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+                }
+                *reinterpret_cast<float4*>(xr + c) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(xr + c + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                if (xb) {
+                    *reinterpret_cast<uint4*>(xb + (size_t)t * d + c) = u;   // already bf16
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
+                }
+            }
+            if (ss_out) {
+                ss = block_sum(ss, red);
+                if (threadIdx.x == 0) ss_out[t] = ss;
+            }
+            return;
+        }
+    }
     for (int c = threadIdx.x; c < d; c += blockDim.x) {
         const float v = bad ? 0.f : ld_elt(src, c);
         xr[c] = v;
@@ -111,7 +140,7 @@ cudaError_t launch_embed(const uint32_t* tokens, int T, int V, int d, const void
 }
 
 // ----------------------------------------------------------------------------- RMSNorm
-// forward.rs: `e.rms_norm(x, w, out, ncols, nrows, eps)` -- one block per row.
+// forward.rs, Model::forward: the row RMSNorm step (nrows rows of ncols) -- one block per row.
 template <typename To>
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                To* __restrict__ y, int cols, float eps,
@@ -226,7 +255,8 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, void* y, int y_dtype,
 
 // ----------------------------------------------------------------------------- RoPE angles
 // cos/sin of angle = pos * base^(-2i/r), computed in float64 and rounded to
-// float32 (forward.rs `rope_neox(..., rope_dim_count, ..., freq_base, 1.0)`).
+// float32 (forward.rs, the NeoX RoPE step: rope_dim_count rotated dims, base freq_base,
+// frequency scale 1).
 __device__ __forceinline__ float2 rope_cs(double pos, int i, int rope_dims, double base) {
     const double theta = pow(base, -2.0 * (double)i / (double)rope_dims);
     double sn, cs;
@@ -323,7 +353,7 @@ cudaError_t launch_qk_norm_rope(void* x, int dtype, int ld, const float* w_norm,
 }
 
 // ----------------------------------------------------------------------------- SwiGLU
-// forward.rs `ffn_act`: act = silu(gate) * up, silu(x) = x / (1 + e^-x).
+// forward.rs, the FFN activation: act = silu(gate) * up, silu(x) = x / (1 + e^-x).
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 template <typename T>
@@ -406,7 +436,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
     __shared__ float Bs[SG_BK][SG_BN + 4];
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
     const int m0 = blockIdx.y * SG_BM, n0 = blockIdx.x * SG_BN;
-    float acc[4][4] = {};
+    // Two-level sum: each run of 4 * SG_BK = 64 products is summed on its own
+    // and the runs' sums are added to acc, so rounding grows with sqrt(64) +
+    // sqrt(K / 64) rather than sqrt(K) (K reaches 12288 in the down projection).
+    float acc[4][4] = {}, part[4][4] = {};
     for (int k0 = 0; k0 < K; k0 += SG_BK) {
         for (int i = threadIdx.x; i < SG_BM * SG_BK; i += 256) {
             const int r = i / SG_BK, c = i % SG_BK;
@@ -426,9 +459,18 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < 4; ++j) part[i][j] = fmaf(a[i], b[j], part[i][j]);
         }
         __syncthreads();
+        if ((k0 / SG_BK) % 4 == 3 || k0 + SG_BK >= K) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[i][j] += part[i][j];
+                    part[i][j] = 0.f;
+                }
+        }
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -459,8 +501,8 @@ cudaError_t launch_gemm_simt(const float* x, int ldx, const float* W, void* y, i
 }
 
 // ----------------------------------------------------------------------------- SIMT attention
-// forward.rs `e.sdpa_naive(q, k, v, attn, head_dim, n_head, n_head_kv, t, t,
-// scale, true)`: one warp per (query t, head i); keys in chunks of 32 (one
+// forward.rs, Model::forward, the causal attention step over all T keys with
+// scale 1/sqrt(head_dim): one warp per (query t, head i); keys in chunks of 32 (one
 // per lane), online softmax in float32 with expf.  kv head = i / (h / g).
 // Query row t sees keys k0 .. t + q_pos0: k0 = t - tok_pos[t] for packed
 // sequences, else 0; q_pos0 > 0 when the queries follow q_pos0 earlier keys
@@ -501,8 +543,11 @@ __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __re
         const float alpha = expf(m - mn);     // m = -inf on the first chunk -> 0
         const float p = (s <= kl) ? expf(sc - mn) : 0.f;
         l = l * alpha + warp_sum(p);
+        // this chunk's sum of p v on its own, then folded into the rescaled total
+        // (a two-level sum: rounding grows with sqrt(32) + sqrt(T / 32), not sqrt(T))
+        float cacc[MAXD];
 #pragma unroll
-        for (int j = 0; j < MAXD; ++j) acc[j] *= alpha;
+        for (int j = 0; j < MAXD; ++j) cacc[j] = 0.f;
         const int nk = min(32, kl - s0 + 1);
         for (int jj = 0; jj < nk; ++jj) {
             const float pj = __shfl_sync(0xffffffffu, p, jj);
@@ -513,10 +558,12 @@ __global__ void attn_simt_kernel(const T* __restrict__ q, int ldq, const T* __re
                 if (e < hd) {
                     const float vv = VT ? ld_elt(v, (size_t)(kvh * hd + e) * ldv + sk)
                                         : ld_elt(v, (size_t)sk * ldv + (size_t)kvh * hd + e);
-                    acc[j] = fmaf(pj, vv, acc[j]);
+                    cacc[j] = fmaf(pj, vv, cacc[j]);
                 }
             }
         }
+#pragma unroll
+        for (int j = 0; j < MAXD; ++j) acc[j] = fmaf(acc[j], alpha, cacc[j]);
         m = mn;
     }
     const float inv = 1.0f / l;

@@ -69,8 +69,12 @@ enum { DTP_F32 = 0, DTP_BF16 = 1, DTP_TF32 = 2 };
  *   DTP_PREC_F32:  float32 everywhere (SIMT kernels; the pages' "all f32" stage).
  *   DTP_PREC_TF32: every GEMM on tcgen05 tensor cores with tf32 operands (the
  *                  weights and each GEMM input rounded to tf32) and float32
- *                  accumulation; residual stream, norms, QK-norm/RoPE, attention
- *                  (float32 SIMT kernel), SwiGLU and logits in float32.
+ *                  accumulation; attention on the tcgen05 flash-attention kernel
+ *                  (kind::tf32: q/k/v and P rounded to tf32, float32 scores,
+ *                  softmax and output; packed sequences and head_dim other than
+ *                  64 / 128 use the float32 SIMT kernel on the same tf32 values);
+ *                  residual stream, norms, QK-norm/RoPE, SwiGLU and logits in
+ *                  float32.
  *   DTP_PREC_BF16: bf16 GEMM/attention operands, float32 accumulation, float32
  *                  residual stream, norms, softmax and logits (tcgen05 tensor cores).
  *   DTP_PREC_E4M3: quantised weights and GEMM inputs: every GEMM operand is OCP
@@ -287,7 +291,8 @@ const char* dtp_last_error(void);
  * Per-op entry points (the steps of forward.rs `Model::forward`)
  * ------------------------------------------------------------------------------------ */
 
-/* rms_norm (forward.rs: `e.rms_norm(x, w, out, ncols, nrows, eps)`):
+/* RMSNorm (forward.rs, Model::forward: the engine's row RMSNorm step over
+ * nrows rows of ncols values with a weight vector and eps):
  * y[r, c] = x[r, c] / sqrt(mean_c(x[r, :]^2) + eps) * w[c].
  * x device float32 [rows, cols]; w device float32 [cols]; y device [rows, cols]
  * of y_dtype (DTP_F32, DTP_BF16 or DTP_TF32; bf16 / tf32 rounded to nearest
@@ -295,9 +300,10 @@ const char* dtp_last_error(void);
 int dtp_rms_norm(const float* x, const float* w, void* y, int y_dtype, int rows, int cols,
                  float eps, dtp_stream_t stream);
 
-/* Per-head QK-RMSNorm then NeoX RoPE, in place (forward.rs: the q/k `rms_norm`
- * with ncols = head_dim, nrows = heads*T, then `e.rope_neox(x, pos, head_dim,
- * rope_dim_count, heads, T, freq_base, 1.0)`).
+/* Per-head QK-RMSNorm then NeoX RoPE, in place (forward.rs, Model::forward:
+ * the QK-norm step, an RMSNorm over rows of head_dim values, heads*T rows,
+ * then the NeoX rotation of rope_dim_count dims per head at the token
+ * positions, base freq_base, frequency scale 1).
  * x device [T, n_heads*head_dim] of dtype (DTP_F32 or DTP_BF16);
  * w_norm device float32 [head_dim], or NULL to apply RoPE only;
  * pos device int32 [T] positions, or NULL for 0..T-1.
@@ -311,8 +317,8 @@ int dtp_qk_norm_rope_neox(void* x, int dtype, const float* w_norm, const int32_t
 /* Device workspace dtp_sdpa_causal_gqa needs (0 for DTP_F32). */
 size_t dtp_sdpa_workspace_size(int T, int n_head_kv, int head_dim, int dtype);
 
-/* Causal grouped-query attention (forward.rs: `e.sdpa_naive(q, k, v, attn,
- * head_dim, n_head, n_head_kv, T, T, scale, true)`):
+/* Causal grouped-query attention (forward.rs, Model::forward: the attention
+ * step, causal, with as many keys as queries and the caller's scale):
  * out[t, i] = sum_{s<=t} softmax_s(scale * q[t,i].k[s,j]) v[s,j],
  * j = i / (n_head / n_head_kv).
  * q, out device [T, n_head*head_dim]; k, v device [T, n_head_kv*head_dim];
@@ -349,13 +355,15 @@ int dtp_sdpa_causal_gqa_noalloc(const void* q, const void* k, const void* v, voi
                                 int n_head, int n_head_kv, int head_dim, float scale,
                                 dtp_stream_t stream);
 
-/* SwiGLU (forward.rs `ffn_act`; the T-parallel page's `silu_mul`):
+/* SwiGLU (forward.rs, Model::forward: the FFN activation of the dense arm;
+ * the T-parallel page names the same step silu_mul):
  * out[i] = silu(gate[i]) * up[i], silu(x) = x / (1 + e^-x); n elements of
  * dtype, arithmetic in float32.  out may alias gate or up. */
 int dtp_swiglu(const void* gate, const void* up, void* out, int dtype, size_t n,
                dtp_stream_t stream);
 
-/* Linear (forward.rs `e.matmul(&w, &x, t)`): y[M, N] = x[M, K] W[N, K]^T
+/* Linear (forward.rs, Model::forward: a projection matmul, plus the residual
+ * add when a residual is given): y[M, N] = x[M, K] W[N, K]^T
  * (+ residual[M, N]).
  * x, W device, both of dtype: DTP_F32 -> float32 SIMT kernel; DTP_BF16 ->
  * tcgen05 tensor cores with float32 accumulation (K % 8 == 0); DTP_TF32 ->
@@ -395,8 +403,8 @@ int dtp_linear_e4m3(const uint8_t* xq, const float* x_scale, const uint8_t* wq,
                     dtp_stream_t stream);
 
 /* Fused QKV projection with per-head QK-RMSNorm and NeoX RoPE: the bf16 path's
- * first GEMM of a layer (forward.rs: the wq/wk/wv `e.matmul`s, the q/k
- * `rms_norm` over head_dim rows and `e.rope_neox`, as one tcgen05 GEMM whose
+ * first GEMM of a layer (forward.rs, Model::forward: the three Q/K/V
+ * projections, the QK-norm over head_dim rows and the NeoX rotation, as one tcgen05 GEMM whose
  * epilogue normalises and rotates each head at positions 0..T-1).
  *   h      device bf16 [T, d] (the normed layer input)
  *   w_qkv  device bf16 [(n_head + 2 n_head_kv) * head_dim, d]: Wq rows, then Wk, then Wv
@@ -416,7 +424,7 @@ int dtp_qkv_norm_rope(const void* h, const void* w_qkv, const float* q_norm, con
                       void* workspace, size_t ws_bytes, dtp_stream_t stream);
 
 /* Fused gate/up projection and SwiGLU: the bf16 path's FFN GEMM (forward.rs:
- * the ffn_gate / ffn_up `e.matmul`s and `ffn_act`).
+ * the gate and up projections and the FFN activation).
  *   z      device bf16 [T, d]
  *   w_gu   device bf16 [2*n_ff, d]: gate and up rows interleaved in blocks of 64
  *          (rows 128b..128b+63 = gate rows 64b..64b+63, rows 128b+64..128b+127 =
@@ -442,7 +450,11 @@ int dtp_selftest_wait_timeout(dtp_stream_t stream);
 enum {
     DTP_K_EMBED = 0, DTP_K_RMSNORM = 1, DTP_K_GEMM_QKV = 2, DTP_K_ATTN = 3, DTP_K_GEMM_O = 4,
     DTP_K_GEMM_GATEUP = 5, DTP_K_GEMM_DOWN = 6, DTP_K_GEMM_LMHEAD = 7, DTP_K_OTHER = 8,
-    DTP_K_COUNT = 9
+    /* spans of dtp_fwd_prefill_host_batch, not single kernels (not counted by
+     * dtp_launch_count): one prompt's whole pass on the caller's stream, and
+     * one prompt's logits copy on the library's copy stream */
+    DTP_K_PROMPT = 9, DTP_K_D2H = 10,
+    DTP_K_COUNT = 11
 };
 
 /* Start recording a CUDA event pair around each launch of every kernel kind
@@ -456,6 +468,12 @@ int dtp_timer_disable(void);
 /* After the recorded work has completed: number of recorded launches of
  * `kind` and their summed duration in milliseconds. */
 int dtp_timer_read(int kind, int* count, float* total_ms);
+
+/* After the recorded work has completed: start and end of each recorded launch
+ * (or span) of `kind`, in milliseconds after the start of the first recorded
+ * launch of `ref_kind` (negative if earlier), for the first `cap` of them;
+ * *count = the number recorded.  start_ms / end_ms: host float [cap]. */
+int dtp_timer_spans(int kind, int ref_kind, int cap, float* start_ms, float* end_ms, int* count);
 
 /* Launch counter: kernels this library has launched on the calling process
  * since the last reset (every kernel of every entry point). */

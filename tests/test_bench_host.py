@@ -33,3 +33,22 @@ def test_reference_arm_prints_one_complete_line():
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     # the time per step is the workload's tokens at the reported rate
     assert abs(d["ms_per_step"] - 1000.0 * d["config"]["T"] / d["value"]) < 1e-6 * d["ms_per_step"]
+    assert d["ms_per_step_kind"].startswith("extrapolated")
+    assert cb["extrapolated_step_s"] > 0 and 0 < cb["sample_s"]
+
+
+def test_span_summary_arithmetic():
+    """The e2e diagnostic's overlap bookkeeping on hand-made spans: passes of
+    10 ms back to back with 2 ms gaps, copies of 6 ms starting 1 ms after
+    each pass ends."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    fwd = [(0.0, 10.0), (12.0, 22.0), (24.0, 34.0)]
+    cpy = [(11.0, 17.0), (23.0, 29.0), (35.0, 41.0)]
+    s = bench.span_summary(fwd, cpy)
+    assert s["prompts"] == 3 and s["span_ms"] == 41.0
+    assert s["forward_ms_mean"] == 10.0 and s["copy_ms_max"] == 6.0
+    assert s["compute_idle_ms_total"] == 4.0
+    assert s["copy_start_after_ready_ms_mean"] == 1.0
+    assert s["copy_overlapped_with_next_forward_ms_total"] == 10.0   # 5 + 5

@@ -327,6 +327,52 @@ def test_qkv_norm_rope_fused(dtp, T, d, nh, nkv, hd, r):
     assert not vt[:, T:].any()                       # padding columns untouched
 
 
+@pytest.mark.parametrize("hd,r", [(128, 64), (64, 64), (128, 128)])
+def test_qkv_epilogue_rope_position_and_pair_indexing_bit_exact(dtp, hd, r):
+    """The forward pass's own RoPE (the fused QKV epilogue, T = 4096): every token
+    feeds the same q/k row, whose first r/2 dims are 1 and the rest of the
+    rotated half 0, so after the QK-norm pair (i, i + r/2) holds c (cos, sin)(pos *
+    theta_i), c = 1 / rms(row).  From the bf16 outputs alone, the integer
+    position that best explains each row's r/2 angles must be the row's own
+    index, every pair's angle must match it, and dims >= r must not rotate."""
+    T, d, nh, nkv = 4096, 64, 2, 1
+    half, base = r // 2, 1e4
+    nq, nk = nh * hd, nkv * hd
+    pattern = np.zeros(hd)
+    pattern[:half] = 1.0
+    pattern[r:] = np.linspace(0.5, 1.5, hd - r)        # pass-through dims
+    W = np.zeros((nq + 2 * nk, d), np.float32)
+    for head in range(nh + nkv):                        # q heads, then the k head
+        W[head * hd:(head + 1) * hd, 0] = pattern
+    W[nq + nk:, 0] = 1.0                                # v: untouched by the epilogue's RoPE
+    h = np.zeros((T, d), np.float32)
+    h[:, 0] = 1.0                                       # every token: q = k = pattern
+    q = torch.empty((T, nq), dtype=torch.bfloat16, device=dev)
+    k = torch.empty((T, nk), dtype=torch.bfloat16, device=dev)
+    vt = torch.zeros((nk, T), dtype=torch.bfloat16, device=dev)
+    ones = t32(np.ones(hd, np.float32))
+    dtp.qkv_norm_rope(t32(h).bfloat16(), t32(W).bfloat16(), ones, ones, q, k, vt, nh, nkv, hd,
+                      r, base, 1e-6)
+    torch.cuda.synchronize()
+    dtp.check()
+    theta = base ** (-2.0 * np.arange(half) / r)
+    cand = np.exp(1j * np.arange(T)[:, None] * theta[None, :])       # [position, pair]
+    rows = np.concatenate([q.float().cpu().numpy().reshape(T, nh, hd),
+                           k.float().cpu().numpy().reshape(T, nkv, hd)], axis=1)
+    for head in range(nh + nkv):
+        y = rows[:, head].astype(np.float64)
+        ang = np.arctan2(y[:, half:r], y[:, :half])                    # [row, pair]
+        score = np.real(np.exp(1j * ang) @ cand.conj().T)               # [row, position]
+        assert np.array_equal(np.argmax(score, axis=1), np.arange(T)), head
+        err = np.angle(np.exp(1j * (ang - np.arange(T)[:, None] * theta[None, :])))
+        assert np.abs(err).max() <= 2e-2, (head, np.abs(err).max())    # bf16: ~2^-8 rad
+        np.testing.assert_allclose(np.hypot(y[:, half:r], y[:, :half]),
+                                   1 / np.sqrt(np.mean(pattern ** 2) + 1e-6), rtol=2 ** -7)
+        if r < hd:                                     # scaled by the norm only, never rotated
+            ratio = y[:, r:] / pattern[r:]
+            np.testing.assert_allclose(ratio, ratio[:, :1].repeat(hd - r, 1), rtol=2 ** -7)
+
+
 @pytest.mark.parametrize("T,d,F", [(1, 64, 64), (200, 512, 1536), (513, 1024, 3072),
                                    (1024, 256, 2560)])   # 8 x 20 tiles: more than SMs
 def test_gate_up_swiglu_fused(dtp, T, d, F):
