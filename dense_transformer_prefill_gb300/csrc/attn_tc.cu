@@ -15,8 +15,11 @@
 //   warps 2-5   softmax of head 0; warps 6-9 softmax of head 1: TMEM lane =
 //               query row; scores scaled into log2 units, running max kept
 //               unless it grows by more than 8 (then O is rescaled in TMEM),
-//               P = 2^(s - m) rounded to bf16 into 128-byte-swizzled shared
+//               P = 2^(s - m) rounded to f16 into 128-byte-swizzled shared
 //               memory, row sums in float32
+// Q K^T runs on bf16 operands; P V on f16 operands (P <= 2^8 under the
+// rescale rule, and v^T holds f16 copies of the bf16 values, which f16
+// represents exactly in its range), so P keeps 11 significant bits, not 8.
 // The same kernel runs on float32 operands holding tf32 values (F32: kind::tf32,
 // 32-key tiles so that both heads' float32 Q tiles fit in shared memory, P
 // rounded to tf32, float32 output).
@@ -117,7 +120,7 @@ __device__ __forceinline__ void row_max_bf16(uint32_t tS, int row, int dof, floa
     }
 }
 
-// P = 2^(s*sl2 - m_ref) of this thread's row, rounded to bf16 into the row's
+// P = 2^(s*sl2 - m_ref) of this thread's row, rounded to f16 into the row's
 // 128-byte-swizzled shared-memory slots; rs += sum(P).  The scale-and-shift and
 // the row sum run on packed float pairs (two lanes of work per instruction).
 template <bool DIAG, int BKV>
@@ -149,10 +152,10 @@ __device__ __forceinline__ void row_exp_bf16(uint32_t tS, uint8_t* Prow, int sw,
                 e[t + 1] = ev.y;
             }
             uint4 u;
-            u.x = ptx::pack_bf16x2(e[0], e[1]);
-            u.y = ptx::pack_bf16x2(e[2], e[3]);
-            u.z = ptx::pack_bf16x2(e[4], e[5]);
-            u.w = ptx::pack_bf16x2(e[6], e[7]);
+            u.x = ptx::pack_f16x2(e[0], e[1]);
+            u.y = ptx::pack_f16x2(e[2], e[3]);
+            u.z = ptx::pack_f16x2(e[4], e[5]);
+            u.w = ptx::pack_f16x2(e[6], e[7]);
             const int chunk_all = (c >> 3) + c8;          // 16-byte chunk index 0..15
             const int atom = chunk_all >> 3, chunk = chunk_all & 7;
             *reinterpret_cast<uint4*>(Prow + atom * BQ * 128 + ((chunk ^ sw) << 4)) = u;
@@ -344,7 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
             const uint32_t idS = F32 ? ptx::idesc_tf32_f32(BQ, BKV) : ptx::idesc_bf16_f32(BQ, BKV);
-            const uint32_t idO = F32 ? ptx::idesc_tf32_f32(BQ, HD) : ptx::idesc_bf16_f32(BQ, HD);
+            // P V^T: f16 A and B (the kind::f16 MMA reads the operand types from
+            // the descriptor; both operands of one MMA share a type)
+            const uint32_t idO = F32 ? ptx::idesc_tf32_f32(BQ, HD) : ptx::idesc_f16_f32(BQ, HD);
             auto mma = [&](uint32_t d, uint64_t da, uint64_t db, uint32_t id, uint32_t acc) {
                 if constexpr (F32) ptx::umma_tf32_ss(d, da, db, id, acc);
                 else ptx::umma_bf16_ss(d, da, db, id, acc);
@@ -587,6 +592,8 @@ cudaError_t launch_attn(const void* q, long long ldq, int q_head_stride, const v
     using C = ACfg<128, F32>;     // element geometry does not depend on HD
     const CUtensorMapDataType dt =
         F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType dtv =
+        F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tq, tk, tv;
     const int hd = head_dim;
     // keys: T rows, or p0 + T rows of a KV state (the map ends there, so keys past
@@ -596,7 +603,7 @@ cudaError_t launch_attn(const void* q, long long ldq, int q_head_stride, const v
                       C::AE) ||
         !make_tmap_2d(&tk, k, dt, C::EB, kv_len, (uint64_t)n_head_kv * hd, (uint64_t)ldk, C::BKV,
                       C::AE) ||
-        !make_tmap_2d(&tv, vt, dt, C::EB, (uint64_t)n_head_kv * hd, (uint64_t)vt_cols,
+        !make_tmap_2d(&tv, vt, dtv, C::EB, (uint64_t)n_head_kv * hd, (uint64_t)vt_cols,
                       (uint64_t)ldvt, hd, C::AE))
         return cudaErrorInvalidValue;
     AParams p;
@@ -623,7 +630,7 @@ cudaError_t launch_attn(const void* q, long long ldq, int q_head_stride, const v
 }  // namespace
 
 cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
-                           const __nv_bfloat16* vt, long long ldvt, __nv_bfloat16* out, int T,
+                           const __half* vt, long long ldvt, __nv_bfloat16* out, int T,
                            int n_head, int n_head_kv, int head_dim, float scale, cudaStream_t s) {
     AttnVarlen none;
     return launch_attn_tc_varlen(q, k, vt, ldvt, T, out, T, n_head, n_head_kv, head_dim, scale,
@@ -631,7 +638,7 @@ cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
 }
 
 cudaError_t launch_attn_tc_varlen(const __nv_bfloat16* q, const __nv_bfloat16* k,
-                                  const __nv_bfloat16* vt, long long ldvt, long long vt_cols,
+                                  const __half* vt, long long ldvt, long long vt_cols,
                                   __nv_bfloat16* out, int T, int n_head, int n_head_kv,
                                   int head_dim, float scale, const AttnVarlen& vl,
                                   cudaStream_t s) {

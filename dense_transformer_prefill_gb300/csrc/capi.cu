@@ -458,7 +458,7 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
     bf* gate = c->attn_gate ? (bf*)(ws + W.gate) : nullptr;
     bf* q = (bf*)(ws + W.q);
     bf* k = (bf*)(ws + W.k);
-    bf* vt = (bf*)(ws + W.vt);
+    __half* vt = (__half*)(ws + W.vt);      // f16 copies of bf16(v), key index contiguous
     bf* attn = (bf*)(ws + W.attn);
     bf* act = (bf*)(ws + W.act);
     float2* rope = (float2*)(ws + W.rope);
@@ -539,10 +539,10 @@ static int fwd_bf16(const dtp_config* c, const uint8_t* P, const PackedLayout& L
         // with a KV cache the keys are written straight into it (attention reads them
         // there); a chunk writes its keys and values into the state at position p0
         bf* kl = o.k_cache ? (bf*)o.k_cache + (size_t)l * T * nk : k;
-        bf* vtl = vt;
+        __half* vtl = vt;
         if (S.base) {
             kl = (bf*)S.k(l);
-            vtl = (bf*)S.v(l);
+            vtl = (__half*)S.v(l);
         }
         e.q = q;
         e.k = kl + (size_t)S.p0 * nk;
@@ -965,6 +965,10 @@ int dtp_check(dtp_stream_t stream) {
     unsigned bits = read_clear_simt_errors() | read_clear_gemm_errors() | read_clear_attn_errors();
     if (bits & ERRBIT_TIMEOUT)
         return fail(DTP_ERR_DEVICE_TIMEOUT, "a kernel's bounded pipeline wait gave up");
+    if (bits & ERRBIT_VRANGE)
+        return fail(DTP_ERR_VALUE_RANGE,
+                    "a value v entering bf16 attention was beyond the f16 range (|v| > 65504) "
+                    "or not finite");
     if (bits & ERRBIT_SEQLENS)
         return fail(DTP_ERR_INVALID_ARG,
                     "cu_seqlens was not 0 = cu[0] <= cu[1] <= ... <= cu[n_seq] = total (no "
@@ -1049,7 +1053,7 @@ int dtp_sdpa_causal_gqa(const void* q, const void* k, const void* v, void* out, 
                                           scale, none, s));
         return DTP_OK;
     }
-    __nv_bfloat16* vt = (__nv_bfloat16*)workspace;
+    __half* vt = (__half*)workspace;
     DTP_CUDA_CHECK(launch_transpose_v((const __nv_bfloat16*)v, vt, T, n_head_kv * head_dim,
                                       (int)ldvt, s));
     DTP_CUDA_CHECK(launch_attn_tc((const __nv_bfloat16*)q, (const __nv_bfloat16*)k, vt, ldvt,
@@ -1191,7 +1195,7 @@ int dtp_qkv_norm_rope(const void* h, const void* w_qkv, const float* q_norm, con
     GemmEpiArgs e;
     e.q = (__nv_bfloat16*)q;
     e.k = (__nv_bfloat16*)k;
-    e.vt = (__nv_bfloat16*)vt;
+    e.vt = (__half*)vt;
     e.ldvt = ldvt;
     e.q_norm = q_norm;
     e.k_norm = k_norm;

@@ -187,6 +187,21 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// 32 values of one v^T column run (stride ld): v is rounded to bf16, as every
+// attention operand of the bf16 path, and stored as the f16 holding that bf16
+// value exactly (the P V^T MMA takes f16 operands).  A value beyond the f16
+// range raises ERRBIT_VRANGE.
+__device__ __forceinline__ void store_vt32(__half* dst, long long ld, const uint32_t (&r)[32]) {
+    bool over = false;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float vb = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[j])));
+        over |= !(fabsf(vb) <= 65504.0f);
+        dst[(size_t)j * ld] = __float2half_rn(vb);
+    }
+    if (over) atomicOr(&g_gemm_err, ERRBIT_VRANGE);
+}
+
 // The fused RMSNorm's row scale 1 / sqrt(mean(x^2) + eps) from the producer's
 // per-tile partial sums (summed in tile order), or 1 when the GEMM has none.
 __device__ __forceinline__ float row_rstd(const GemmEpiArgs& ea, int grow, int M) {
@@ -342,10 +357,8 @@ __device__ __forceinline__ void epi_qkv(const Params& p, uint32_t tbase, int gro
                 acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
                 if (live) {
                     const int tcol = ea.tok_vcol ? ea.tok_vcol[grow] : grow;
-                    __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        dst[(size_t)j * ea.ldvt] = __float2bfloat16_rn(f32(r[j]));
+                    __half* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
+                    store_vt32(dst, ea.ldvt, r);
                     if (ea.v_rows) {            // token-major copy (a decode KV cache)
                         float y[32];
 #pragma unroll
@@ -641,10 +654,8 @@ __device__ __forceinline__ void epi_qkv_tma(const Params& p, EpiStage& st, uint3
                 acc_ld32<SC>(p, tbase, th + c, grow, n0, r, rsc);
                 if (live) {
                     const int tcol = ea.tok_vcol ? ea.tok_vcol[grow] : grow;
-                    __nv_bfloat16* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        dst[(size_t)j * ea.ldvt] = __float2bfloat16_rn(f32(r[j]));
+                    __half* dst = ea.vt + (size_t)(vcol + c) * ea.ldvt + tcol;
+                    store_vt32(dst, ea.ldvt, r);
                     if (ea.v_rows) {
                         float y[32];
 #pragma unroll

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -23,7 +24,8 @@ void clear_error();
     } while (0)
 
 // Device error word bits (each kernel family keeps its own word).
-enum : unsigned { ERRBIT_TOKEN_RANGE = 1u, ERRBIT_TIMEOUT = 2u, ERRBIT_SEQLENS = 4u };
+enum : unsigned { ERRBIT_TOKEN_RANGE = 1u, ERRBIT_TIMEOUT = 2u, ERRBIT_SEQLENS = 4u,
+                  ERRBIT_VRANGE = 8u };
 
 // Read and clear the error words of every kernel family on the current device.
 unsigned read_clear_simt_errors();
@@ -103,7 +105,9 @@ cudaError_t launch_attn_simt(const void* q, int ldq, const void* k, int ldk, con
 cudaError_t launch_seq_meta(const int* cu_seqlens, int n_seq, int total, int* tile_start,
                             int* vcol_start, int* last_row, int* tok_pos, int* tok_vcol,
                             long long vt_cols, cudaStream_t s);
-cudaError_t launch_transpose_v(const __nv_bfloat16* v, __nv_bfloat16* vt, int T, int width,
+// v [T, width] bf16 -> vt [width, ldt] f16 (key index contiguous), each value
+// converted exactly; a |v| beyond the f16 range raises ERRBIT_VRANGE.
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, __half* vt, int T, int width,
                                int ldt, cudaStream_t s);
 // to_dtype: DTP_F32, DTP_BF16 or DTP_TF32 (float32 rounded to tf32)
 cudaError_t launch_pack_matrix(const float* src, int rows, int cols, void* dst, int to_dtype,
@@ -116,7 +120,7 @@ cudaError_t launch_copy_rows_f32(const float* src, int lds, float* dst, int ldd,
 // ----------------------------------------------------------------------------- tcgen05 GEMM
 enum GemmEpi {
     EPI_STORE = 0,    // y = acc (+ residual), y f32 or bf16
-    EPI_QKV = 1,      // q/k: per-head RMSNorm + NeoX RoPE -> bf16; v -> bf16 transposed
+    EPI_QKV = 1,      // q/k: per-head RMSNorm + NeoX RoPE -> bf16; v -> transposed f16 of bf16(v)
     EPI_SWIGLU = 2,   // gate/up interleaved in 64-column blocks -> silu(g)*u bf16
 };
 
@@ -132,7 +136,7 @@ struct GemmEpiArgs {
     // EPI_QKV
     __nv_bfloat16* q = nullptr;         // [M, n_head*hd]
     __nv_bfloat16* k = nullptr;         // [M, n_head_kv*hd]
-    __nv_bfloat16* vt = nullptr;        // [n_head_kv*hd, ldvt]
+    __half* vt = nullptr;               // [n_head_kv*hd, ldvt]: f16 copies of bf16(v)
     long long ldvt = 0;
     __nv_bfloat16* v_rows = nullptr;    // optional token-major v [M, n_head_kv*hd]
     const int* tok_pos = nullptr;       // optional per-row RoPE position (default: the row)
@@ -176,10 +180,11 @@ cudaError_t launch_gemm_tc_e4m3(const uint8_t* x, const uint8_t* W, int M, int N
 cudaError_t launch_selftest_wait(cudaStream_t s);
 
 // ----------------------------------------------------------------------------- tcgen05 attention
-// q [T, n_head*hd] bf16, k [T, n_head_kv*hd] bf16, vt [n_head_kv*hd, ldvt] bf16,
-// out [T, n_head*hd] bf16.
+// q [T, n_head*hd] bf16, k [T, n_head_kv*hd] bf16, vt [n_head_kv*hd, ldvt] f16
+// (bf16 values, exactly), out [T, n_head*hd] bf16.  S = Q K^T on bf16 operands;
+// P (f16) V^T (f16) on f16 operands.
 cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
-                           const __nv_bfloat16* vt, long long ldvt, __nv_bfloat16* out, int T,
+                           const __half* vt, long long ldvt, __nv_bfloat16* out, int T,
                            int n_head, int n_head_kv, int head_dim, float scale, cudaStream_t s);
 // Several sequences packed along the token axis (see seq_meta in simt.cu).
 struct AttnVarlen {
@@ -193,7 +198,7 @@ struct AttnVarlen {
     const int* vcol_start = nullptr;   // [n_seq]
 };
 cudaError_t launch_attn_tc_varlen(const __nv_bfloat16* q, const __nv_bfloat16* k,
-                                  const __nv_bfloat16* vt, long long ldvt, long long vt_cols,
+                                  const __half* vt, long long ldvt, long long vt_cols,
                                   __nv_bfloat16* out, int T, int n_head, int n_head_kv,
                                   int head_dim, float scale, const AttnVarlen& vl,
                                   cudaStream_t s);

@@ -19,8 +19,8 @@
 
 namespace dtp {
 
-// 8 MiB: room for v^T of n_head_kv * head_dim * round_up(T, 8) bf16 values,
-// e.g. 8 kv heads x 128 dims x 4096 tokens.
+// 8 MiB: room for v^T of n_head_kv * head_dim * round_up(T, 8) two-byte values
+// (f16 copies of the bf16 v), e.g. 8 kv heads x 128 dims x 4096 tokens.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -73,14 +73,14 @@ extern "C" int dtp_sdpa_causal_gqa_noalloc(const void* q, const void* k, const v
     if (need > kNoAllocScratchBytes)
         return fail(DTP_ERR_WORKSPACE,
                     "attention needs %zu bytes of scratch for v^T (n_head_kv*head_dim*T rounded "
-                    "up to 8, bf16) but the allocation-free variant has a fixed %zu bytes; use "
+                    "up to 8, 2 bytes each) but the allocation-free variant has a fixed %zu bytes; use "
                     "dtp_sdpa_causal_gqa with a workspace",
                     need, kNoAllocScratchBytes);
     void* scratch = nullptr;
     int rc = scratch_address(&scratch);
     if (rc) return rc;
     cudaStream_t s = (cudaStream_t)stream;
-    __nv_bfloat16* vt = (__nv_bfloat16*)scratch;
+    __half* vt = (__half*)scratch;
     DTP_CUDA_CHECK(launch_transpose_v((const __nv_bfloat16*)v, vt, T, n_head_kv * head_dim,
                                       (int)ldvt, s));
     DTP_CUDA_CHECK(launch_attn_tc((const __nv_bfloat16*)q, (const __nv_bfloat16*)k, vt, ldvt,

@@ -215,6 +215,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16 with f16 A and B (format 0), f32 D, both
+// K-major.  A and B of one MMA must have the same type.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::tf32 (A/B format 2 = tf32), f32 D, both K-major.
 // One MMA consumes K = 8 tf32 (32 bytes of each row), like K = 16 bf16.
 __host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
@@ -369,6 +376,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
 

@@ -625,11 +625,35 @@ __global__ void transpose_v_kernel(const E* __restrict__ v, int ldv, E* __restri
     }
 }
 
-cudaError_t launch_transpose_v(const __nv_bfloat16* v, __nv_bfloat16* vt, int T, int width,
+// bf16 v [T, width] -> f16 v^T [width, ldt]: each bf16 value converted exactly
+// (the bf16 attention's P V^T MMA takes f16 operands); a value beyond the f16
+// range raises ERRBIT_VRANGE.
+__global__ void transpose_v_f16_kernel(const __nv_bfloat16* __restrict__ v, int ldv,
+                                       __half* __restrict__ vt, int T, int width, int ldt) {
+    __shared__ float tile[32][33];
+    const int t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int t = t0 + i, c = c0 + threadIdx.x;
+        tile[i][threadIdx.x] = (t < T && c < width) ? __bfloat162float(v[(size_t)t * ldv + c]) : 0.f;
+    }
+    __syncthreads();
+    bool over = false;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i, t = t0 + threadIdx.x;
+        if (c < width && t < T) {
+            const float x = tile[threadIdx.x][i];
+            over |= !(fabsf(x) <= 65504.0f);
+            vt[(size_t)c * ldt + t] = __float2half_rn(x);
+        }
+    }
+    if (over) atomicOr(&g_simt_err, ERRBIT_VRANGE);
+}
+
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, __half* vt, int T, int width,
                                int ldt, cudaStream_t s) {
     LaunchScope ls(DTP_K_OTHER, s);
     dim3 grid((T + 31) / 32, (width + 31) / 32), block(32, 8);
-    transpose_v_kernel<<<grid, block, 0, s>>>(v, width, vt, T, width, ldt);
+    transpose_v_f16_kernel<<<grid, block, 0, s>>>(v, width, vt, T, width, ldt);
     return cudaGetLastError();
 }
 

@@ -57,7 +57,9 @@ enum {
     DTP_ERR_TOKEN_RANGE = -3,    /* a token id >= n_vocab                                     */
     DTP_ERR_WORKSPACE = -4,      /* workspace or packed buffer smaller than required          */
     DTP_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed                         */
-    DTP_ERR_DEVICE_TIMEOUT = -6  /* a kernel's bounded wait gave up (reported by dtp_check)   */
+    DTP_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded wait gave up (reported by dtp_check)   */
+    DTP_ERR_VALUE_RANGE = -7     /* bf16 attention met a v value outside the f16 range or not
+                                    finite (reported by dtp_check; see dtp_sdpa_causal_gqa)  */
 };
 
 /* Element type of an activation buffer.  DTP_TF32 is float32 storage whose
@@ -225,7 +227,9 @@ int dtp_fwd_prefill_varlen(const dtp_config* cfg, const void* packed, size_t pac
  * offset l * S with S the per-layer stride below,
  *   DTP_PREC_BF16 / DTP_PREC_E4M3:
  *                  K  bf16 [max_T, nk] token-major, then (256-byte aligned)
- *                  V^T bf16 [nk, ldvt], ldvt = max_T rounded up to 8
+ *                  V^T f16 [nk, ldvt], ldvt = max_T rounded up to 8: f16 copies
+ *                  of the bf16 values (exact; the attention's P V^T product takes
+ *                  f16 operands)
  *   DTP_PREC_TF32: the same with float32 elements (with a head_dim other than 64
  *                  or 128, or an odd n_head / n_head_kv, V is token-major
  *                  [max_T, nk] inside the V^T region instead)
@@ -280,7 +284,8 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
 
 /* Synchronise `stream`, then report and clear the device error words raised
  * by this library's kernels since the last call: DTP_OK,
- * DTP_ERR_TOKEN_RANGE, DTP_ERR_DEVICE_TIMEOUT, or DTP_ERR_CUDA (a sticky
+ * DTP_ERR_TOKEN_RANGE, DTP_ERR_DEVICE_TIMEOUT, DTP_ERR_VALUE_RANGE,
+ * DTP_ERR_INVALID_ARG (packed-sequence offsets), or DTP_ERR_CUDA (a sticky
  * CUDA error). */
 int dtp_check(dtp_stream_t stream);
 
@@ -323,8 +328,10 @@ size_t dtp_sdpa_workspace_size(int T, int n_head_kv, int head_dim, int dtype);
  * j = i / (n_head / n_head_kv).
  * q, out device [T, n_head*head_dim]; k, v device [T, n_head_kv*head_dim];
  * all of dtype.  DTP_F32: float32 SIMT kernel.  DTP_BF16: tcgen05 flash
- * attention (bf16 operands, float32 scores/softmax/accumulation, P rounded to
- * bf16 for the PV product).  DTP_TF32: the same on float32 buffers holding tf32
+ * attention: q k^T on bf16 operands, float32 scores/softmax/accumulation, and
+ * the PV product on f16 operands (P rounded to f16; v copied exactly into f16,
+ * so every |v| must be at most 65504 -- otherwise dtp_check reports
+ * DTP_ERR_VALUE_RANGE and the output is not meaningful).  DTP_TF32: the same on float32 buffers holding tf32
  * values (kind::tf32, P rounded to tf32, float32 output).  The tensor-core
  * kinds require head_dim 64 or 128 and an even group size n_head / n_head_kv,
  * and a workspace of dtp_sdpa_workspace_size bytes (device, 256-byte aligned). */
@@ -411,8 +418,10 @@ int dtp_linear_e4m3(const uint8_t* xq, const float* x_scale, const uint8_t* wq,
  *   q_norm, k_norm  device float32 [head_dim]
  *   q      device bf16 [T, n_head*head_dim]     (written)
  *   k      device bf16 [T, n_head_kv*head_dim]  (written)
- *   vt     device bf16 [n_head_kv*head_dim, ldvt], v transposed (written; columns
- *          T..ldvt-1 untouched); ldvt >= T, ldvt % 8 == 0
+ *   vt     device f16 [n_head_kv*head_dim, ldvt], v transposed, each value
+ *          bf16(v) held exactly in f16 (written; columns T..ldvt-1 untouched);
+ *          ldvt >= T, ldvt % 8 == 0.  A |v| beyond 65504 (the f16 range) raises
+ *          DTP_ERR_VALUE_RANGE in dtp_check.
  *   workspace  device, >= dtp_qkv_norm_rope_workspace_size(T, rope_dim_count)
  *          bytes, 16-byte aligned (the cos/sin table).
  * Requires d % 8 == 0, head_dim 64 or 128, (rope_dim_count/2) % 32 == 0 and

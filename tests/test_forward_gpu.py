@@ -25,6 +25,7 @@ import torch
 import oracle
 import synth
 from helpers import argmax_agreement_near_tie, load_model, oracle_forward, rel_l2
+from parity_record import record
 
 pytestmark = pytest.mark.gpu
 dev = torch.device("cuda")
@@ -44,6 +45,7 @@ def assert_parity(cfg, gl, gh, rl, rh):
     metrics = {"layer_rel_l2": [round(e, 6) for e in layer_err],
                "logit_rel_l2": rel_l2(gl, rl),
                "logit_max_abs": float(np.max(np.abs(gl - rl)))}
+    record(f"kernel parity {cfg.name} {cfg.precision} T={cfg.T} L={cfg.n_layer}", metrics)
     if cfg.precision == "f32":
         assert max(layer_err) <= 1e-5, metrics
         assert metrics["logit_rel_l2"] <= 1e-5, metrics
@@ -353,10 +355,11 @@ def test_chunked_prefill_state_is_the_kv_cache(dtp, prec):
         if prec == "f32":
             vs = lay[k_bytes:k_bytes + max_T * nk * 4].view(cdt).view(max_T, nk)
             assert torch.equal(vs[:T], vc[l])
-        else:               # V^T, key index contiguous
+        else:               # V^T, key index contiguous (bf16 mode: f16 copies of the bf16 v)
             ldvt = up(max_T, 8)
-            vt = lay[k_bytes:k_bytes + nk * ldvt * eb].view(cdt).view(nk, ldvt)
-            assert torch.equal(vt[:, :T].t(), vc[l])
+            vdt = torch.float16 if prec == "bf16" else cdt
+            vt = lay[k_bytes:k_bytes + nk * ldvt * eb].view(vdt).view(nk, ldvt)
+            assert torch.equal(vt[:, :T].t().float(), vc[l].float())
 
 
 def test_chunked_prefill_head_dim_128_gated(dtp):

@@ -311,7 +311,7 @@ def test_qkv_norm_rope_fused(dtp, T, d, nh, nkv, hd, r):
     q = torch.empty((T, nq), dtype=torch.bfloat16, device=dev)
     k = torch.empty((T, nk), dtype=torch.bfloat16, device=dev)
     ldvt = (T + 7) // 8 * 8
-    vt = torch.zeros((nk, ldvt), dtype=torch.bfloat16, device=dev)
+    vt = torch.zeros((nk, ldvt), dtype=torch.float16, device=dev)     # f16 copies of bf16(v)
     dtp.qkv_norm_rope(t32(h).bfloat16(), t32(W).bfloat16(), t32(qn), t32(kn), q, k, vt, nh, nkv, hd,
                       r, 1e6, 1e-6)
     torch.cuda.synchronize()
@@ -323,7 +323,9 @@ def test_qkv_norm_rope_fused(dtp, T, d, nh, nkv, hd, r):
     rv = oracle.round_bf16(qkv[:, nq + nk:])
     np.testing.assert_allclose(q.float().cpu().numpy(), rq, rtol=2 ** -7, atol=1e-5)
     np.testing.assert_allclose(k.float().cpu().numpy(), rk, rtol=2 ** -7, atol=1e-5)
-    np.testing.assert_allclose(vt.float().cpu().numpy()[:, :T].T, rv, rtol=2 ** -7, atol=1e-5)
+    vt_got = vt.float().cpu().numpy()[:, :T].T
+    np.testing.assert_allclose(vt_got, rv, rtol=2 ** -7, atol=1e-5)
+    assert np.array_equal(oracle.round_bf16(vt_got), vt_got)     # bf16 values, held exactly
     assert not vt[:, T:].any()                       # padding columns untouched
 
 
@@ -349,7 +351,7 @@ def test_qkv_epilogue_rope_position_and_pair_indexing_bit_exact(dtp, hd, r):
     h[:, 0] = 1.0                                       # every token: q = k = pattern
     q = torch.empty((T, nq), dtype=torch.bfloat16, device=dev)
     k = torch.empty((T, nk), dtype=torch.bfloat16, device=dev)
-    vt = torch.zeros((nk, T), dtype=torch.bfloat16, device=dev)
+    vt = torch.zeros((nk, T), dtype=torch.float16, device=dev)
     ones = t32(np.ones(hd, np.float32))
     dtp.qkv_norm_rope(t32(h).bfloat16(), t32(W).bfloat16(), ones, ones, q, k, vt, nh, nkv, hd,
                       r, base, 1e-6)
