@@ -242,7 +242,9 @@ def span_summary(fwd, cpy) -> dict:
             "copy_ms_max": max(c_ms) if c_ms else None,
             "compute_idle_ms_total": sum(idle),
             "copy_start_after_ready_ms_mean": statistics.mean(wait) if wait else None,
-            "copy_overlapped_with_next_forward_ms_total": sum(overlap)}
+            "copy_overlapped_with_next_forward_ms_total": sum(overlap),
+            "per_prompt_ms": [[round(b, 1), round(e, 1)] for b, e in fwd],
+            "per_copy_ms": [[round(b, 1), round(e, 1)] for b, e in cpy]}
 
 
 def l2_note(cfg) -> str:

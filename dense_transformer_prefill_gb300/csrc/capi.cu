@@ -203,14 +203,21 @@ struct Workspace {
     long long ldvt;
     size_t q8, s8;                               // e4m3 GEMM operand + row scales
     size_t ssp;                                  // bf16: fused RMSNorm partial sums [tiles][T]
-    size_t tokens, logits, logits2;              // _host staging (logits2: batch ping-pong)
+    size_t tokens, logits, logits_more;          // _host staging (logits_more: the batch's
+                                                 // further kBatchBuffers - 1 logit buffers)
     size_t tile_start, vcol_start, last_row, tok_pos, tok_vcol;   // packed sequences
     size_t total;
 };
 
+// Device logit buffers of dtp_fwd_prefill_host_batch: prompt j's pass writes
+// buffer j % kBatchBuffers, which is free again once prompt j - kBatchBuffers's
+// logits copy has landed, so a slow copy stalls the passes only after the
+// other buffers fill up.
+constexpr int kBatchBuffers = 2;
+
 // Workspace for T tokens; n_seq > 0 adds the packed-sequence schedule and pads
 // each sequence's v^T block to a multiple of 8 columns; host adds the token and
-// logit staging (a second logit buffer with batch).
+// logit staging (kBatchBuffers logit buffers with batch).
 static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_seq = 0,
                                   bool batch = false) {
     Workspace W = {};
@@ -253,7 +260,7 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_s
     if (host) {
         W.tokens = take((size_t)T * 4);
         W.logits = take((size_t)T * c->n_vocab * 4);
-        if (batch) W.logits2 = take((size_t)T * c->n_vocab * 4);
+        if (batch) W.logits_more = take((size_t)(kBatchBuffers - 1) * T * c->n_vocab * 4);
     }
     if (n_seq > 0) {
         W.tile_start = take(((size_t)n_seq + 2) * 4);
@@ -905,8 +912,10 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
     if (!k) return fail(DTP_ERR_CUDA, "could not create the copy stream");
     uint8_t* ws = (uint8_t*)workspace;
     uint32_t* tok_d = (uint32_t*)(ws + W.tokens);
-    float* buf[2] = {(float*)(ws + W.logits), (float*)(ws + W.logits2)};
     const size_t lbytes = (size_t)T * cfg->n_vocab * 4;
+    float* buf[kBatchBuffers];
+    buf[0] = (float*)(ws + W.logits);
+    for (int b = 1; b < kBatchBuffers; ++b) buf[b] = (float*)(ws + W.logits_more + (b - 1) * lbytes);
     // ready[j]: prompt j's logits are on the device; copied[b]: buffer b is free again
     std::vector<cudaEvent_t> ev;
     auto new_event = [&](cudaEvent_t* e) {
@@ -914,10 +923,10 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
         ev.push_back(*e);
         return true;
     };
-    cudaEvent_t copied[2] = {nullptr, nullptr};
+    cudaEvent_t copied[kBatchBuffers] = {};
     rc = DTP_OK;
     for (int j = 0; j < n && rc == DTP_OK; ++j) {
-        const int b = j & 1;
+        const int b = j % kBatchBuffers;
         cudaError_t e = cudaSuccess;
         if (copied[b]) e = cudaStreamWaitEvent(s, copied[b], 0);
         if (e == cudaSuccess)
@@ -953,7 +962,7 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
         copied[b] = done;
     }
     // `stream` completes only after every copy has landed
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < kBatchBuffers; ++b)
         if (copied[b]) cudaStreamWaitEvent(s, copied[b], 0);
     for (cudaEvent_t e : ev) cudaEventDestroy(e);      // released once they complete
     return rc;
