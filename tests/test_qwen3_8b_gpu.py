@@ -164,3 +164,38 @@ def test_stated_bar_8b(run8b, prec, bar):
     if bar == BARS[0]:
         record(f"stated qwen3-8b-shape {prec} rows 0..{R - 1}", m)
     assert bar_holds(prec, bar, m), {k: v for k, v in m.items() if not isinstance(v, list)}
+
+
+def test_long_sequence_rows_at_16k(dtp):
+    """The 8B shape at T = 16384, the attention sweep's longest sequence, through
+    the whole bf16 pass (128 query tiles, up to 128 key tiles per query tile):
+    layers 0 and 35 on the GPU's own 16384-row input, compared on rows spread to
+    T - 1, within one layer's bf16 rounding bound (2u, u = 2^-8)."""
+    cfg = CFG.replace(T=16384)
+    T, d = cfg.T, cfg.n_embd
+    rows = np.unique(np.concatenate([np.linspace(0, T - 1, 24).astype(int), [16256, 16300, T - 1]]))
+    m = dtp.Model(cfg)
+    for l in range(cfg.n_layer):
+        m.load_layer(l, synth.layer_weights(cfg, l))
+    m.load_globals(synth.tok_embd(cfg), synth.output_norm(cfg), synth.output_weight(cfg))
+    toks = torch.as_tensor(synth.tokens(cfg).astype(np.int32), device=dev)
+    hidden = torch.empty((cfg.n_layer + 1, T, d), dtype=torch.float32, device=dev)
+    dtp.fwd_prefill_ex(m.c, m.packed, toks, m.workspace(T), hidden=hidden)   # no logits
+    torch.cuda.synchronize()
+    dtp.check()
+    layers = (0, 35)
+    x_in = {l: hidden[l].cpu().numpy().astype(np.float64) for l in layers}
+    x_out = {l: hidden[l + 1][torch.as_tensor(rows, device=dev)].cpu().numpy().astype(np.float64)
+             for l in layers}
+    del m, hidden
+    gc.collect()
+    torch.cuda.empty_cache()
+    worst = {}
+    for l in layers:
+        lw = {k: v.astype(np.float64) for k, v in synth.layer_weights(cfg, l).items()}
+        ref = oracle.forward_layer(cfg, lw, x_in[l], np.arange(T), bf16_operands=True,
+                                   bf16_fused_norm=True, rows=rows)
+        errs = [rel_l2(x_out[l][i], ref[i]) for i in range(len(rows))]
+        worst[str(l)] = max(errs)
+        assert max(errs) <= 2 * 2.0 ** -8, (l, errs)
+    record("8b T=16384 long-range rows", {"rows": rows.tolist(), "per_layer_max": worst})
