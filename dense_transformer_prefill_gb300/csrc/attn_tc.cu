@@ -290,6 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
+    // the warp-collective TMEM allocation and the CTA barrier below are
+    // .aligned: every warp arrives converged (thread 0 ran the set-up alone)
+    __syncwarp();
     if (warp == 0) {
         ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
         ptx::tmem_relinquish();
@@ -554,6 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // Warps 0 and 1 ran their roles on one lane: converge each warp before the
+    // CTA barrier, which counts whole warps.  Without this, a GB300 probe saw
+    // the producer's lane leave the barrier while the softmax warps still ran.
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) {

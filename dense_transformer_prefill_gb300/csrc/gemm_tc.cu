@@ -720,6 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
+    // the warp-collective TMEM allocation and the barriers below are .aligned:
+    // every warp arrives converged (thread 0 ran the set-up alone)
+    __syncwarp();
     if (warp == 0) {
         if constexpr (CL == 1) {
             ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
@@ -738,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tmR);
         }
     }
+    __syncwarp();
     ptx::tc_fence_before();
     if constexpr (CL > 1)
         ptx::cluster_sync();      // the peer's barriers exist before anything arrives on them
@@ -943,6 +947,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
+    // warps 0 and 1 ran their roles on one lane: converge each warp before the
+    // CTA and cluster barriers, which count whole warps
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     // pairs: both CTAs are done with TMEM and every arrival on the other's
