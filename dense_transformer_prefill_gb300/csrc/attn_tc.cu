@@ -26,7 +26,11 @@
 // Causality: key tiles up to the one holding the tile's last query position;
 // tiles that reach past the first query position mask key > query.  Queries may
 // start at a position p0 > 0 (chunked prefill against earlier keys).
-// Query tiles are scheduled longest first.
+// Persistent: one CTA per SM walks work items (a query tile of a head pair),
+// longest first, in rounds of one item per CTA whose direction alternates;
+// TMEM, barriers and the pipeline carry over from item to item, so the next
+// item's Q/K loads and first Q K^T overlap the previous item's last softmax
+// and epilogue.
 #include <math.h>
 #include <mutex>
 
@@ -221,6 +225,57 @@ __device__ __forceinline__ void row_exp(uint32_t tS, uint8_t* Prow, int sw, int 
     }
 }
 
+// One work item: a 128-row query tile of a head pair.  Items are numbered
+// longest first (the query tile with the most key tiles first); item w -> its
+// query tile, kv head g and first query head h0, the sequence it belongs to,
+// the position of its first query and its number of key tiles.  Returns false
+// for an item beyond a packed-sequence schedule.
+struct AItem {
+    int qt, g, h0, seq_start, seq_len, vstart, qpos0, n_kv;
+};
+__device__ __forceinline__ bool attn_item(const AParams& p, int w, int bkv, AItem& it) {
+    const int G = p.n_head / p.n_head_kv, pairs = G / 2;
+    const int items_per_qt = p.n_head_kv * pairs;
+    const int tile_idx = p.n_qt - 1 - w / items_per_qt;
+    const int rem = w % items_per_qt;
+    it.g = rem / pairs;
+    it.h0 = it.g * G + 2 * (rem % pairs);
+    it.qt = tile_idx;
+    it.seq_start = 0;
+    it.seq_len = p.T;
+    it.vstart = 0;
+    it.qpos0 = p.p0;
+    int kv_len = p.kv_len;
+    if (p.n_seq > 0) {
+        if (tile_idx >= p.tile_start[p.n_seq]) return false;
+        int lo = 0, hi = p.n_seq - 1;                        // last b with tile_start[b] <= tile_idx
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.tile_start[mid] <= tile_idx) lo = mid;
+            else hi = mid - 1;
+        }
+        it.qt = tile_idx - p.tile_start[lo];
+        it.seq_start = p.cu_seqlens[lo];
+        it.seq_len = p.cu_seqlens[lo + 1] - it.seq_start;
+        it.vstart = p.vcol_start[lo];
+        it.qpos0 = 0;
+        kv_len = it.seq_len;
+    }
+    it.qpos0 += it.qt * BQ;                 // position of the tile's first query
+    // key tiles up to the one holding the tile's last query position
+    const int kv_tiles = (kv_len + bkv - 1) / bkv, need_tiles = (it.qpos0 + BQ - 1) / bkv + 1;
+    it.n_kv = kv_tiles < need_tiles ? kv_tiles : need_tiles;
+    return true;
+}
+
+// The r-th item of CTA b among `nb` persistent CTAs: rounds of nb items, the
+// direction alternating round by round (longest items spread evenly).  -1 when
+// the CTA has no r-th item.
+__device__ __forceinline__ int attn_item_index(int r, int b, int nb, int n_items) {
+    const int w = r * nb + ((r & 1) ? nb - 1 - b : b);
+    return w < n_items ? w : -1;
+}
+
 template <int HD, bool F32>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -244,36 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_full = bars + 9;      // [2]
     uint64_t* o_done = bars + 11;     // [2]
     uint64_t* drain = bars + 13;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 14);
+    uint64_t* q_empty = bars + 14;    // the item's last Q K^T is done: Q may be replaced
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 15);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = p.n_head / p.n_head_kv, pairs = G / 2;
-    const int items_per_qt = p.n_head_kv * pairs;
-    const int tile_idx = p.n_qt - 1 - (int)blockIdx.x / items_per_qt;   // longest tiles first
-    const int rem = (int)blockIdx.x % items_per_qt;
-    const int g = rem / pairs;
-    const int h0 = g * G + 2 * (rem % pairs);
-    int qt = tile_idx, seq_start = 0, seq_len = p.T, vstart = 0, qpos0 = p.p0, kv_len = p.kv_len;
-    if (p.n_seq > 0) {
-        if (tile_idx >= p.tile_start[p.n_seq]) return;      // beyond the schedule: whole CTA
-        int lo = 0, hi = p.n_seq - 1;                        // last b with tile_start[b] <= tile_idx
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.tile_start[mid] <= tile_idx) lo = mid;
-            else hi = mid - 1;
-        }
-        qt = tile_idx - p.tile_start[lo];
-        seq_start = p.cu_seqlens[lo];
-        seq_len = p.cu_seqlens[lo + 1] - seq_start;
-        vstart = p.vcol_start[lo];
-        qpos0 = 0;
-        kv_len = seq_len;
-    }
-    qpos0 += qt * BQ;                       // position of the tile's first query
-    // key tiles up to the one holding the tile's last query position
-    const int kv_tiles = (kv_len + BKV - 1) / BKV, need_tiles = (qpos0 + BQ - 1) / BKV + 1;
-    const int n_kv = kv_tiles < need_tiles ? kv_tiles : need_tiles;
+    // persistent: this CTA takes items b, then (rounds alternating direction)
+    // one per round of gridDim.x items, until they run out
+    const int n_items = p.n_qt * p.n_head_kv * (p.n_head / p.n_head_kv / 2);
+    const int b = (int)blockIdx.x, nb = (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
@@ -287,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&o_done[i], 1);
         }
         ptx::mbar_init(drain, 1);
+        ptx::mbar_init(q_empty, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -308,35 +343,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tmQ);
             ptx::tma_prefetch_desc(&tmK);
             ptx::tma_prefetch_desc(&tmV);
-            ptx::mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
-            for (int i = 0; i < 2; ++i)
-                for (int a = 0; a < HD / AE; ++a)
-                    ptx::tma_load_2d(&tmQ, q_full, sQ + i * C::Q_BYTES + a * BQ * 128,
-                                     (h0 + i) * p.q_head_stride + a * AE, seq_start + qt * BQ);
-            int k_issued = 0, v_issued[2] = {0, 0};
-            for (int j = 0; j < n_kv; ++j) {
-                if (!ptx::wait_bounded(k_empty, (j & 1) ^ 1, abort_flag, &g_attn_err, ERRBIT_TIMEOUT))
+            // loads so far (they index the barriers' phases across items)
+            int q_issued = 0, k_issued = 0, v_issued[2] = {0, 0}, kv_loads = 0;
+            for (int r = 0; !*abort_flag; ++r) {
+                const int w = attn_item_index(r, b, nb, n_items);
+                if (w < 0) break;
+                AItem it;
+                if (!attn_item(p, w, BKV, it)) continue;
+                // the previous item's last Q K^T has read Q
+                if (q_issued > 0 && !ptx::wait_bounded(q_empty, (q_issued - 1) & 1, abort_flag,
+                                                       &g_attn_err, ERRBIT_TIMEOUT))
                     break;
-                ptx::mbar_arrive_expect_tx(k_full, C::K_BYTES);
-                for (int a = 0; a < HD / AE; ++a)
-                    ptx::tma_load_2d(&tmK, k_full, sK + a * BKV * 128, g * HD + a * AE,
-                                     seq_start + j * BKV);
-                ++k_issued;
-                const int vs = j & 1;
-                if (!ptx::wait_bounded(&v_empty[vs], ((j >> 1) & 1) ^ 1, abort_flag, &g_attn_err,
-                                       ERRBIT_TIMEOUT))
-                    break;
-                ptx::mbar_arrive_expect_tx(&v_full[vs], C::V_BYTES);
-                for (int a = 0; a < BKV / AE; ++a)
-                    ptx::tma_load_2d(&tmV, &v_full[vs], sV + vs * C::V_BYTES + a * HD * 128,
-                                     vstart + j * BKV + a * AE, g * HD);
-                ++v_issued[vs];
+                ptx::mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
+                for (int i = 0; i < 2; ++i)
+                    for (int a = 0; a < HD / AE; ++a)
+                        ptx::tma_load_2d(&tmQ, q_full, sQ + i * C::Q_BYTES + a * BQ * 128,
+                                         (it.h0 + i) * p.q_head_stride + a * AE,
+                                         it.seq_start + it.qt * BQ);
+                ++q_issued;
+                for (int j = 0; j < it.n_kv; ++j) {
+                    if (!ptx::wait_bounded(k_empty, (k_issued & 1) ^ 1, abort_flag, &g_attn_err,
+                                           ERRBIT_TIMEOUT))
+                        break;
+                    ptx::mbar_arrive_expect_tx(k_full, C::K_BYTES);
+                    for (int a = 0; a < HD / AE; ++a)
+                        ptx::tma_load_2d(&tmK, k_full, sK + a * BKV * 128, it.g * HD + a * AE,
+                                         it.seq_start + j * BKV);
+                    ++k_issued;
+                    const int vs = kv_loads & 1;
+                    if (!ptx::wait_bounded(&v_empty[vs], ((kv_loads >> 1) & 1) ^ 1, abort_flag,
+                                           &g_attn_err, ERRBIT_TIMEOUT))
+                        break;
+                    ptx::mbar_arrive_expect_tx(&v_full[vs], C::V_BYTES);
+                    for (int a = 0; a < BKV / AE; ++a)
+                        ptx::tma_load_2d(&tmV, &v_full[vs], sV + vs * C::V_BYTES + a * HD * 128,
+                                         it.vstart + j * BKV + a * AE, it.g * HD);
+                    ++v_issued[vs];
+                    ++kv_loads;
+                }
             }
             if (*abort_flag) {
                 // let the loads still in flight land before the CTA can exit: the
                 // latest phase of each barrier completes when its bytes arrive
                 volatile int never = 0;
-                ptx::wait_bounded(q_full, 0, &never, &g_attn_err, ERRBIT_TIMEOUT);
+                if (q_issued)
+                    ptx::wait_bounded(q_full, (q_issued - 1) & 1, &never, &g_attn_err,
+                                      ERRBIT_TIMEOUT);
                 if (k_issued)
                     ptx::wait_bounded(k_full, (k_issued - 1) & 1, &never, &g_attn_err,
                                       ERRBIT_TIMEOUT);
@@ -383,38 +435,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto W = [&](uint64_t* b, uint32_t par) {
                 return ptx::wait_bounded(b, par, abort_flag, &g_attn_err, ERRBIT_TIMEOUT);
             };
-            bool ok = W(q_full, 0) && W(k_full, 0);
-            if (ok) {
+            // consumed so far, across items (they index the barriers' phases)
+            int items = 0, k_used = 0, kv_used = 0, tiles = 0;
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int w = attn_item_index(r, b, nb, n_items);
+                if (w < 0) break;
+                AItem it;
+                if (!attn_item(p, w, BKV, it)) continue;
+                const int n_kv = it.n_kv;
+                ok = W(q_full, items & 1) && W(k_full, k_used & 1);
+                if (!ok) break;
                 ptx::tc_fence_after();
                 issue_S(0);
                 ptx::umma_commit(&s_full[0]);
                 issue_S(1);
                 ptx::umma_commit(&s_full[1]);
                 ptx::umma_commit(k_empty);
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int vs = j & 1;
-                if (!(W(&v_full[vs], (j >> 1) & 1) && W(&p_full[0], j & 1))) break;
-                ptx::tc_fence_after();
-                issue_PV(0, vs, j);
-                ptx::umma_commit(&o_done[0]);
-                const bool more = j + 1 < n_kv;
-                if (more) {
-                    if (!W(k_full, (j + 1) & 1)) break;
+                ++k_used;
+                if (n_kv == 1) ptx::umma_commit(q_empty);    // the item's last use of Q
+                // the softmax of this item's tile 0 follows the previous item's
+                // epilogue in the same warps, so p_full(tile 0) also means that
+                // epilogue has read O: PV(0) may overwrite it
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    const int vs = kv_used & 1, t = tiles + j;
+                    if (!(W(&v_full[vs], (kv_used >> 1) & 1) && W(&p_full[0], t & 1))) {
+                        ok = false;
+                        break;
+                    }
                     ptx::tc_fence_after();
-                    issue_S(0);
-                    ptx::umma_commit(&s_full[0]);
+                    issue_PV(0, vs, j);
+                    ptx::umma_commit(&o_done[0]);
+                    const bool more = j + 1 < n_kv;
+                    if (more) {
+                        if (!W(k_full, k_used & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        issue_S(0);
+                        ptx::umma_commit(&s_full[0]);
+                    }
+                    if (!W(&p_full[1], t & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    issue_PV(1, vs, j);
+                    ptx::umma_commit(&o_done[1]);
+                    ptx::umma_commit(&v_empty[vs]);
+                    ++kv_used;
+                    if (more) {
+                        issue_S(1);
+                        ptx::umma_commit(&s_full[1]);
+                        ptx::umma_commit(k_empty);
+                        ++k_used;
+                        if (j + 2 == n_kv) ptx::umma_commit(q_empty);
+                    }
                 }
-                if (!W(&p_full[1], j & 1)) break;
-                ptx::tc_fence_after();
-                issue_PV(1, vs, j);
-                ptx::umma_commit(&o_done[1]);
-                ptx::umma_commit(&v_empty[vs]);
-                if (more) {
-                    issue_S(1);
-                    ptx::umma_commit(&s_full[1]);
-                    ptx::umma_commit(k_empty);
-                }
+                tiles += n_kv;
+                ++items;
             }
             ptx::umma_commit(drain);
             volatile int never = 0;
@@ -425,135 +505,148 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = (warp - 2) / 4;            // which head of the pair
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        const int qrel = qt * BQ + row;                      // position within the sequence
-        const int qrow = seq_start + qrel;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem_base + lane_off + C::S_COL0 + i * BKV;
         const uint32_t tO = tmem_base + lane_off + C::O_COL0 + i * HD;
         uint8_t* Prow = sP + i * C::P_BYTES + row * 128;
         const int sw = row & 7;
-        float m = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            ok = ptx::wait_bounded(&s_full[i], j & 1, abort_flag, &g_attn_err, ERRBIT_TIMEOUT);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            // P_i and O_i are free once PV_i(j-1) has completed (it precedes S_i(j)
-            // on the tensor pipe, so this wait normally returns at once)
-            if (j > 0) {
-                ok = ptx::wait_bounded(&o_done[i], (j - 1) & 1, abort_flag, &g_attn_err,
-                                       ERRBIT_TIMEOUT);
+        int tiles = 0;                           // key tiles so far, across items
+        for (int r = 0; ok; ++r) {
+            const int w = attn_item_index(r, b, nb, n_items);
+            if (w < 0) break;
+            AItem it;
+            if (!attn_item(p, w, BKV, it)) continue;
+            const int n_kv = it.n_kv, qpos0 = it.qpos0, h0 = it.h0, seq_len = it.seq_len;
+            const int qrel = it.qt * BQ + row;                   // position within the sequence
+            const int qrow = it.seq_start + qrel;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < n_kv; ++j) {
+                const int t = tiles + j;
+                ok = ptx::wait_bounded(&s_full[i], t & 1, abort_flag, &g_attn_err, ERRBIT_TIMEOUT);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-            }
-            const int dof = qpos0 - j * BKV;           // key col c hidden iff c > row + dof
-            const bool diag = dof < BKV - 1;
-            const float sl2 = p.scale_log2;
-            // Speculative single pass: P against the running max m.  A score more
-            // than 2^8 above m makes its P, and so the row sum, exceed 2^8; only
-            // then is the tile max taken, and if it does raise the row's max by more
-            // than 2^8 that row takes the new max, l and O are rescaled and the warp
-            // redoes the pass.  The first tile takes its max before the pass.
-            float rs = 0.f;
-            if (j == 0) {
-                float mx = -INFINITY;
-                if (diag) row_max<true, F32, BKV>(tS, row, dof, mx);
-                else row_max<false, F32, BKV>(tS, row, dof, mx);
-                m = mx * sl2;                   // key 0 is never masked on the first tile
-                if (diag) row_exp<true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
-                else row_exp<false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
-            } else {
-                if (diag) row_exp<true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
-                else row_exp<false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
-                const bool suspect = !(rs <= kRescaleSum);
-                if (__any_sync(0xffffffffu, suspect)) {
+                // P_i and O_i are free once PV_i(j-1) has completed (it precedes
+                // S_i(j) on the tensor pipe, so this wait normally returns at once);
+                // at j = 0 the previous item's epilogue waited for its last PV
+                if (j > 0) {
+                    ok = ptx::wait_bounded(&o_done[i], (t - 1) & 1, abort_flag, &g_attn_err,
+                                           ERRBIT_TIMEOUT);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                }
+                const int dof = qpos0 - j * BKV;           // key col c hidden iff c > row + dof
+                const bool diag = dof < BKV - 1;
+                const float sl2 = p.scale_log2;
+                // Speculative single pass: P against the running max m.  A score more
+                // than 2^8 above m makes its P, and so the row sum, exceed 2^8; only
+                // then is the tile max taken, and if it does raise the row's max by more
+                // than 2^8 that row takes the new max, l and O are rescaled and the warp
+                // redoes the pass.  The first tile takes its max before the pass.
+                float rs = 0.f;
+                if (j == 0) {
                     float mx = -INFINITY;
                     if (diag) row_max<true, F32, BKV>(tS, row, dof, mx);
                     else row_max<false, F32, BKV>(tS, row, dof, mx);
-                    const float m_tile = mx * sl2;
-                    const bool need = m_tile > m + kRescaleLog2;
-                    if (__any_sync(0xffffffffu, need)) {
-                        float alpha = 1.f;
-                        if (need) {
-                            alpha = ex2(m - m_tile);
-                            m = m_tile;
-                            l *= alpha;
-                        }
-#pragma unroll 1
-                        for (int c = 0; c < HD; c += 32) {
-                            uint32_t r[32];
-                            __syncwarp();
-                            ptx::tmem_ld32(tO + c, r);
-#pragma unroll
-                            for (int t = 0; t < 32; ++t)
-                                r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
-                            ptx::tmem_st32(tO + c, r);
-                        }
-                        rs = 0.f;
-                        if (diag) row_exp<true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
-                        else row_exp<false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
-                    }
-                }
-            }
-            l += rs;
-            // every lane's P row is visible to the tensor core before lane 0
-            // releases the warp's quarter of P_i
-            ptx::fence_proxy_async_smem();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&p_full[i]);
-        }
-        if (ok) {
-            ok = ptx::wait_bounded(&o_done[i], (n_kv - 1) & 1, abort_flag, &g_attn_err,
-                                   ERRBIT_TIMEOUT);
-            if (__all_sync(0xffffffffu, ok)) {
-                ptx::tc_fence_after();
-                const float inv = 1.0f / l;
-                const size_t obase = (size_t)qrow * p.ldo + (size_t)(h0 + i) * HD;
-                __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + obase;
-                float* orow32 = reinterpret_cast<float*>(p.out) + obase;
-#pragma unroll 1
-                for (int c = 0; c < HD; c += 32) {
-                    uint32_t r[32];
-                    __syncwarp();
-                    ptx::tmem_ld32(tO + c, r);
-                    if (F32 && qrel < seq_len && qrow < p.T) {
-#pragma unroll
-                        for (int t = 0; t < 32; t += 4)
-                            *reinterpret_cast<float4*>(orow32 + c + t) =
-                                make_float4(__uint_as_float(r[t]) * inv, __uint_as_float(r[t + 1]) * inv,
-                                            __uint_as_float(r[t + 2]) * inv,
-                                            __uint_as_float(r[t + 3]) * inv);
-                    } else if (qrel < seq_len && qrow < p.T) {
-#pragma unroll
-                        for (int t = 0; t < 32; t += 8) {
-                            float o[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(r[t + e]) * inv;
-                            if (p.gate) {      // gated attention: out *= sigmoid(gate)
-                                const uint4 gv = *reinterpret_cast<const uint4*>(
-                                    p.gate + (size_t)qrow * p.ldo + (size_t)(h0 + i) * HD + c + t);
-                                const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&gv);
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    o[e] = o[e] / (1.0f + expf(-__bfloat162float(gb[e])));
+                    m = mx * sl2;                   // key 0 is never masked on the first tile
+                    if (diag) row_exp<true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                    else row_exp<false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                } else {
+                    if (diag) row_exp<true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                    else row_exp<false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                    const bool suspect = !(rs <= kRescaleSum);
+                    if (__any_sync(0xffffffffu, suspect)) {
+                        float mx = -INFINITY;
+                        if (diag) row_max<true, F32, BKV>(tS, row, dof, mx);
+                        else row_max<false, F32, BKV>(tS, row, dof, mx);
+                        const float m_tile = mx * sl2;
+                        const bool need = m_tile > m + kRescaleLog2;
+                        if (__any_sync(0xffffffffu, need)) {
+                            float alpha = 1.f;
+                            if (need) {
+                                alpha = ex2(m - m_tile);
+                                m = m_tile;
+                                l *= alpha;
                             }
-                            uint4 u;
-                            u.x = ptx::pack_bf16x2(o[0], o[1]);
-                            u.y = ptx::pack_bf16x2(o[2], o[3]);
-                            u.z = ptx::pack_bf16x2(o[4], o[5]);
-                            u.w = ptx::pack_bf16x2(o[6], o[7]);
-                            *reinterpret_cast<uint4*>(orow + c + t) = u;
+#pragma unroll 1
+                            for (int c = 0; c < HD; c += 32) {
+                                uint32_t r[32];
+                                __syncwarp();
+                                ptx::tmem_ld32(tO + c, r);
+#pragma unroll
+                                for (int t = 0; t < 32; ++t)
+                                    r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+                                ptx::tmem_st32(tO + c, r);
+                            }
+                            rs = 0.f;
+                            if (diag) row_exp<true, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                            else row_exp<false, F32, BKV>(tS, Prow, sw, row, dof, sl2, m, rs);
+                        }
+                    }
+                }
+                l += rs;
+                // every lane's P row is visible to the tensor core before lane 0
+                // releases the warp's quarter of P_i
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&p_full[i]);
+            }
+            if (!ok) break;
+            ok = ptx::wait_bounded(&o_done[i], (tiles + n_kv - 1) & 1, abort_flag, &g_attn_err,
+                                   ERRBIT_TIMEOUT);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                {   // the epilogue: O / l, and the gate, to the output rows
+                    ptx::tc_fence_after();
+                    const float inv = 1.0f / l;
+                    const size_t obase = (size_t)qrow * p.ldo + (size_t)(h0 + i) * HD;
+                    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + obase;
+                    float* orow32 = reinterpret_cast<float*>(p.out) + obase;
+#pragma unroll 1
+                    for (int c = 0; c < HD; c += 32) {
+                        uint32_t r[32];
+                        __syncwarp();
+                        ptx::tmem_ld32(tO + c, r);
+                        if (F32 && qrel < seq_len && qrow < p.T) {
+#pragma unroll
+                            for (int t = 0; t < 32; t += 4)
+                                *reinterpret_cast<float4*>(orow32 + c + t) =
+                                    make_float4(__uint_as_float(r[t]) * inv, __uint_as_float(r[t + 1]) * inv,
+                                                __uint_as_float(r[t + 2]) * inv,
+                                                __uint_as_float(r[t + 3]) * inv);
+                        } else if (qrel < seq_len && qrow < p.T) {
+#pragma unroll
+                            for (int t = 0; t < 32; t += 8) {
+                                float o[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(r[t + e]) * inv;
+                                if (p.gate) {      // gated attention: out *= sigmoid(gate)
+                                    const uint4 gv = *reinterpret_cast<const uint4*>(
+                                        p.gate + (size_t)qrow * p.ldo + (size_t)(h0 + i) * HD + c + t);
+                                    const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&gv);
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        o[e] = o[e] / (1.0f + expf(-__bfloat162float(gb[e])));
+                                }
+                                uint4 u;
+                                u.x = ptx::pack_bf16x2(o[0], o[1]);
+                                u.y = ptx::pack_bf16x2(o[2], o[3]);
+                                u.z = ptx::pack_bf16x2(o[4], o[5]);
+                                u.w = ptx::pack_bf16x2(o[6], o[7]);
+                                *reinterpret_cast<uint4*>(orow + c + t) = u;
+                            }
                         }
                     }
                 }
             }
+            tiles += n_kv;
         }
     }
 
@@ -581,8 +674,11 @@ cudaError_t launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
+    // persistent CTAs, one per SM (the shared memory allows no second), each
+    // taking its share of the work items
     const int G = p.n_head / p.n_head_kv;
-    const int grid = p.n_qt * p.n_head_kv * (G / 2);
+    const int n_items = p.n_qt * p.n_head_kv * (G / 2);
+    const int grid = n_items < num_sms() ? n_items : num_sms();
     attn_tc_kernel<HD, F32><<<grid, kThreads, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
