@@ -33,6 +33,8 @@ import synth  # noqa: E402
 
 METRIC = "prefill tokens/s and TFLOP/s vs GB300 peak (1 GPU), logits vs CPU oracle"
 UNIT = "tokens/s"
+# device logit buffers of the end-to-end leg (2.49 GB each at the 8B shape)
+E2E_DEVICE_BUFFERS = 8
 
 
 def load_peaks() -> dict:
@@ -397,14 +399,16 @@ def main():
     e2e = None
     if not args.no_e2e:
         # one prompt per step, host to host: tokens in, the forward pass, all
-        # logits out; the batch call overlaps prompt j's logits copy with prompt
-        # j+1's forward pass (two pinned host logit buffers, used alternately)
+        # logits out; the batch call overlaps prompt j's logits copy with the next
+        # forward passes (two pinned host logit buffers, used alternately; eight
+        # device logit buffers, so a copy slowed on the host side holds the
+        # passes back only after seven more have finished)
         tok_h = [torch.as_tensor(synth.tokens(cfg, seed=2000 + 97 * rank + j).astype(np.int32))
                  .pin_memory() for j in range(args.steps)]
         log_h = [torch.empty((cfg.T, cfg.n_vocab), dtype=torch.float32).pin_memory()
                  for _ in range(2)]
-        ws_h = torch.empty(dtp.workspace_size_host_batch(m.c, cfg.T), dtype=torch.uint8,
-                           device=dev)
+        ws_h = torch.empty(dtp.workspace_size_host_batch(m.c, cfg.T, E2E_DEVICE_BUFFERS),
+                           dtype=torch.uint8, device=dev)
         outs = [log_h[j % 2] for j in range(args.steps)]
         dtp.fwd_prefill_host_batch(m.c, m.packed, tok_h[:2], log_h, ws_h)
         torch.cuda.synchronize(dev)
@@ -446,11 +450,12 @@ def main():
                "spans": e2e_spans,
                "d2h_ms_per_step_alone": d2h_ms,
                "d2h_gbs_alone": log_h[0].numel() * 4 / d2h_ms / 1e6,
+               "device_logit_buffers": E2E_DEVICE_BUFFERS,
                "h2d_bytes_per_step": int(tok_h[0].numel() * 4),
                "d2h_bytes_per_step": int(log_h[0].numel() * 4),
                "path": "dtp_fwd_prefill_host_batch: one prompt per step, pinned host tokens in, "
                        "all pinned host logits out; each prompt's logits copy overlaps the next "
-                       "prompt's forward pass"}
+                       "prompts' forward passes"}
         del log_h, outs, ws_h
 
     if rank != 0:

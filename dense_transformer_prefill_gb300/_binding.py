@@ -70,6 +70,7 @@ _SIGS = {
     "dtp_linear_e4m3": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                          c_void_p, c_void_p], c_int),
     "dtp_workspace_size_host_batch": ([ctypes.POINTER(Config), c_int], c_size_t),
+    "dtp_workspace_size_host_batch_n": ([ctypes.POINTER(Config), c_int, c_int], c_size_t),
     "dtp_fwd_prefill_host_batch": ([ctypes.POINTER(Config), c_void_p, c_size_t, c_void_p, c_int,
                                     c_int, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "dtp_kv_state_size": ([ctypes.POINTER(Config), c_int], c_size_t),
@@ -255,8 +256,12 @@ def fwd_prefill_host(c: Config, packed: torch.Tensor, tokens_host: torch.Tensor,
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def workspace_size_host_batch(c: Config, T: int) -> int:
-    return lib().dtp_workspace_size_host_batch(ctypes.byref(c), T)
+def workspace_size_host_batch(c: Config, T: int, n_buffers: int = 2) -> int:
+    """Workspace bytes for fwd_prefill_host_batch with n_buffers (2..8) device
+    logit buffers; 0 when n_buffers is out of range."""
+    if n_buffers == 2:
+        return lib().dtp_workspace_size_host_batch(ctypes.byref(c), T)
+    return lib().dtp_workspace_size_host_batch_n(ctypes.byref(c), T, n_buffers)
 
 
 def fwd_prefill_host_batch(c: Config, packed: torch.Tensor, tokens_host: list, logits_host: list,

@@ -204,22 +204,24 @@ struct Workspace {
     size_t q8, s8;                               // e4m3 GEMM operand + row scales
     size_t ssp;                                  // bf16: fused RMSNorm partial sums [tiles][T]
     size_t tokens, logits, logits_more;          // _host staging (logits_more: the batch's
-                                                 // further kBatchBuffers - 1 logit buffers)
+                                                 // further logit buffers)
     size_t tile_start, vcol_start, last_row, tok_pos, tok_vcol;   // packed sequences
     size_t total;
 };
 
-// Device logit buffers of dtp_fwd_prefill_host_batch: prompt j's pass writes
-// buffer j % kBatchBuffers, which is free again once prompt j - kBatchBuffers's
+// Device logit buffers of dtp_fwd_prefill_host_batch: with nb buffers, prompt
+// j's pass writes buffer j % nb, which is free again once prompt j - nb's
 // logits copy has landed, so a slow copy stalls the passes only after the
-// other buffers fill up.
-constexpr int kBatchBuffers = 2;
+// other nb - 1 buffers fill up.  nb is what the caller's workspace holds,
+// between 2 and kMaxBatchBuffers.
+constexpr int kMinBatchBuffers = 2;
+constexpr int kMaxBatchBuffers = 8;
 
 // Workspace for T tokens; n_seq > 0 adds the packed-sequence schedule and pads
 // each sequence's v^T block to a multiple of 8 columns; host adds the token and
-// logit staging (kBatchBuffers logit buffers with batch).
+// logit staging (batch_buffers logit buffers with a batch).
 static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_seq = 0,
-                                  bool batch = false) {
+                                  int batch_buffers = 0) {
     Workspace W = {};
     const size_t d = c->n_embd, hd = c->head_dim, nq = (size_t)c->n_head * hd,
                  nk = (size_t)c->n_head_kv * hd, F = c->n_ff;
@@ -260,7 +262,8 @@ static Workspace workspace_layout(const dtp_config* c, int T, bool host, int n_s
     if (host) {
         W.tokens = take((size_t)T * 4);
         W.logits = take((size_t)T * c->n_vocab * 4);
-        if (batch) W.logits_more = take((size_t)(kBatchBuffers - 1) * T * c->n_vocab * 4);
+        if (batch_buffers > 1)
+            W.logits_more = take((size_t)(batch_buffers - 1) * T * c->n_vocab * 4);
     }
     if (n_seq > 0) {
         W.tile_start = take(((size_t)n_seq + 2) * 4);
@@ -869,9 +872,15 @@ int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packe
     return DTP_OK;
 }
 
+size_t dtp_workspace_size_host_batch_n(const dtp_config* cfg, int T, int n_buffers) {
+    if (validate_config(cfg) != DTP_OK || T <= 0 || n_buffers < kMinBatchBuffers ||
+        n_buffers > kMaxBatchBuffers)
+        return 0;
+    return workspace_layout(cfg, T, true, 0, n_buffers).total;
+}
+
 size_t dtp_workspace_size_host_batch(const dtp_config* cfg, int T) {
-    if (validate_config(cfg) != DTP_OK || T <= 0) return 0;
-    return workspace_layout(cfg, T, true, 0, true).total;
+    return dtp_workspace_size_host_batch_n(cfg, T, kMinBatchBuffers);
 }
 
 // The library's device-to-host copy stream of the current device (created once).
@@ -903,9 +912,17 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
                 return fail(DTP_ERR_TOKEN_RANGE, "prompt %d: token %u at position %d >= n_vocab %d",
                             j, tokens_host[j][t], t, cfg->n_vocab);
     }
-    Workspace W = workspace_layout(cfg, T, true, 0, true);
+    // as many logit buffers as the workspace holds
+    int nb = kMinBatchBuffers;
+    Workspace W = workspace_layout(cfg, T, true, 0, nb);
     if (ws_bytes < W.total)
         return fail(DTP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, W.total);
+    while (nb < kMaxBatchBuffers) {
+        const Workspace W2 = workspace_layout(cfg, T, true, 0, nb + 1);
+        if (W2.total > ws_bytes) break;
+        W = W2;
+        ++nb;
+    }
     if (!aligned(workspace, 256)) return fail(DTP_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     cudaStream_t k = copy_stream();
@@ -913,9 +930,9 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
     uint8_t* ws = (uint8_t*)workspace;
     uint32_t* tok_d = (uint32_t*)(ws + W.tokens);
     const size_t lbytes = (size_t)T * cfg->n_vocab * 4;
-    float* buf[kBatchBuffers];
+    float* buf[kMaxBatchBuffers];
     buf[0] = (float*)(ws + W.logits);
-    for (int b = 1; b < kBatchBuffers; ++b) buf[b] = (float*)(ws + W.logits_more + (b - 1) * lbytes);
+    for (int b = 1; b < nb; ++b) buf[b] = (float*)(ws + W.logits_more + (b - 1) * lbytes);
     // ready[j]: prompt j's logits are on the device; copied[b]: buffer b is free again
     std::vector<cudaEvent_t> ev;
     auto new_event = [&](cudaEvent_t* e) {
@@ -923,10 +940,10 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
         ev.push_back(*e);
         return true;
     };
-    cudaEvent_t copied[kBatchBuffers] = {};
+    cudaEvent_t copied[kMaxBatchBuffers] = {};
     rc = DTP_OK;
     for (int j = 0; j < n && rc == DTP_OK; ++j) {
-        const int b = j % kBatchBuffers;
+        const int b = j % nb;
         cudaError_t e = cudaSuccess;
         if (copied[b]) e = cudaStreamWaitEvent(s, copied[b], 0);
         if (e == cudaSuccess)
@@ -962,7 +979,7 @@ int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t
         copied[b] = done;
     }
     // `stream` completes only after every copy has landed
-    for (int b = 0; b < kBatchBuffers; ++b)
+    for (int b = 0; b < nb; ++b)
         if (copied[b]) cudaStreamWaitEvent(s, copied[b], 0);
     for (cudaEvent_t e : ev) cudaEventDestroy(e);      // released once they complete
     return rc;

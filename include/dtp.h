@@ -267,16 +267,23 @@ int dtp_fwd_prefill_host(const dtp_config* cfg, const void* packed, size_t packe
 /* n prompts of T tokens each, host to host, in order: prompt j's tokens are
  * copied in, its forward pass runs on `stream`, and its logits are copied out to
  * logits_host[j] on a device-to-host stream of the library's own, so that the
- * copy of prompt j overlaps the forward pass of prompt j + 1 (two device logit
- * buffers alternate).  Everything is enqueued before the call returns; `stream`
- * completes only after the last copy has landed, so synchronising `stream`
- * makes every logits_host[j] readable.
+ * copy of prompt j overlaps the forward pass of prompt j + 1.  The passes write
+ * nb device logit buffers in turn (prompt j: buffer j % nb), and a pass waits
+ * for the copy that last used its buffer, so a slow copy holds the passes back
+ * only once the other nb - 1 buffers are full.  nb is the largest count from
+ * 2 to 8 whose workspace fits in ws_bytes.  Everything is enqueued before the
+ * call returns; `stream` completes only after the last copy has landed, so
+ * synchronising `stream` makes every logits_host[j] readable.
  *   tokens_host  n host pointers to uint32 [T] (range-checked on the host first)
  *   logits_host  n host pointers to float32 [T, n_vocab] (page-locked memory makes
  *                the copies asynchronous)
- *   workspace    >= dtp_workspace_size_host_batch(cfg, T) bytes
- * One call at a time per device: the library's copy stream is shared. */
+ *   workspace    >= dtp_workspace_size_host_batch(cfg, T) bytes (two logit
+ *                buffers); dtp_workspace_size_host_batch_n(cfg, T, nb) bytes
+ *                for nb of them (each adds T * n_vocab * 4 bytes)
+ * One call at a time per device: the library's copy stream is shared.
+ * dtp_workspace_size_host_batch_n returns 0 for nb outside 2..8. */
 size_t dtp_workspace_size_host_batch(const dtp_config* cfg, int T);
+size_t dtp_workspace_size_host_batch_n(const dtp_config* cfg, int T, int n_buffers);
 int dtp_fwd_prefill_host_batch(const dtp_config* cfg, const void* packed, size_t packed_bytes,
                                const uint32_t* const* tokens_host, int n, int T,
                                float* const* logits_host, void* workspace, size_t ws_bytes,

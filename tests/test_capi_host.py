@@ -35,6 +35,21 @@ def _cfg(dtp, name="small", **kw):
     return dtp.config_from(synth.CONFIGS[name].replace(**kw))
 
 
+def test_host_batch_workspace_buys_logit_buffers(dtp):
+    """Each logit buffer past the two of dtp_workspace_size_host_batch adds one
+    T x n_vocab float32 block (rounded up to the 256-byte alignment); counts
+    outside 2..8 size to 0."""
+    c = _cfg(dtp)
+    T = 200
+    block = (T * c.n_vocab * 4 + 255) // 256 * 256
+    two = dtp.workspace_size_host_batch(c, T)
+    assert two > dtp.workspace_size_host(c, T)
+    for nb in range(2, 9):
+        assert dtp.workspace_size_host_batch(c, T, nb) == two + (nb - 2) * block
+    assert dtp.workspace_size_host_batch(c, T, 1) == 0
+    assert dtp.workspace_size_host_batch(c, T, 9) == 0
+
+
 def test_sizes_and_config_validation(dtp):
     c = _cfg(dtp)
     assert dtp.packed_size(c) > 0 and dtp.workspace_size(c, 256) > 0

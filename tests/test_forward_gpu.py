@@ -375,17 +375,19 @@ def test_chunked_prefill_head_dim_128_gated(dtp):
     assert_parity(cfg, gl, gh, rl, rh)
 
 
-def test_host_batch_matches_single_calls(dtp):
+@pytest.mark.parametrize("n_buffers", [2, 3, 8])
+def test_host_batch_matches_single_calls(dtp, n_buffers):
     """dtp_fwd_prefill_host_batch: n prompts host to host with the logits copies
-    overlapping the next forward pass give exactly the logits of n separate
-    dtp_fwd_prefill_host calls (odd n exercises both device buffers unevenly)."""
+    overlapping the next forward passes give exactly the logits of n separate
+    dtp_fwd_prefill_host calls, with two, three or eight device logit buffers
+    (n = 5 reuses the buffers unevenly, or not at all with eight)."""
     cfg = synth.CONFIGS["small"].replace(n_layer=2)
     m = load_model(dtp, cfg)
     T, n = 200, 5
     toks = [torch.as_tensor(synth.uniform_int(7, 70 + j, T, cfg.n_vocab).astype(np.int32)).pin_memory()
             for j in range(n)]
     outs = [torch.full((T, cfg.n_vocab), float("nan")).pin_memory() for _ in range(n)]
-    ws = torch.empty(dtp.workspace_size_host_batch(m.c, T), dtype=torch.uint8, device=dev)
+    ws = torch.empty(dtp.workspace_size_host_batch(m.c, T, n_buffers), dtype=torch.uint8, device=dev)
     dtp.fwd_prefill_host_batch(m.c, m.packed, toks, outs, ws)
     torch.cuda.current_stream().synchronize()
     dtp.check()
