@@ -188,9 +188,10 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // 32 values of one v^T column run (stride ld): v is rounded to bf16, as every
-// attention operand of the bf16 path, and stored as the f16 holding that bf16
-// value exactly (the P V^T MMA takes f16 operands).  A value beyond the f16
-// range raises ERRBIT_VRANGE.
+// attention operand of the bf16 path, and stored as f16 (the P V^T MMA takes
+// f16 operands), which holds the bf16 value exactly from 2^-14 up to 65504 and
+// smaller ones on its subnormal grid.  A value beyond the f16 range raises
+// ERRBIT_VRANGE.
 __device__ __forceinline__ void store_vt32(__half* dst, long long ld, const uint32_t (&r)[32]) {
     bool over = false;
 #pragma unroll

@@ -106,7 +106,8 @@ cudaError_t launch_seq_meta(const int* cu_seqlens, int n_seq, int total, int* ti
                             int* vcol_start, int* last_row, int* tok_pos, int* tok_vcol,
                             long long vt_cols, cudaStream_t s);
 // v [T, width] bf16 -> vt [width, ldt] f16 (key index contiguous), each value
-// converted exactly; a |v| beyond the f16 range raises ERRBIT_VRANGE.
+// converted to f16 (exact from 2^-14 up to 65504); a |v| beyond the f16 range
+// raises ERRBIT_VRANGE.
 cudaError_t launch_transpose_v(const __nv_bfloat16* v, __half* vt, int T, int width,
                                int ldt, cudaStream_t s);
 // to_dtype: DTP_F32, DTP_BF16 or DTP_TF32 (float32 rounded to tf32)
@@ -181,7 +182,7 @@ cudaError_t launch_selftest_wait(cudaStream_t s);
 
 // ----------------------------------------------------------------------------- tcgen05 attention
 // q [T, n_head*hd] bf16, k [T, n_head_kv*hd] bf16, vt [n_head_kv*hd, ldvt] f16
-// (bf16 values, exactly), out [T, n_head*hd] bf16.  S = Q K^T on bf16 operands;
+// (f16 of the bf16 values), out [T, n_head*hd] bf16.  S = Q K^T on bf16 operands;
 // P (f16) V^T (f16) on f16 operands.
 cudaError_t launch_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                            const __half* vt, long long ldvt, __nv_bfloat16* out, int T,

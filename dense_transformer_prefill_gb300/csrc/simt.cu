@@ -625,9 +625,9 @@ __global__ void transpose_v_kernel(const E* __restrict__ v, int ldv, E* __restri
     }
 }
 
-// bf16 v [T, width] -> f16 v^T [width, ldt]: each bf16 value converted exactly
-// (the bf16 attention's P V^T MMA takes f16 operands); a value beyond the f16
-// range raises ERRBIT_VRANGE.
+// bf16 v [T, width] -> f16 v^T [width, ldt]: each bf16 value converted to f16
+// (exact from 2^-14 up to 65504; the bf16 attention's P V^T MMA takes f16
+// operands); a value beyond the f16 range raises ERRBIT_VRANGE.
 __global__ void transpose_v_f16_kernel(const __nv_bfloat16* __restrict__ v, int ldv,
                                        __half* __restrict__ vt, int T, int width, int ldt) {
     __shared__ float tile[32][33];

@@ -336,8 +336,10 @@ size_t dtp_sdpa_workspace_size(int T, int n_head_kv, int head_dim, int dtype);
  * q, out device [T, n_head*head_dim]; k, v device [T, n_head_kv*head_dim];
  * all of dtype.  DTP_F32: float32 SIMT kernel.  DTP_BF16: tcgen05 flash
  * attention: q k^T on bf16 operands, float32 scores/softmax/accumulation, and
- * the PV product on f16 operands (P rounded to f16; v copied exactly into f16,
- * so every |v| must be at most 65504 -- otherwise dtp_check reports
+ * the PV product on f16 operands (P rounded to f16; v converted to f16, which
+ * holds every bf16 value exactly from 2^-14 up to 65504 and rounds smaller
+ * magnitudes to its subnormal grid, an absolute error of at most 2^-25; every
+ * |v| must be at most 65504 -- otherwise dtp_check reports
  * DTP_ERR_VALUE_RANGE and the output is not meaningful).  DTP_TF32: the same on float32 buffers holding tf32
  * values (kind::tf32, P rounded to tf32, float32 output).  The tensor-core
  * kinds require head_dim 64 or 128 and an even group size n_head / n_head_kv,
@@ -426,7 +428,8 @@ int dtp_linear_e4m3(const uint8_t* xq, const float* x_scale, const uint8_t* wq,
  *   q      device bf16 [T, n_head*head_dim]     (written)
  *   k      device bf16 [T, n_head_kv*head_dim]  (written)
  *   vt     device f16 [n_head_kv*head_dim, ldvt], v transposed, each value
- *          bf16(v) held exactly in f16 (written; columns T..ldvt-1 untouched);
+ *          f16(bf16(v)): exact from 2^-14 up to 65504, smaller magnitudes on
+ *          f16's subnormal grid (written; columns T..ldvt-1 untouched);
  *          ldvt >= T, ldvt % 8 == 0.  A |v| beyond 65504 (the f16 range) raises
  *          DTP_ERR_VALUE_RANGE in dtp_check.
  *   workspace  device, >= dtp_qkv_norm_rope_workspace_size(T, rope_dim_count)

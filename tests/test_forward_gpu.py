@@ -355,11 +355,11 @@ def test_chunked_prefill_state_is_the_kv_cache(dtp, prec):
         if prec == "f32":
             vs = lay[k_bytes:k_bytes + max_T * nk * 4].view(cdt).view(max_T, nk)
             assert torch.equal(vs[:T], vc[l])
-        else:               # V^T, key index contiguous (bf16 mode: f16 copies of the bf16 v)
-            ldvt = up(max_T, 8)
+        else:               # V^T, key index contiguous (bf16 mode: f16 of the bf16 v, which
+            ldvt = up(max_T, 8)     # is the bf16 value except below f16's smallest normal)
             vdt = torch.float16 if prec == "bf16" else cdt
             vt = lay[k_bytes:k_bytes + nk * ldvt * eb].view(vdt).view(nk, ldvt)
-            assert torch.equal(vt[:, :T].t().float(), vc[l].float())
+            assert torch.equal(vt[:, :T].t(), vc[l].to(vdt))
 
 
 def test_chunked_prefill_head_dim_128_gated(dtp):

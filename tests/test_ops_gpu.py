@@ -325,7 +325,7 @@ def test_qkv_norm_rope_fused(dtp, T, d, nh, nkv, hd, r):
     np.testing.assert_allclose(k.float().cpu().numpy(), rk, rtol=2 ** -7, atol=1e-5)
     vt_got = vt.float().cpu().numpy()[:, :T].T
     np.testing.assert_allclose(vt_got, rv, rtol=2 ** -7, atol=1e-5)
-    assert np.array_equal(oracle.round_bf16(vt_got), vt_got)     # bf16 values, held exactly
+    assert np.array_equal(oracle.round_bf16(vt_got), vt_got)     # f16 of bf16 values: still bf16 values
     assert not vt[:, T:].any()                       # padding columns untouched
 
 
