@@ -18,8 +18,9 @@
 //               P = 2^(s - m) rounded to f16 into 128-byte-swizzled shared
 //               memory, row sums in float32
 // Q K^T runs on bf16 operands; P V on f16 operands (P <= 2^8 under the
-// rescale rule, and v^T holds f16 copies of the bf16 values, which f16
-// represents exactly in its range), so P keeps 11 significant bits, not 8.
+// rescale rule, and v^T holds f16 copies of the bf16 values, exact from 2^-14
+// up to the f16 range, smaller ones within 2^-25), so P keeps 11 significant
+// bits, not 8.
 // The same kernel runs on float32 operands holding tf32 values (F32: kind::tf32,
 // 32-key tiles so that both heads' float32 Q tiles fit in shared memory, P
 // rounded to tf32, float32 output).
