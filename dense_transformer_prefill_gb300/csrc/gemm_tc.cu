@@ -36,6 +36,16 @@
 
 namespace dtp {
 
+// Every wait of these kernels lets try_wait suspend the thread (up to 1 ms, or
+// until the phase completes): the producer, MMA and epilogue threads wait for
+// long stretches, and looping on short suspensions took issue slots and power
+// from the rest of the SM.  Against the short default, alternated on the 8B
+// forward (ms per step): gate/up 16.00 vs 16.42, down 9.23 vs 9.82, QKV 4.93
+// vs 5.09, O 3.97 vs 4.02; the whole step 97.5k vs 95.2k tokens/s.  (The
+// attention kernel keeps the short default: its softmax/MMA hand-offs are
+// latency-bound, and the long suspension made it 4% slower.)
+constexpr bool kSuspendWaits = true;
+
 static __device__ unsigned g_gemm_err = 0;
 
 unsigned read_clear_gemm_errors() {
@@ -54,7 +64,7 @@ __global__ void selftest_wait_kernel() {
         ptx::mbar_init(&bar, 1);
         abort_flag = 0;
         ptx::fence_mbar_init();
-        ptx::wait_bounded(&bar, 0, &abort_flag, &g_gemm_err, ERRBIT_TIMEOUT);
+        ptx::wait_bounded<kSuspendWaits>(&bar, 0, &abort_flag, &g_gemm_err, ERRBIT_TIMEOUT);
     }
 }
 
@@ -76,6 +86,7 @@ constexpr int kThreads = 192;
 constexpr int kCluster = 2;
 
 constexpr int kSmemLimit = 232448;   // dynamic shared memory one CTA may use (227 KB)
+
 
 // CL = 2: a CTA pair computes a 256 x BN tile with cta_group::2 MMAs; each CTA
 // holds its 128 A rows and half of the B rows, so a stage is smaller and the
@@ -475,7 +486,7 @@ __device__ __forceinline__ bool epi_store_tma(const Params& p, EpiStage& st, uin
             for (int j = 0; j < 32; ++j) v[32 + j] = f32(r[j]);
         }
         if (resid) {
-            const bool ok = ptx::wait_bounded(st.rbar[b], st.rphase[b], abort_flag, &g_gemm_err,
+            const bool ok = ptx::wait_bounded<kSuspendWaits>(st.rbar[b], st.rphase[b], abort_flag, &g_gemm_err,
                                               ERRBIT_TIMEOUT);
             if (!__all_sync(0xffffffffu, ok)) return false;
             st.rphase[b] ^= 1;
@@ -763,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 const int mb = tile % p.tiles_m, nb = tile / p.tiles_m;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!ptx::wait_bounded(&empty[stage], phase ^ 1, abort_flag, &g_gemm_err,
+                    if (!ptx::wait_bounded<kSuspendWaits>(&empty[stage], phase ^ 1, abort_flag, &g_gemm_err,
                                            ERRBIT_TIMEOUT))
                         goto producer_done;
                     // a stage holds 128 bytes of K per row: 64 bf16, 32 tf32, 128 e4m3
@@ -790,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the even CTA's last commits arrive on this CTA's empty barriers:
                 // see every stage released once more before the CTA may exit
                 for (int i = 0; i < C::STAGES; ++i) {
-                    if (!ptx::wait_bounded(&empty[stage], phase ^ 1, abort_flag, &g_gemm_err,
+                    if (!ptx::wait_bounded<kSuspendWaits>(&empty[stage], phase ^ 1, abort_flag, &g_gemm_err,
                                            ERRBIT_TIMEOUT))
                         break;
                     if (++stage == C::STAGES) {
@@ -811,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ph ^= 1;
                     }
                     volatile int never = 0;
-                    ptx::wait_bounded(&full[s], ph, &never, &g_gemm_err, ERRBIT_TIMEOUT);
+                    ptx::wait_bounded<kSuspendWaits>(&full[s], ph, &never, &g_gemm_err, ERRBIT_TIMEOUT);
                 }
             }
         }
@@ -827,14 +838,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                if (!ptx::wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, &g_gemm_err,
+                if (!ptx::wait_bounded<kSuspendWaits>(&tempty[acc], acc_phase ^ 1, abort_flag, &g_gemm_err,
                                        ERRBIT_TIMEOUT))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * C::ACC_STRIDE;
                 bool ok = true;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!ptx::wait_bounded(&full[stage], phase, abort_flag, &g_gemm_err,
+                    if (!ptx::wait_bounded<kSuspendWaits>(&full[stage], phase, abort_flag, &g_gemm_err,
                                            ERRBIT_TIMEOUT)) {
                         ok = false;
                         break;
@@ -882,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 ptx::umma_commit_pair(drain, 1);
             volatile int never = 0;
-            ptx::wait_bounded(drain, 0, &never, &g_gemm_err, ERRBIT_TIMEOUT);
+            ptx::wait_bounded<kSuspendWaits>(drain, 0, &never, &g_gemm_err, ERRBIT_TIMEOUT);
         }
     } else {
         // ---------------------------------------------------- epilogue warps 2..5
@@ -907,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             st.row0 = mb * BM + quarter * 32;
             // the first residual chunk of the tile loads while the main loop runs
             if (resid_tma) stage_prefetch(st, st.cnt & 1, &tmR, n0);
-            const bool ok = ptx::wait_bounded(&tfull[acc], acc_phase, abort_flag, &g_gemm_err,
+            const bool ok = ptx::wait_bounded<kSuspendWaits>(&tfull[acc], acc_phase, abort_flag, &g_gemm_err,
                                               ERRBIT_TIMEOUT);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
@@ -943,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             volatile int never = 0;
             for (int b = 0; b < 2; ++b)
                 if (st.pending[b])
-                    ptx::wait_bounded(st.rbar[b], st.rphase[b], &never, &g_gemm_err, ERRBIT_TIMEOUT);
+                    ptx::wait_bounded<kSuspendWaits>(st.rbar[b], st.rphase[b], &never, &g_gemm_err, ERRBIT_TIMEOUT);
         }
         __syncwarp();
     }

@@ -37,15 +37,32 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// One try_wait.  SUSPEND: let it suspend the thread for up to kTryWaitSuspendNs
+// (it still returns as soon as the phase completes), so that a thread waiting
+// long does not loop and take issue slots (and power) from the warps beside
+// it; without, the suspension limit is the system's own, which wakes the
+// thread sooner after the phase completes.
+constexpr uint32_t kTryWaitSuspendNs = 1000000;   // 1 ms
+
+template <bool SUSPEND = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if constexpr (SUSPEND)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(kTryWaitSuspendNs)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
@@ -54,14 +71,15 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
 // Wait until the phase of `bar` with parity `parity` has completed.  Returns
 // false (after raising `err_bits` in *err_word and *abort_flag) if that takes
 // longer than kWaitLimitNs, or if another role of the CTA already aborted.
+template <bool SUSPEND = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
                                              volatile int* abort_flag, unsigned* err_word,
                                              unsigned err_bits) {
     const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait<SUSPEND>(a, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(a, parity)) return true;
+        if (mbar_try_wait<SUSPEND>(a, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer() - t0 > kWaitLimitNs) {
